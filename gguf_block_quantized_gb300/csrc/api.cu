@@ -1,0 +1,299 @@
+// api.cu — the C ABI of libsyn (declared in include/syn.h): argument checks, dispatch to
+// the kernels, the per-(device, stream) prefill workspace and the device status words.
+//
+// Conventions follow "The GGML ecosystem, and where synapse fits": unsupported input is
+// rejected, never approximated (section 1, and the synapse table in section 7); untrusted
+// input is validated without exceptions; the matrix orientation is ggml_mul_mat's
+// (yakaai ggml documentation, examples/simple).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdlib>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "kernels.h"
+#include "syn.h"
+
+namespace {
+
+using syn::launch_act_half;
+
+std::atomic<long long> g_launches{0};
+std::atomic<int> g_gemv_max_tok{[] {
+    const char* e = std::getenv("SYN_GEMV_MAX_TOK");
+    if (e && *e) {
+        char* end = nullptr;
+        long v = std::strtol(e, &end, 10);
+        if (end && *end == 0 && v >= 0 && v < (1 << 30)) return (int)v;
+    }
+    return 8;
+}()};
+
+struct DeviceState {
+    bool init = false;
+    int sms = 0;
+    int* words = nullptr;  // [0] timeout/error word, [1] quantize range flag
+};
+
+struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_dev;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+int current_device(int* dev) {
+    return cudaGetDevice(dev) == cudaSuccess ? SYN_OK : SYN_ERR_CUDA;
+}
+
+// Per-device state: SM count, capability check, the two status words.
+int device_state(DeviceState** out) {
+    int dev;
+    if (current_device(&dev) != SYN_OK) return SYN_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& st = g_dev[dev];
+    if (!st.init) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SYN_ERR_CUDA;
+        if (major != 10 || minor != 3) return SYN_ERR_DEVICE;  // built for sm_103a only
+        int* w = nullptr;
+        if (cudaMalloc(&w, 2 * sizeof(int)) != cudaSuccess) return SYN_ERR_NOMEM;
+        if (cudaMemset(w, 0, 2 * sizeof(int)) != cudaSuccess) return SYN_ERR_CUDA;
+        if (cudaDeviceSynchronize() != cudaSuccess) return SYN_ERR_CUDA;
+        st.sms = sms;
+        st.words = w;
+        st.init = true;
+    }
+    *out = &st;
+    return SYN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+bool known_type(int t) {
+    return t == SYN_TYPE_Q8_0 || t == SYN_TYPE_Q4_K || t == SYN_TYPE_Q6_K || t == SYN_TYPE_Q8_K;
+}
+
+int64_t elems(int t) { return t == SYN_TYPE_Q8_0 ? 32 : 256; }
+int64_t bytes_of(int t) {
+    return t == SYN_TYPE_Q8_0 ? 34 : t == SYN_TYPE_Q4_K ? 144 : t == SYN_TYPE_Q6_K ? 210 : 292;
+}
+
+int check_cuda(cudaError_t e) { return e == cudaSuccess ? SYN_OK : SYN_ERR_CUDA; }
+
+// Largest shapes a single call may take (int32 index arithmetic inside the kernels stays
+// far from overflow within these limits).
+constexpr int64_t kMaxElems = int64_t(1) << 40;
+
+// Prefill workspace bytes: the fp16 activation operand.
+size_t prefill_ws_bytes(int64_t n_in, int64_t n_tok) { return (size_t)(n_in * n_tok * 2 + 256); }
+
+int workspace_for(cudaStream_t s, size_t need, void** out) {
+    int dev;
+    if (current_device(&dev) != SYN_OK) return SYN_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace& w = g_ws[{dev, s}];
+    if (w.bytes < need) {
+        if (w.ptr) {
+            if (cudaDeviceSynchronize() != cudaSuccess) return SYN_ERR_CUDA;
+            cudaFree(w.ptr);
+            w.ptr = nullptr;
+            w.bytes = 0;
+        }
+        if (cudaMalloc(&w.ptr, need) != cudaSuccess) {
+            w.ptr = nullptr;
+            return SYN_ERR_NOMEM;
+        }
+        w.bytes = need;
+    }
+    *out = w.ptr;
+    return SYN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t syn_block_elems(int type) { return known_type(type) ? elems(type) : -1; }
+
+int64_t syn_block_bytes(int type) { return known_type(type) ? bytes_of(type) : -1; }
+
+int64_t syn_row_bytes(int type, int64_t n) {
+    if (!known_type(type) || n <= 0 || n % elems(type)) return -1;
+    return n / elems(type) * bytes_of(type);
+}
+
+const char* syn_strerror(int status) {
+    switch (status) {
+    case SYN_OK: return "ok";
+    case SYN_ERR_TYPE: return "unknown or unsupported block format";
+    case SYN_ERR_SHAPE: return "bad shape (size <= 0 or not a multiple of the block size)";
+    case SYN_ERR_NULL: return "null pointer";
+    case SYN_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case SYN_ERR_RANGE: return "non-finite input or scale out of fp16 range";
+    case SYN_ERR_CUDA: return "CUDA error";
+    case SYN_ERR_TIMEOUT: return "a device-side wait timed out";
+    case SYN_ERR_NOMEM: return "out of device memory";
+    case SYN_ERR_DEVICE: return "device is not sm_103 (GB300)";
+    default: return "unknown status";
+    }
+}
+
+int64_t syn_launch_count(void) { return g_launches.load(); }
+
+int syn_set_gemv_max_tok(int n) {
+    if (n < 0) return -1;
+    return g_gemv_max_tok.exchange(n);
+}
+
+int syn_quantize(int type, const float* src, void* dst, int64_t n_rows, int64_t n_per_row, syn_stream_t stream) {
+    if (!known_type(type)) return SYN_ERR_TYPE;
+    if (n_rows < 0 || n_per_row <= 0 || n_per_row % elems(type) || n_rows * n_per_row > kMaxElems)
+        return SYN_ERR_SHAPE;
+    if (n_rows == 0) return SYN_OK;
+    if (!src || !dst) return SYN_ERR_NULL;
+    if (!aligned16(src) || !aligned16(dst)) return SYN_ERR_ALIGN;
+    DeviceState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int* range = st->words + 1;
+    if (cudaMemsetAsync(range, 0, sizeof(int), s) != cudaSuccess) return SYN_ERR_CUDA;
+    const int64_t nblocks = n_rows * (n_per_row / elems(type));
+    if (syn::launch_quantize(type, src, dst, nblocks, range, st->sms, s) != cudaSuccess) return SYN_ERR_CUDA;
+    g_launches++;
+    int flag = 0;
+    if (cudaMemcpyAsync(&flag, range, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return SYN_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SYN_ERR_CUDA;
+    return flag ? SYN_ERR_RANGE : SYN_OK;
+}
+
+int syn_dequantize(int type, const void* src, float* dst, int64_t n_rows, int64_t n_per_row, syn_stream_t stream) {
+    if (!known_type(type)) return SYN_ERR_TYPE;
+    if (n_rows < 0 || n_per_row <= 0 || n_per_row % elems(type) || n_rows * n_per_row > kMaxElems)
+        return SYN_ERR_SHAPE;
+    if (n_rows == 0) return SYN_OK;
+    if (!src || !dst) return SYN_ERR_NULL;
+    if (!aligned16(src) || !aligned16(dst)) return SYN_ERR_ALIGN;
+    DeviceState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    const int64_t nblocks = n_rows * (n_per_row / elems(type));
+    if (syn::launch_dequantize(type, src, dst, nblocks, st->sms, reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return SYN_ERR_CUDA;
+    g_launches++;
+    return SYN_OK;
+}
+
+int syn_quantize_activations(int wtype, const float* X, int64_t n_tok, int64_t n_in, int8_t* qs, float* d,
+                             int16_t* bsums, syn_stream_t stream) {
+    if (wtype != SYN_TYPE_Q8_0 && wtype != SYN_TYPE_Q4_K && wtype != SYN_TYPE_Q6_K) return SYN_ERR_TYPE;
+    const int xt = wtype == SYN_TYPE_Q8_0 ? SYN_TYPE_Q8_0 : SYN_TYPE_Q8_K;
+    if (n_tok < 0 || n_in <= 0 || n_in % elems(xt) || n_tok * n_in > kMaxElems) return SYN_ERR_SHAPE;
+    if (n_tok == 0) return SYN_OK;
+    if (!X || !qs || !d || (xt == SYN_TYPE_Q8_K && !bsums)) return SYN_ERR_NULL;
+    if (!aligned16(X) || !aligned16(qs) || !aligned16(d) || (bsums && !aligned16(bsums))) return SYN_ERR_ALIGN;
+    DeviceState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    const int64_t nblocks = n_tok * (n_in / elems(xt));
+    if (syn::launch_quantize_act(xt, X, nblocks, qs, d, xt == SYN_TYPE_Q8_K ? bsums : nullptr, st->sms,
+                                 reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SYN_ERR_CUDA;
+    g_launches++;
+    return SYN_OK;
+}
+
+int syn_reserve(int64_t max_n_in, int64_t max_n_tok, syn_stream_t stream) {
+    if (max_n_in <= 0 || max_n_tok < 0 || max_n_in * max_n_tok > kMaxElems) return SYN_ERR_SHAPE;
+    DeviceState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    void* p;
+    return workspace_for(reinterpret_cast<cudaStream_t>(stream), prefill_ws_bytes(max_n_in, max_n_tok), &p);
+}
+
+int syn_release(void) {
+    int dev;
+    if (current_device(&dev) != SYN_OK) return SYN_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return SYN_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (auto it = g_ws.begin(); it != g_ws.end();) {
+        if (it->first.first == dev) {
+            cudaFree(it->second.ptr);
+            it = g_ws.erase(it);
+        } else {
+            ++it;
+        }
+    }
+    return SYN_OK;
+}
+
+int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in, const float* X, int64_t n_tok, float* Y,
+                syn_stream_t stream) {
+    if (type != SYN_TYPE_Q8_0 && type != SYN_TYPE_Q4_K && type != SYN_TYPE_Q6_K) return SYN_ERR_TYPE;
+    if (n_out <= 0 || n_in <= 0 || n_tok < 0 || n_in % elems(type) || n_out * n_in > kMaxElems ||
+        n_tok * n_in > kMaxElems || n_tok * n_out > kMaxElems || n_out > (int64_t(1) << 31))
+        return SYN_ERR_SHAPE;
+    if (n_tok == 0) return SYN_OK;
+    if (!W || !X || !Y) return SYN_ERR_NULL;
+    if (!aligned16(W) || !aligned16(X) || !aligned16(Y)) return SYN_ERR_ALIGN;
+    DeviceState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n_tok <= g_gemv_max_tok.load()) {
+        rc = check_cuda(syn::launch_gemv(type, W, n_out, n_in, X, n_tok, Y, st->words, st->sms, s));
+        if (rc == SYN_OK) g_launches++;
+        return rc;
+    }
+    void* ws;
+    rc = workspace_for(s, prefill_ws_bytes(n_in, n_tok), &ws);
+    if (rc) return rc;
+    const int xt = type == SYN_TYPE_Q8_0 ? SYN_TYPE_Q8_0 : SYN_TYPE_Q8_K;
+    if (launch_act_half(xt, X, n_tok * (n_in / elems(xt)), ws, st->sms, s) != cudaSuccess) return SYN_ERR_CUDA;
+    g_launches++;
+    if (syn::launch_gemm(type, W, n_out, n_in, ws, n_tok, Y, st->words, st->sms, s) != cudaSuccess)
+        return SYN_ERR_CUDA;
+    g_launches++;
+    return SYN_OK;
+}
+
+int syn_block_sums(int type, const void* W, int64_t n_out, int64_t n_in, const void* Xq, int64_t n_tok, int32_t* S,
+                   syn_stream_t stream) {
+    if (type != SYN_TYPE_Q8_0 && type != SYN_TYPE_Q4_K && type != SYN_TYPE_Q6_K) return SYN_ERR_TYPE;
+    if (n_out <= 0 || n_in <= 0 || n_tok < 0 || n_in % elems(type) || n_out * n_in > kMaxElems ||
+        n_tok * n_out * (n_in / elems(type)) > kMaxElems)
+        return SYN_ERR_SHAPE;
+    if (n_tok == 0) return SYN_OK;
+    if (!W || !Xq || !S) return SYN_ERR_NULL;
+    DeviceState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    if (syn::launch_block_sums(type, W, n_out, n_in / elems(type), Xq, n_tok, S,
+                               reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SYN_ERR_CUDA;
+    g_launches++;
+    return SYN_OK;
+}
+
+int syn_device_status(int clear) {
+    DeviceState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    if (cudaDeviceSynchronize() != cudaSuccess) return SYN_ERR_CUDA;
+    int w = 0;
+    if (cudaMemcpy(&w, st->words, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SYN_ERR_CUDA;
+    if (clear && cudaMemset(st->words, 0, sizeof(int)) != cudaSuccess) return SYN_ERR_CUDA;
+    return w ? SYN_ERR_TIMEOUT : SYN_OK;
+}
+
+}  // extern "C"

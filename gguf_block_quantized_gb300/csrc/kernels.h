@@ -1,0 +1,28 @@
+// kernels.h — host-side launchers of the libsyn kernels (internal to the library).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace syn {
+
+cudaError_t launch_quantize(int type, const float* src, void* dst, int64_t n_blocks, int* range_err,
+                            int sms, cudaStream_t s);
+cudaError_t launch_dequantize(int type, const void* src, float* dst, int64_t n_blocks, int sms,
+                              cudaStream_t s);
+cudaError_t launch_quantize_act(int xtype, const float* X, int64_t n_blocks, int8_t* qs, float* d,
+                                int16_t* bsums, int sms, cudaStream_t s);
+cudaError_t launch_act_half(int xtype, const float* X, int64_t n_blocks, void* xh, int sms,
+                            cudaStream_t s);
+cudaError_t launch_block_sums(int type, const void* W, int64_t n_out, int64_t nb, const void* Xq,
+                              int64_t n_tok, int32_t* S, cudaStream_t s);
+
+// Decode product: Y = W * Xq for small n_tok (one launch).
+cudaError_t launch_gemv(int type, const void* W, int64_t n_out, int64_t n_in, const float* X,
+                        int64_t n_tok, float* Y, int* err, int sms, cudaStream_t s);
+
+// Prefill product on the tensor cores.  xh: n_tok x n_in fp16 activations (already
+// quantized and expanded).  Y is overwritten.
+cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, const void* xh,
+                        int64_t n_tok, float* Y, int* err, int sms, cudaStream_t s);
+
+}  // namespace syn

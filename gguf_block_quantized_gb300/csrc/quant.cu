@@ -1,0 +1,451 @@
+// quant.cu — quantize / dequantize kernels, the stand-alone activation step, the prefill
+// activation step (fp16 operand for the tensor cores) and the integer block sums.
+//
+// "The GGML ecosystem, and where synapse fits", section 5: block formats (format table),
+// dequantize_row_* (embedding / norm expansion) and the activation conversion to the
+// vec_dot_type ("Products: weights against quantized activations").
+#include "kernels.h"
+#include "quant_dev.cuh"
+
+namespace syn {
+
+// ---------------------------------------------------------------------------------------
+// weight / block quantize: one warp per block (Q8_0: one warp per 4 blocks)
+// ---------------------------------------------------------------------------------------
+
+__device__ __forceinline__ void st_u16(uint8_t* p, uint32_t v) {
+    *reinterpret_cast<uint16_t*>(p) = static_cast<uint16_t>(v);
+}
+
+template <int T>
+__global__ void __launch_bounds__(256) k_quantize(const float* __restrict__ src,
+                                                  uint8_t* __restrict__ dst, int64_t n_blocks,
+                                                  int* __restrict__ range_err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    bool ok_all = true;
+    if (T == SYN_Q8_0) {
+        // 4 blocks per warp step: lanes 8g..8g+7 own block 4*step+g
+        for (int64_t base = warp * 4; base < n_blocks; base += n_warps * 4) {
+            int64_t b = base + (lane >> 3);
+            int e = (lane & 7) * 4;
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            if (b < n_blocks) {
+                float4 x = *reinterpret_cast<const float4*>(src + b * 32 + e);
+                v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+            }
+            uint16_t db;
+            bool fin;
+            uint32_t q = q8_0_group(v, &db, &fin);
+            if (b < n_blocks) {
+                uint8_t* p = dst + b * 34;
+                if ((lane & 7) == 0) st_u16(p, db);
+                st_u16(p + 2 + e, q & 0xFFFF);
+                st_u16(p + 4 + e, q >> 16);
+                ok_all &= fin;
+            }
+        }
+    } else {
+        for (int64_t b = warp; b < n_blocks; b += n_warps) {
+            const float* x = src + b * 256 + lane * 8;
+            float4 x0 = *reinterpret_cast<const float4*>(x);
+            float4 x1 = *reinterpret_cast<const float4*>(x + 4);
+            float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            uint32_t w0, w1;
+            bool fin;
+            if (T == SYN_Q8_K) {
+                float d;
+                int bs;
+                q8_k_warp(v, &w0, &w1, &d, &bs, &fin);
+                uint8_t* p = dst + b * 292;
+                if (lane == 0) *reinterpret_cast<float*>(p) = d;
+                *reinterpret_cast<uint32_t*>(p + 4 + lane * 8) = w0;
+                *reinterpret_cast<uint32_t*>(p + 8 + lane * 8) = w1;
+                if ((lane & 1) == 0) st_u16(p + 260 + lane, (uint32_t)bs);
+            } else if (T == SYN_Q4_K) {
+                int sc, mn;
+                uint16_t db, dmb;
+                q4_k_warp(v, &w0, &w1, &sc, &mn, &db, &dmb, &fin);
+                uint8_t* p = dst + b * 144;
+                // codes: byte 32c+l = q[64c+l] | q[64c+32+l] << 4; lane L holds
+                // q[8L..8L+7]; lanes with (L & 4) == 0 take the high nibbles from L+4.
+                uint32_t h0 = __shfl_down_sync(0xffffffffu, w0, 4);
+                uint32_t h1 = __shfl_down_sync(0xffffffffu, w1, 4);
+                if ((lane & 4) == 0) {
+                    int c = lane >> 3, l = (lane & 3) * 8;
+                    uint2 out;
+                    out.x = w0 | (h0 << 4);
+                    out.y = w1 | (h1 << 4);
+                    *reinterpret_cast<uint2*>(p + 16 + 32 * c + l) = out;
+                }
+                // 6-bit scales and mins: sub-block j's values sit in lane 4j
+                int scj[8], mnj[8];
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    scj[j] = __shfl_sync(0xffffffffu, sc, 4 * j);
+                    mnj[j] = __shfl_sync(0xffffffffu, mn, 4 * j);
+                }
+                if (lane == 0) {
+                    uint8_t sb[12];
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        sb[j] = (uint8_t)((scj[j] & 63) | ((scj[j + 4] >> 4) << 6));
+                        sb[j + 4] = (uint8_t)((mnj[j] & 63) | ((mnj[j + 4] >> 4) << 6));
+                        sb[j + 8] = (uint8_t)((scj[j + 4] & 15) | ((mnj[j + 4] & 15) << 4));
+                    }
+                    uint4 hdr;
+                    hdr.x = (uint32_t)db | ((uint32_t)dmb << 16);
+                    hdr.y = sb[0] | (sb[1] << 8) | (sb[2] << 16) | ((uint32_t)sb[3] << 24);
+                    hdr.z = sb[4] | (sb[5] << 8) | (sb[6] << 16) | ((uint32_t)sb[7] << 24);
+                    hdr.w = sb[8] | (sb[9] << 8) | (sb[10] << 16) | ((uint32_t)sb[11] << 24);
+                    *reinterpret_cast<uint4*>(p) = hdr;
+                }
+            } else {  // Q6_K
+                int sc;
+                uint16_t db;
+                q6_k_warp(v, &w0, &w1, &sc, &db, &fin);
+                uint8_t* p = dst + b * 210;
+                // lane L: half h = L/16, quarter = (L%16)/4, l0 = 8*(L%4).  Quarter-0
+                // lanes gather quarters 1..3 (lanes +4, +8, +12) and write the planes.
+                uint32_t b0 = __shfl_down_sync(0xffffffffu, w0, 4), b1 = __shfl_down_sync(0xffffffffu, w1, 4);
+                uint32_t c0 = __shfl_down_sync(0xffffffffu, w0, 8), c1 = __shfl_down_sync(0xffffffffu, w1, 8);
+                uint32_t d0 = __shfl_down_sync(0xffffffffu, w0, 12), d1 = __shfl_down_sync(0xffffffffu, w1, 12);
+                if ((lane & 15) < 4) {
+                    int h = lane >> 4, l0 = (lane & 3) * 8;
+                    uint32_t qa[2] = {w0, w1}, qb[2] = {b0, b1}, qc[2] = {c0, c1}, qd[2] = {d0, d1};
+#pragma unroll
+                    for (int k = 0; k < 2; k++) {
+                        uint32_t lo1 = (qa[k] & 0x0F0F0F0Fu) | ((qc[k] & 0x0F0F0F0Fu) << 4);
+                        uint32_t lo2 = (qb[k] & 0x0F0F0F0Fu) | ((qd[k] & 0x0F0F0F0Fu) << 4);
+                        uint32_t hb = ((qa[k] >> 4) & 0x03030303u) | (((qb[k] >> 4) & 0x03030303u) << 2) |
+                                      (((qc[k] >> 4) & 0x03030303u) << 4) | (((qd[k] >> 4) & 0x03030303u) << 6);
+                        uint8_t* ql = p + 64 * h + l0 + 4 * k;
+                        uint8_t* qh = p + 128 + 32 * h + l0 + 4 * k;
+                        st_u16(ql, lo1 & 0xFFFF); st_u16(ql + 2, lo1 >> 16);
+                        st_u16(ql + 32, lo2 & 0xFFFF); st_u16(ql + 34, lo2 >> 16);
+                        st_u16(qh, hb & 0xFFFF); st_u16(qh + 2, hb >> 16);
+                    }
+                }
+                if ((lane & 1) == 0) p[192 + (lane >> 1)] = (uint8_t)(int8_t)sc;
+                if (lane == 0) st_u16(p + 208, db);
+            }
+            ok_all &= fin;
+        }
+    }
+    if (!__all_sync(0xffffffffu, ok_all) && lane == 0) atomicExch(range_err, 1);
+}
+
+// ---------------------------------------------------------------------------------------
+// dequantize: one warp per block (Q8_0: one warp per 4 blocks), 8 outputs per lane
+// ---------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint16_t ld_u16(const uint8_t* p) {
+    return *reinterpret_cast<const uint16_t*>(p);
+}
+
+template <int T>
+__global__ void __launch_bounds__(256) k_dequantize(const uint8_t* __restrict__ src,
+                                                    float* __restrict__ dst, int64_t n_blocks) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    if (T == SYN_Q8_0) {
+        for (int64_t base = warp * 4; base < n_blocks; base += n_warps * 4) {
+            int64_t b = base + (lane >> 3);
+            if (b >= n_blocks) continue;
+            const uint8_t* p = src + b * 34;
+            float D = h2f_bits(ld_u16(p));
+            int e = (lane & 7) * 4;
+            float4 y;
+            y.x = __fmul_rn(D, (float)(int8_t)p[2 + e]);
+            y.y = __fmul_rn(D, (float)(int8_t)p[3 + e]);
+            y.z = __fmul_rn(D, (float)(int8_t)p[4 + e]);
+            y.w = __fmul_rn(D, (float)(int8_t)p[5 + e]);
+            *reinterpret_cast<float4*>(dst + b * 32 + e) = y;
+        }
+        return;
+    }
+    for (int64_t b = warp; b < n_blocks; b += n_warps) {
+        float y[8];
+        if (T == SYN_Q8_K) {
+            const uint8_t* p = src + b * 292;
+            float d = *reinterpret_cast<const float*>(p);
+            uint32_t w0 = *reinterpret_cast<const uint32_t*>(p + 4 + lane * 8);
+            uint32_t w1 = *reinterpret_cast<const uint32_t*>(p + 8 + lane * 8);
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                y[i] = __fmul_rn(d, (float)(int8_t)(w0 >> (8 * i)));
+                y[4 + i] = __fmul_rn(d, (float)(int8_t)(w1 >> (8 * i)));
+            }
+        } else if (T == SYN_Q4_K) {
+            const uint8_t* p = src + b * 144;
+            float D = h2f_bits(ld_u16(p)), Dm = h2f_bits(ld_u16(p + 2));
+            const uint8_t* sb = p + 4;
+            int j = lane >> 2;  // sub-block of this lane's 8 values
+            int sc, mn;
+            if (j < 4) {
+                sc = sb[j] & 63;
+                mn = sb[j + 4] & 63;
+            } else {
+                sc = (sb[j + 4] & 15) | ((sb[j - 4] >> 6) << 4);
+                mn = (sb[j + 4] >> 4) | ((sb[j] >> 6) << 4);
+            }
+            float S = __fmul_rn(D, (float)sc), M = __fmul_rn(Dm, (float)mn);
+            int c = j >> 1, shift = (j & 1) * 4, l = (lane & 3) * 8;
+            const uint8_t* qs = p + 16 + 32 * c + l;
+#pragma unroll
+            for (int i = 0; i < 8; i++) y[i] = __fsub_rn(__fmul_rn(S, (float)((qs[i] >> shift) & 15)), M);
+        } else {  // Q6_K
+            const uint8_t* p = src + b * 210;
+            float D = h2f_bits(ld_u16(p + 208));
+            int e0 = lane * 8;  // values e0..e0+7, one sub-block
+            float S = __fmul_rn(D, (float)(int8_t)p[192 + (e0 >> 4)]);
+            int h = e0 >> 7, w = e0 & 127, quarter = w >> 5, l0 = w & 31;
+            const uint8_t* ql = p + 64 * h + l0 + ((quarter & 1) ? 32 : 0);
+            const uint8_t* qh = p + 128 + 32 * h + l0;
+            int nshift = (quarter >= 2) ? 4 : 0;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                int q = ((ql[i] >> nshift) & 15) | (((qh[i] >> (2 * quarter)) & 3) << 4);
+                y[i] = __fmul_rn(S, (float)(q - 32));
+            }
+        }
+        float* o = dst + b * 256 + lane * 8;
+        *reinterpret_cast<float4*>(o) = make_float4(y[0], y[1], y[2], y[3]);
+        *reinterpret_cast<float4*>(o + 4) = make_float4(y[4], y[5], y[6], y[7]);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// activations -> vec_dot_type, structure-of-arrays (codes, scales, 16-sums)
+// ---------------------------------------------------------------------------------------
+
+template <int XT>
+__global__ void __launch_bounds__(256) k_quantize_act(const float* __restrict__ X, int64_t n_rows_blocks,
+                                                      int8_t* __restrict__ qs, float* __restrict__ d,
+                                                      int16_t* __restrict__ bsums) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    if (XT == SYN_Q8_0) {
+        for (int64_t base = warp * 4; base < n_rows_blocks; base += n_warps * 4) {
+            int64_t b = base + (lane >> 3);
+            int e = (lane & 7) * 4;
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            if (b < n_rows_blocks) {
+                float4 x = *reinterpret_cast<const float4*>(X + b * 32 + e);
+                v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+            }
+            uint16_t db;
+            bool fin;
+            uint32_t q = q8_0_group(v, &db, &fin);
+            if (b < n_rows_blocks) {
+                *reinterpret_cast<uint32_t*>(qs + b * 32 + e) = q;
+                if ((lane & 7) == 0) d[b] = h2f_bits(db);
+            }
+        }
+    } else {
+        for (int64_t b = warp; b < n_rows_blocks; b += n_warps) {
+            const float* x = X + b * 256 + lane * 8;
+            float4 x0 = *reinterpret_cast<const float4*>(x);
+            float4 x1 = *reinterpret_cast<const float4*>(x + 4);
+            float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            uint32_t w0, w1;
+            float dd;
+            int bs;
+            bool fin;
+            q8_k_warp(v, &w0, &w1, &dd, &bs, &fin);
+            *reinterpret_cast<uint2*>(qs + b * 256 + lane * 8) = make_uint2(w0, w1);
+            if (lane == 0) d[b] = dd;
+            if ((lane & 1) == 0 && bsums) bsums[b * 16 + (lane >> 1)] = (int16_t)bs;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// prefill activation step: quantize to the vec_dot_type and write x_hat = fp16(d * q),
+// the tensor-core operand (token-major, n_in contiguous fp16 per token)
+// ---------------------------------------------------------------------------------------
+
+template <int XT>
+__global__ void __launch_bounds__(256) k_act_half(const float* __restrict__ X, int64_t n_rows_blocks,
+                                                  __half* __restrict__ xh) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    if (XT == SYN_Q8_0) {
+        for (int64_t base = warp * 4; base < n_rows_blocks; base += n_warps * 4) {
+            int64_t b = base + (lane >> 3);
+            int e = (lane & 7) * 4;
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            if (b < n_rows_blocks) {
+                float4 x = *reinterpret_cast<const float4*>(X + b * 32 + e);
+                v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+            }
+            uint16_t db;
+            bool fin;
+            uint32_t q = q8_0_group(v, &db, &fin);
+            if (b < n_rows_blocks) {
+                float D = h2f_bits(db);
+                __half2 a = __floats2half2_rn(__fmul_rn(D, (float)(int8_t)(q)), __fmul_rn(D, (float)(int8_t)(q >> 8)));
+                __half2 c = __floats2half2_rn(__fmul_rn(D, (float)(int8_t)(q >> 16)), __fmul_rn(D, (float)(int8_t)(q >> 24)));
+                uint2 out = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&c));
+                *reinterpret_cast<uint2*>(xh + b * 32 + e) = out;
+            }
+        }
+    } else {
+        for (int64_t b = warp; b < n_rows_blocks; b += n_warps) {
+            const float* x = X + b * 256 + lane * 8;
+            float4 x0 = *reinterpret_cast<const float4*>(x);
+            float4 x1 = *reinterpret_cast<const float4*>(x + 4);
+            float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            uint32_t w0, w1;
+            float dd;
+            int bs;
+            bool fin;
+            q8_k_warp(v, &w0, &w1, &dd, &bs, &fin);
+            uint32_t hv[4];
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                uint32_t w = (k < 2) ? w0 : w1;
+                int sh = (k & 1) * 16;
+                __half2 h2 = __floats2half2_rn(__fmul_rn(dd, (float)(int8_t)(w >> sh)),
+                                               __fmul_rn(dd, (float)(int8_t)(w >> (sh + 8))));
+                hv[k] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            *reinterpret_cast<uint4*>(xh + b * 256 + lane * 8) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// integer block sums (bit-exact check of the block dot; not on the hot path)
+// ---------------------------------------------------------------------------------------
+
+template <int T>
+__global__ void k_block_sums(const uint8_t* __restrict__ W, int64_t n_out, int64_t nb,
+                             const uint8_t* __restrict__ Xq, int64_t n_tok,
+                             int32_t* __restrict__ S) {
+    int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int64_t total = n_tok * n_out * nb;
+    if (idx >= total) return;
+    int64_t b = idx % nb;
+    int64_t o = (idx / nb) % n_out;
+    int64_t t = idx / (nb * n_out);
+    int32_t s0 = 0, s1 = 0;
+    if (T == SYN_Q8_0) {
+        const uint8_t* w = W + (o * nb + b) * 34;
+        const uint8_t* x = Xq + (t * nb + b) * 34;
+        for (int i = 0; i < 32; i++) s0 += (int32_t)(int8_t)w[2 + i] * (int32_t)(int8_t)x[2 + i];
+    } else {
+        const uint8_t* x = Xq + (t * nb + b) * 292;
+        const int8_t* xq = reinterpret_cast<const int8_t*>(x + 4);
+        const int16_t* bs = reinterpret_cast<const int16_t*>(x + 260);
+        if (T == SYN_Q4_K) {
+            const uint8_t* w = W + (o * nb + b) * 144;
+            const uint8_t* sb = w + 4;
+            for (int j = 0; j < 8; j++) {
+                int sc, mn;
+                if (j < 4) { sc = sb[j] & 63; mn = sb[j + 4] & 63; }
+                else { sc = (sb[j + 4] & 15) | ((sb[j - 4] >> 6) << 4); mn = (sb[j + 4] >> 4) | ((sb[j] >> 6) << 4); }
+                int dot = 0;
+                for (int l = 0; l < 32; l++) {
+                    int q = (w[16 + 32 * (j >> 1) + l] >> ((j & 1) * 4)) & 15;
+                    dot += q * xq[32 * j + l];
+                }
+                s0 += sc * dot;
+                s1 += mn * (bs[2 * j] + bs[2 * j + 1]);
+            }
+        } else {
+            const uint8_t* w = W + (o * nb + b) * 210;
+            for (int i = 0; i < 256; i++) {
+                int h = i >> 7, wi = i & 127, quarter = wi >> 5, l = wi & 31;
+                int lo = (w[64 * h + l + ((quarter & 1) ? 32 : 0)] >> ((quarter >= 2) ? 4 : 0)) & 15;
+                int hi = (w[128 + 32 * h + l] >> (2 * quarter)) & 3;
+                int q = lo | (hi << 4);
+                s0 += (int32_t)(int8_t)w[192 + (i >> 4)] * (q - 32) * xq[i];
+            }
+        }
+    }
+    S[idx * 2] = s0;
+    S[idx * 2 + 1] = s1;
+}
+
+// ---------------------------------------------------------------------------------------
+// host launchers
+// ---------------------------------------------------------------------------------------
+
+static int grid_for(int64_t warps_needed, int sms) {
+    int64_t ctas = (warps_needed + 7) / 8;
+    int64_t cap = (int64_t)sms * 8;
+    if (ctas > cap) ctas = cap;
+    return ctas < 1 ? 1 : (int)ctas;
+}
+
+cudaError_t launch_quantize(int type, const float* src, void* dst, int64_t n_blocks, int* range_err,
+                            int sms, cudaStream_t s) {
+    int64_t warps = (type == SYN_Q8_0) ? (n_blocks + 3) / 4 : n_blocks;
+    int g = grid_for(warps, sms);
+    uint8_t* d = static_cast<uint8_t*>(dst);
+    switch (type) {
+    case SYN_Q8_0: k_quantize<SYN_Q8_0><<<g, 256, 0, s>>>(src, d, n_blocks, range_err); break;
+    case SYN_Q4_K: k_quantize<SYN_Q4_K><<<g, 256, 0, s>>>(src, d, n_blocks, range_err); break;
+    case SYN_Q6_K: k_quantize<SYN_Q6_K><<<g, 256, 0, s>>>(src, d, n_blocks, range_err); break;
+    case SYN_Q8_K: k_quantize<SYN_Q8_K><<<g, 256, 0, s>>>(src, d, n_blocks, range_err); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(int type, const void* src, float* dst, int64_t n_blocks, int sms,
+                              cudaStream_t s) {
+    int64_t warps = (type == SYN_Q8_0) ? (n_blocks + 3) / 4 : n_blocks;
+    int g = grid_for(warps, sms);
+    const uint8_t* p = static_cast<const uint8_t*>(src);
+    switch (type) {
+    case SYN_Q8_0: k_dequantize<SYN_Q8_0><<<g, 256, 0, s>>>(p, dst, n_blocks); break;
+    case SYN_Q4_K: k_dequantize<SYN_Q4_K><<<g, 256, 0, s>>>(p, dst, n_blocks); break;
+    case SYN_Q6_K: k_dequantize<SYN_Q6_K><<<g, 256, 0, s>>>(p, dst, n_blocks); break;
+    case SYN_Q8_K: k_dequantize<SYN_Q8_K><<<g, 256, 0, s>>>(p, dst, n_blocks); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_act(int xtype, const float* X, int64_t n_blocks, int8_t* qs, float* d,
+                                int16_t* bsums, int sms, cudaStream_t s) {
+    int64_t warps = (xtype == SYN_Q8_0) ? (n_blocks + 3) / 4 : n_blocks;
+    int g = grid_for(warps, sms);
+    if (xtype == SYN_Q8_0) k_quantize_act<SYN_Q8_0><<<g, 256, 0, s>>>(X, n_blocks, qs, d, bsums);
+    else k_quantize_act<SYN_Q8_K><<<g, 256, 0, s>>>(X, n_blocks, qs, d, bsums);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_act_half(int xtype, const float* X, int64_t n_blocks, void* xh, int sms,
+                            cudaStream_t s) {
+    int64_t warps = (xtype == SYN_Q8_0) ? (n_blocks + 3) / 4 : n_blocks;
+    int g = grid_for(warps, sms);
+    __half* h = static_cast<__half*>(xh);
+    if (xtype == SYN_Q8_0) k_act_half<SYN_Q8_0><<<g, 256, 0, s>>>(X, n_blocks, h);
+    else k_act_half<SYN_Q8_K><<<g, 256, 0, s>>>(X, n_blocks, h);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_block_sums(int type, const void* W, int64_t n_out, int64_t nb, const void* Xq,
+                              int64_t n_tok, int32_t* S, cudaStream_t s) {
+    int64_t total = n_tok * n_out * nb;
+    if (total == 0) return cudaSuccess;
+    int64_t g = (total + 255) / 256;
+    const uint8_t* w = static_cast<const uint8_t*>(W);
+    const uint8_t* x = static_cast<const uint8_t*>(Xq);
+    switch (type) {
+    case SYN_Q8_0: k_block_sums<SYN_Q8_0><<<(unsigned)g, 256, 0, s>>>(w, n_out, nb, x, n_tok, S); break;
+    case SYN_Q4_K: k_block_sums<SYN_Q4_K><<<(unsigned)g, 256, 0, s>>>(w, n_out, nb, x, n_tok, S); break;
+    case SYN_Q6_K: k_block_sums<SYN_Q6_K><<<(unsigned)g, 256, 0, s>>>(w, n_out, nb, x, n_tok, S); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace syn

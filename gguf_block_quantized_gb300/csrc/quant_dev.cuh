@@ -1,0 +1,160 @@
+// quant_dev.cuh — warp-cooperative block encoders, used by the quantize kernels and by
+// the activation step of the product kernels (the same code, so that the activations a
+// product uses are exactly those syn_quantize_activations returns).
+//
+// Encoders: plain readings of the format table in "The GGML ecosystem, and where synapse
+// fits", section 5, with the activation conversion of "Products: weights against
+// quantized activations" (Q8_0 for Q8_0 weights, Q8_K for the K-quants).  Every float
+// operation is an explicit round-to-nearest intrinsic: no contraction into FMA, IEEE
+// division, so the bytes equal those of a scalar fp32 implementation.
+#pragma once
+#include "common.cuh"
+
+namespace syn {
+
+__device__ __forceinline__ float clampf(float v, float lo, float hi) {
+    return v < lo ? lo : (v > hi ? hi : v);
+}
+
+__device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
+    return (uint32_t)(a & 0xFF) | ((uint32_t)(b & 0xFF) << 8) | ((uint32_t)(c & 0xFF) << 16) |
+           ((uint32_t)(d & 0xFF) << 24);
+}
+
+template <int W>
+__device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+    for (int o = 1; o < W; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+template <int W>
+__device__ __forceinline__ float group_min(float v) {
+#pragma unroll
+    for (int o = 1; o < W; o <<= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ bool all_finite4(const float* v) {
+    return isfinite(v[0]) && isfinite(v[1]) && isfinite(v[2]) && isfinite(v[3]);
+}
+
+// ---------------------------------------------------------------------------------------
+// Q8_0: groups of 8 lanes, 4 consecutive values per lane, one 32-block per group.
+// Returns the 4 codes packed in a word and the stored scale (fp16 bits in *dbits).
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t q8_0_group(const float v[4], uint16_t* dbits,
+                                               bool* finite) {
+    float a = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    float amax = group_max<8>(a);
+    float d = __fdiv_rn(amax, 127.0f);
+    __half hd = __float2half_rn(d);
+    float D = __half2float(hd);
+    int q[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        q[i] = (D == 0.0f) ? 0 : (int)clampf(roundf(__fdiv_rn(v[i], D)), -127.0f, 127.0f);
+    *dbits = __half_as_ushort(hd);
+    *finite = all_finite4(v) && !__hisinf(hd);
+    return pack4_s8(q[0], q[1], q[2], q[3]);
+}
+
+// ---------------------------------------------------------------------------------------
+// Q8_K: one warp per 256-block, 8 consecutive values per lane (lane L: 8L..8L+7).
+// Returns the codes as two words, the fp32 scale, and in *bsum the sum of the 16 codes
+// of sub-block L/2 (valid in every lane).
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void q8_k_warp(const float v[8], uint32_t* w0, uint32_t* w1,
+                                          float* dout, int* bsum, bool* finite) {
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) a = fmaxf(a, fabsf(v[i]));
+    float amax = group_max<32>(a);
+    float d = __fdiv_rn(amax, 127.0f);
+    int q[8];
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        q[i] = (d == 0.0f) ? 0 : (int)clampf(roundf(__fdiv_rn(v[i], d)), -127.0f, 127.0f);
+        s += q[i];
+    }
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    *w0 = pack4_s8(q[0], q[1], q[2], q[3]);
+    *w1 = pack4_s8(q[4], q[5], q[6], q[7]);
+    *dout = d;
+    *bsum = s;
+    *finite = all_finite4(v) && all_finite4(v + 4);
+}
+
+// ---------------------------------------------------------------------------------------
+// Q4_K: one warp per 256-block, lane L holds values 8L..8L+7 (sub-block L/4).
+// Produces the codes (two words, one nibble value per byte), the sub-block scale and
+// min codes of the lane's sub-block, and the two fp16 super-scales.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void q4_k_warp(const float v[8], uint32_t* w0, uint32_t* w1,
+                                          int* sc_out, int* mn_out, uint16_t* dbits,
+                                          uint16_t* dminbits, bool* finite) {
+    float lo = 0.0f, hi = v[0];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        lo = fminf(lo, v[i]);
+        hi = fmaxf(hi, v[i]);
+    }
+    lo = group_min<4>(lo);
+    hi = group_max<4>(hi);
+    float s = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+    float m = (lo < 0.0f) ? -lo : 0.0f;
+    // max over the warp; adding +0 turns a -0 maximum (all sub-blocks -0) into +0, the
+    // value a scalar running maximum started at +0 keeps.
+    float smax = __fadd_rn(group_max<32>(s), 0.0f);
+    float mmax = group_max<32>(m);
+    __half hd = __float2half_rn(__fdiv_rn(smax, 63.0f));
+    __half hdm = __float2half_rn(__fdiv_rn(mmax, 63.0f));
+    float D = __half2float(hd), Dm = __half2float(hdm);
+    int sc = (D == 0.0f) ? 0 : (int)fminf(63.0f, roundf(__fdiv_rn(s, D)));
+    int mn = (Dm == 0.0f) ? 0 : (int)fminf(63.0f, roundf(__fdiv_rn(m, Dm)));
+    float S = __fmul_rn(D, (float)sc);
+    float M = __fmul_rn(Dm, (float)mn);
+    int q[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        q[i] = (S > 0.0f) ? (int)clampf(roundf(__fdiv_rn(__fadd_rn(v[i], M), S)), 0.0f, 15.0f) : 0;
+    *w0 = pack4_s8(q[0], q[1], q[2], q[3]);
+    *w1 = pack4_s8(q[4], q[5], q[6], q[7]);
+    *sc_out = sc;
+    *mn_out = mn;
+    *dbits = __half_as_ushort(hd);
+    *dminbits = __half_as_ushort(hdm);
+    bool f = all_finite4(v) && all_finite4(v + 4);
+    *finite = f && !__hisinf(hd) && !__hisinf(hdm);
+}
+
+// ---------------------------------------------------------------------------------------
+// Q6_K: one warp per 256-block, lane L holds values 8L..8L+7 (sub-block L/2).
+// Produces the stored codes q'+32 (0..63, one per byte), the lane's sub-block scale and
+// the fp16 super-scale.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void q6_k_warp(const float v[8], uint32_t* w0, uint32_t* w1,
+                                          int* sc_out, uint16_t* dbits, bool* finite) {
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) a = fmaxf(a, fabsf(v[i]));
+    float amax = group_max<2>(a);
+    float s = __fdiv_rn(amax, 31.0f);
+    float smax = group_max<32>(s);
+    __half hd = __float2half_rn(__fdiv_rn(smax, 127.0f));
+    float D = __half2float(hd);
+    int sc = (D == 0.0f) ? 0 : (int)fminf(127.0f, roundf(__fdiv_rn(s, D)));
+    float S = __fmul_rn(D, (float)sc);
+    int q[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        q[i] = ((S > 0.0f) ? (int)clampf(roundf(__fdiv_rn(v[i], S)), -32.0f, 31.0f) : 0) + 32;
+    *w0 = pack4_s8(q[0], q[1], q[2], q[3]);
+    *w1 = pack4_s8(q[4], q[5], q[6], q[7]);
+    *sc_out = sc;
+    *dbits = __half_as_ushort(hd);
+    *finite = all_finite4(v) && all_finite4(v + 4) && !__hisinf(hd);
+}
+
+}  // namespace syn

@@ -1,0 +1,170 @@
+/*
+ * syn.h — C ABI of libsyn: GGUF block-quantized mul_mat on one GB300 (sm_103a).
+ *
+ * The operation ("The GGML ecosystem, and where synapse fits", section 5, "Products:
+ * weights against quantized activations"; yakaai ggml documentation, examples/simple):
+ *
+ *   W  n_out x n_in weights in a block format, rows contiguous, each row n_in/B blocks
+ *      (GGUF "ne = [cols, rows]", section 2 of the same page);
+ *   X  n_tok x n_in fp32 activations, token-major;
+ *   Y  n_tok x n_out fp32, Y[t*n_out + o] = sum_i W[o,i] * Xq[t,i]
+ *      i.e. ggml_mul_mat(W, X) = (X W^T): each token's outputs are contiguous.
+ *
+ * Xq is X converted, row by row, to the weight format's vec_dot_type before the product
+ * (Q8_0 for Q8_0 weights, Q8_K for Q4_K and Q6_K weights): the product is that of the
+ * quantized activations, as on the pages, not the exact fp32 product.
+ *
+ * Conventions for every entry point:
+ *   - pointers are DEVICE pointers on the current CUDA device unless stated otherwise,
+ *     owned by the caller; the library keeps no reference after the call returns;
+ *   - work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream) and is
+ *     asynchronous unless stated otherwise;
+ *   - the return value is SYN_OK (0) or a negative SYN_ERR_* code; on an error nothing
+ *     has been enqueued, except for SYN_ERR_CUDA (a launch failed) and SYN_ERR_TIMEOUT;
+ *   - nothing throws, nothing prints.
+ */
+#ifndef SYN_H
+#define SYN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SYN_API __attribute__((visibility("default")))
+#else
+#define SYN_API
+#endif
+
+typedef struct CUstream_st* syn_stream_t; /* identical to cudaStream_t */
+
+/* Block formats (the library's own numbering, not ggml_type values).
+ * Format table, "The GGML ecosystem, and where synapse fits", section 5:
+ *   Q8_0  32 weights,  34 B: fp16 d, 32 int8 q;                       w = d*q
+ *   Q4_K 256 weights, 144 B: fp16 d, fp16 dmin, 12 B of 6-bit scales and mins,
+ *                            128 B of 4-bit q in 8 sub-blocks of 32;  w = d*sc*q - dmin*m
+ *   Q6_K 256 weights, 210 B: 128 B low 4 bits, 64 B high 2 bits, 16 int8 scales, fp16 d;
+ *                            16 sub-blocks of 16;                     w = d*sc*(q - 32)
+ *   Q8_K 256 values,  292 B: fp32 d, 256 int8 q, 16 int16 sums of 16 q (activations only)
+ * In-block byte order: the public GGUF layout (fields in the order listed above). */
+enum {
+    SYN_TYPE_Q8_0 = 1,
+    SYN_TYPE_Q4_K = 2,
+    SYN_TYPE_Q6_K = 3,
+    SYN_TYPE_Q8_K = 4,
+};
+
+enum {
+    SYN_OK = 0,
+    SYN_ERR_TYPE = -1,    /* unknown format, or a format not allowed for this call     */
+    SYN_ERR_SHAPE = -2,   /* a size <= 0 (or < 0 where 0 is allowed), or n_in % B != 0 */
+    SYN_ERR_NULL = -3,    /* a required pointer is NULL                                 */
+    SYN_ERR_ALIGN = -4,   /* a pointer is not 16-byte aligned                           */
+    SYN_ERR_RANGE = -5,   /* quantize input non-finite, or a scale overflows fp16       */
+    SYN_ERR_CUDA = -6,    /* a CUDA call or kernel launch failed                        */
+    SYN_ERR_TIMEOUT = -7, /* a device-side wait gave up (bounded spin); results invalid */
+    SYN_ERR_NOMEM = -8,   /* the workspace could not be allocated                       */
+    SYN_ERR_DEVICE = -9,  /* the current device is not sm_103 / not usable              */
+};
+
+/* Elements per block: 32 (Q8_0) or 256 (Q4_K, Q6_K, Q8_K); -1 for an unknown type. */
+SYN_API int64_t syn_block_elems(int type);
+
+/* Bytes per block: 34, 144, 210, 292; -1 for an unknown type. */
+SYN_API int64_t syn_block_bytes(int type);
+
+/* Bytes of one row of n elements: (n / elems) * bytes; -1 if the type is unknown or
+ * n is not a positive multiple of the block size.  Pure host function. */
+SYN_API int64_t syn_row_bytes(int type, int64_t n);
+
+/* Quantize n_rows rows of n_per_row fp32 values (src, row-major, contiguous) into blocks
+ * (dst, n_rows * syn_row_bytes bytes).  type: Q8_0, Q4_K, Q6_K or Q8_K.
+ * Encoders (plain readings of the format table; bit-exact with the CPU oracle):
+ *   Q8_0  d = fp16(amax/127); q = clamp(round(x / d_stored), -127, 127)
+ *   Q8_K  d = amax/127 (fp32); q = clamp(round(x / d), -127, 127); bsums = sums of 16 q
+ *   Q4_K  per 32-sub-block: lo = min(0, min x), s = (max x - lo)/15, m = -lo;
+ *         d = fp16(max s / 63), dmin = fp16(max m / 63), sc = min(63, round(s/d)),
+ *         mn = min(63, round(m/dmin)), q = clamp(round((x + dmin*mn)/(d*sc)), 0, 15)
+ *   Q6_K  per 16-sub-block: s = amax/31; d = fp16(max s / 127), sc = min(127, round(s/d)),
+ *         q = clamp(round(x/(d*sc)), -32, 31) + 32
+ * round = ties away from zero; a zero scale gives zero codes.
+ * Returns SYN_ERR_RANGE if any input is NaN/Inf or a scale overflows fp16; to report
+ * that, this call SYNCHRONIZES `stream` before returning (it is an offline operation).
+ * Calls that overlap on the GPU share one status word and must not run concurrently.
+ * Alignment: src and dst must be 16-byte aligned.  n_rows == 0 is a no-op. */
+SYN_API int syn_quantize(int type, const float* src, void* dst, int64_t n_rows, int64_t n_per_row,
+                 syn_stream_t stream);
+
+/* Expand blocks back to fp32 ("dequantize_row_*", same page, section 5): dst gets
+ * n_rows * n_per_row floats.  Q8_0: d*q; Q4_K: (d*sc)*q - (dmin*mn); Q6_K:
+ * (d*sc)*(q-32); Q8_K: d*q — each product and difference one fp32 rounding, no FMA,
+ * so the result is bit-exact with the CPU oracle.  Asynchronous.  Alignment: 16 B. */
+SYN_API int syn_dequantize(int type, const void* src, float* dst, int64_t n_rows, int64_t n_per_row,
+                   syn_stream_t stream);
+
+/* The activation step of the product on its own (from_float to the vec_dot_type):
+ * X (n_tok x n_in fp32) -> codes qs (n_tok x n_in int8), scales d (n_tok x n_in/Bx fp32,
+ * Bx = 32 for Q8_0 weights, 256 for K-quant weights; for Q8_0 the value of the stored
+ * fp16 scale) and, for K-quant weights only, bsums (n_tok x n_in/16 int16; may be NULL
+ * for Q8_0).  wtype is the WEIGHT format (Q8_0, Q4_K or Q6_K).  This is the same device
+ * code the product kernels run on their inputs.  Asynchronous.  Alignment: 16 B. */
+SYN_API int syn_quantize_activations(int wtype, const float* X, int64_t n_tok, int64_t n_in,
+                             int8_t* qs, float* d, int16_t* bsums, syn_stream_t stream);
+
+/* Y = ggml_mul_mat(W, X) as described at the top of this file.
+ * type: Q8_0, Q4_K or Q6_K (Q8_K is activation-only and rejected with SYN_ERR_TYPE).
+ * n_tok <= the decode threshold (default 8, see syn_set_gemv_max_tok) runs the decode
+ * kernel: one launch that quantizes X in shared memory and streams W once per group of
+ * up to 8 tokens.  Larger n_tok runs the prefill path: one kernel quantizes X and writes
+ * the dequantized fp16 activations into the library workspace, a second runs the
+ * tensor-core GEMM on W tiles dequantized to fp16 in shared memory (fp32 accumulation).
+ * Accuracy: |y - y_ref| <= 1e-4 * ||dequant(w_row)||_2 * ||x||_2 per element, where
+ * y_ref is the same product evaluated in fp64.  W, X, Y: 16-byte aligned, not aliased.
+ * n_tok == 0 is a no-op.  Asynchronous.  The prefill path may grow the workspace (see
+ * syn_reserve); growth allocates device memory and synchronizes the device, so reserve
+ * before capturing a CUDA graph.  The workspace belongs to (device, stream): calls on one
+ * stream are ordered; calls on different streams use different workspaces. */
+SYN_API int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in,
+                const float* X, int64_t n_tok, float* Y, syn_stream_t stream);
+
+/* Pre-size the prefill workspace of (current device, stream) for products with up to
+ * max_n_in inputs and max_n_tok tokens, so that later syn_mul_mat calls allocate
+ * nothing.  Synchronizes the device when it (re)allocates. */
+SYN_API int syn_reserve(int64_t max_n_in, int64_t max_n_tok, syn_stream_t stream);
+
+/* Free every workspace the library holds on the current device (synchronizes it). */
+SYN_API int syn_release(void);
+
+/* Integer block sums for bit-exact checks (not on the hot path).  Xq holds n_tok rows of
+ * packed vec_dot_type blocks (Q8_0 blocks for Q8_0 weights, Q8_K blocks otherwise).
+ * S[((t*n_out + o)*n_blocks + b)*2 + {0,1}]:  Q8_0 {I, 0}: I = sum qw*qx;
+ * Q4_K {A, Bm}: A = sum_j sc_j * sum_{i in j} q_i*qx_i, Bm = sum_j mn_j * (bsum_2j + bsum_2j+1);
+ * Q6_K {C, 0}: C = sum_j sc_j * sum_{i in j} (q_i - 32)*qx_i.  Asynchronous. */
+SYN_API int syn_block_sums(int type, const void* W, int64_t n_out, int64_t n_in,
+                   const void* Xq, int64_t n_tok, int32_t* S, syn_stream_t stream);
+
+/* Decode/prefill threshold: products with n_tok <= n use the decode kernel.  n >= 0;
+ * 0 forces the prefill path for every n_tok >= 1.  Returns the previous value.
+ * Process-wide; the default is 8, or the value of the environment variable
+ * SYN_GEMV_MAX_TOK when the library is loaded. */
+SYN_API int syn_set_gemv_max_tok(int n);
+
+/* Read (and with clear != 0, reset) the device-side error word of the current device:
+ * SYN_OK, or SYN_ERR_TIMEOUT if a kernel gave up a bounded wait.  Synchronizes the
+ * device. */
+SYN_API int syn_device_status(int clear);
+
+/* Number of kernels this library has launched in this process (all devices). */
+SYN_API int64_t syn_launch_count(void);
+
+/* Static text for a status code. */
+SYN_API const char* syn_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SYN_H */

@@ -1,0 +1,74 @@
+"""The C-ABI library builds, loads and exports every symbol include/syn.h declares; the
+host-side argument checks answer without touching a GPU.  CPU only."""
+import os
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "syn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import torch  # noqa: F401  (loads the CUDA runtime libsyn links against)
+    from gguf_block_quantized_gb300 import build
+    build.build()
+    from gguf_block_quantized_gb300 import syn
+    return syn
+
+
+def declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"SYN_API\s+[\w\s\*]+?\b(syn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared()
+    for must in ("syn_quantize", "syn_dequantize", "syn_mul_mat", "syn_quantize_activations",
+                 "syn_block_elems", "syn_block_bytes", "syn_row_bytes", "syn_strerror"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (syn_\w+)", out))
+    missing = [n for n in declared() if n not in exported]
+    assert not missing, missing
+    assert {n for n, _, _ in lib.EXPORTS} == set(declared())
+
+
+def test_host_functions(lib):
+    assert [lib.syn_block_elems(t) for t in (1, 2, 3, 4)] == [32, 256, 256, 256]
+    assert [lib.syn_block_bytes(t) for t in (1, 2, 3, 4)] == [34, 144, 210, 292]
+    assert lib.syn_block_elems(9) == -1 and lib.syn_block_bytes(0) == -1
+    assert lib.syn_row_bytes(2, 4096) == 16 * 144
+    assert lib.syn_row_bytes(3, 100) == -1 and lib.syn_row_bytes(1, 0) == -1
+    assert lib.syn_strerror(lib.ERR_ALIGN).decode().startswith("pointer")
+    old = lib.syn_set_gemv_max_tok(5)
+    assert lib.syn_set_gemv_max_tok(old) == 5
+    assert lib.syn_set_gemv_max_tok(-1) == -1
+
+
+def test_argument_checks_need_no_gpu(lib):
+    L = lib
+    p = 1 << 20  # any aligned non-null value: the checks below reject before any use
+    assert L.syn_mul_mat(4, p, 4, 256, p, 1, p, None) == L.ERR_TYPE      # Q8_K weights
+    assert L.syn_mul_mat(7, p, 4, 256, p, 1, p, None) == L.ERR_TYPE
+    assert L.syn_mul_mat(2, p, 4, 100, p, 1, p, None) == L.ERR_SHAPE
+    assert L.syn_mul_mat(2, p, 0, 256, p, 1, p, None) == L.ERR_SHAPE
+    assert L.syn_mul_mat(2, p, 4, 256, p, -1, p, None) == L.ERR_SHAPE
+    assert L.syn_mul_mat(2, p, 4, 256, p, 0, p, None) == L.OK           # no-op
+    assert L.syn_mul_mat(2, None, 4, 256, p, 1, p, None) == L.ERR_NULL
+    assert L.syn_mul_mat(2, p + 4, 4, 256, p, 1, p, None) == L.ERR_ALIGN
+    assert L.syn_quantize(2, p, p, 1, 255, None) == L.ERR_SHAPE
+    assert L.syn_quantize(5, p, p, 1, 256, None) == L.ERR_TYPE
+    assert L.syn_quantize(1, p, p, 0, 32, None) == L.OK
+    assert L.syn_quantize(1, p + 8, p, 1, 32, None) == L.ERR_ALIGN
+    assert L.syn_dequantize(3, None, p, 1, 256, None) == L.ERR_NULL
+    assert L.syn_quantize_activations(4, p, 1, 256, p, p, p, None) == L.ERR_TYPE
+    assert L.syn_quantize_activations(2, p, 1, 256, p, p, None, None) == L.ERR_NULL
+    assert L.syn_block_sums(2, p, 1, 300, p, 1, p, None) == L.ERR_SHAPE

@@ -1,0 +1,319 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on the GPU.
+
+Bar: quantized bytes, activation codes/scales/sums and integer block sums bit-exact;
+fp32 products within |y - y_ref| <= 1e-4 * ||dequant(w_row)||_2 * ||x||_2 per element,
+y_ref from the oracle (the same quantized-activation product in fp64).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gguf_block_quantized_gb300 import synth, workloads
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+TOL = 1e-4
+TYPES_W = [oracle.Q8_0, oracle.Q4_K, oracle.Q6_K]
+TYPES_ALL = TYPES_W + [oracle.Q8_K]
+
+
+@pytest.fixture(scope="module")
+def syn():
+    from gguf_block_quantized_gb300 import syn as s
+    return s
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def tolerance(wtype, Wq, n_in, X):
+    """Per-element bound 1e-4 * ||deq(w_row)|| * ||x|| as an (n_tok, n_out) array."""
+    wd = oracle.dequantize(wtype, Wq, n_in).astype(np.float64)
+    wn = np.sqrt((wd * wd).sum(axis=1))
+    xn = np.sqrt((X.astype(np.float64) ** 2).sum(axis=1))
+    return TOL * xn[:, None] * wn[None, :]
+
+
+def assert_close(Y, ref, bound, what):
+    err = np.abs(Y.astype(np.float64) - ref.astype(np.float64))
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside tolerance; "
+                           f"max err/bound {float((err / np.maximum(bound, 1e-300)).max()):.3g}")
+
+
+def inputs_mixed(n_rows, n, seed):
+    """Normal weights plus the degenerate rows the formats have."""
+    x = synth.normal(seed, (n_rows, n), 0.02)
+    if n_rows >= 8:
+        x[1] = 0.0
+        x[2] = synth.normal(seed + 1, n, 1e-6)          # fp16-subnormal scales
+        x[3] = -np.abs(synth.normal(seed + 2, n, 1.0))  # all negative
+        x[4] = np.abs(synth.normal(seed + 3, n, 1.0))   # all positive
+        x[5] = 0.375                                      # constant
+        x[6, ::7] *= 500.0                                # outliers
+        x[7] = synth.uniform(seed + 4, n, -2.0, 2.0)
+    return x
+
+
+# ----------------------------------------------------------------------------------------
+# quantize / dequantize: bit-exact
+# ----------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("t", TYPES_ALL)
+@pytest.mark.parametrize("shape", [(1, 256), (37, 512), (8, 4096), (300, 2304)])
+def test_quantize_bit_exact(syn, t, shape):
+    n_rows, n = shape
+    x = inputs_mixed(n_rows, n, 100 + n_rows)
+    want = oracle.quantize(t, x)
+    got = host(syn.quantize(t, dev(x)))
+    assert got.shape == want.shape
+    mism = np.nonzero(got != want)
+    assert mism[0].size == 0, f"{mism[0].size} bytes differ, first at {mism[0][:3]}, {mism[1][:3]}"
+
+
+@pytest.mark.parametrize("t", TYPES_ALL)
+def test_dequantize_bit_exact(syn, t):
+    n_rows, n = 53, 1024
+    q = oracle.quantize(t, inputs_mixed(n_rows, n, 7))
+    want = oracle.dequantize(t, q, n)
+    got = host(syn.dequantize(t, dev(q), n))
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("t", [oracle.Q4_K, oracle.Q6_K, oracle.Q8_0])
+def test_dequantize_arbitrary_codes_bit_exact(syn, t):
+    """Random block bytes (finite fp16 scales), including negative Q6_K scales."""
+    n_rows, n = 19, 512
+    rb = oracle.row_bytes(t, n)
+    raw = synth.integers(3, (n_rows, rb), 0, 256).astype(np.uint8)
+    nb, bb = n // oracle.BLOCK_ELEMS[t], oracle.BLOCK_BYTES[t]
+    blocks = raw.reshape(n_rows, nb, bb)
+    offs = {oracle.Q8_0: [0], oracle.Q4_K: [0, 2], oracle.Q6_K: [208]}[t]
+    for o in offs:  # keep scales finite: clear the top exponent bit
+        blocks[:, :, o + 1] &= 0xBF
+    want = oracle.dequantize(t, raw, n)
+    got = host(syn.dequantize(t, dev(raw), n))
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_quantize_range_errors(syn):
+    for t in TYPES_ALL:
+        n = oracle.BLOCK_ELEMS[t]
+        x = np.zeros((3, n), np.float32)
+        x[2, 5] = np.nan
+        with pytest.raises(syn.SynError) as e:
+            syn.quantize(t, dev(x))
+        assert e.value.status == syn.ERR_RANGE
+    x = np.zeros((1, 256), np.float32)
+    x[0, 0] = 1e9
+    for t in (oracle.Q4_K, oracle.Q6_K):
+        with pytest.raises(syn.SynError):
+            syn.quantize(t, dev(x))
+    syn.quantize(oracle.Q8_K, dev(x))  # fp32 scale: fine
+
+
+# ----------------------------------------------------------------------------------------
+# activation step and integer block sums: bit-exact
+# ----------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("wt", TYPES_W)
+def test_quantize_activations_bit_exact(syn, wt):
+    n_tok, n_in = 5, 2048
+    X = synth.activations(90, 0, n_tok, n_in)
+    X[1] *= 1e-3
+    X[2, :256] = 0.0
+    xt = oracle.VEC_DOT_TYPE[wt]
+    packed = oracle.quantize(xt, X)
+    qs, d, bs = syn.quantize_activations(wt, dev(X))
+    qs, d = host(qs), host(d)
+    be, bb = oracle.BLOCK_ELEMS[xt], oracle.BLOCK_BYTES[xt]
+    blocks = packed.reshape(n_tok, n_in // be, bb)
+    if xt == oracle.Q8_0:
+        want_d = oracle.fp16_bits_to_fp32(blocks[:, :, 0:2].copy().view(np.uint16)[:, :, 0])
+        want_q = blocks[:, :, 2:].view(np.int8).reshape(n_tok, n_in)
+    else:
+        want_d = blocks[:, :, 0:4].copy().view(np.float32)[:, :, 0]
+        want_q = blocks[:, :, 4:260].view(np.int8).reshape(n_tok, n_in)
+        want_bs = blocks[:, :, 260:292].copy().view(np.int16).reshape(n_tok, n_in // 16)
+        assert np.array_equal(host(bs), want_bs)
+    assert np.array_equal(qs, want_q)
+    assert np.array_equal(d.view(np.uint32), want_d.view(np.uint32))
+
+
+@pytest.mark.parametrize("wt", TYPES_W)
+def test_block_sums_bit_exact(syn, wt):
+    n_out, n_in, n_tok = 9, 1024, 3
+    W = oracle.quantize(wt, synth.normal(61, (n_out, n_in), 0.3))
+    Xq = oracle.quantize(oracle.VEC_DOT_TYPE[wt], synth.normal(62, (n_tok, n_in)))
+    want = oracle.block_sums(wt, W, n_out, n_in, Xq, n_tok)
+    got = host(syn.block_sums(wt, dev(W), n_out, n_in, dev(Xq), n_tok))
+    assert np.array_equal(got, want)
+
+
+# ----------------------------------------------------------------------------------------
+# mul_mat: decode kernel and tensor-core kernel against the oracle
+# ----------------------------------------------------------------------------------------
+
+def run_mul_mat(syn, wt, n_out, n_in, n_tok, seed, path, wstd=0.02):
+    W32 = synth.normal(seed, (n_out, n_in), wstd)
+    X = synth.normal(seed + 1, (n_tok, n_in))
+    Wq = oracle.quantize(wt, W32)
+    old = syn.set_gemv_max_tok(1 << 20 if path == "gemv" else 0)
+    try:
+        Y = host(syn.mul_mat(wt, dev(Wq), n_out, n_in, dev(X)))
+    finally:
+        syn.set_gemv_max_tok(old)
+    assert syn.device_status() == syn.OK
+    ref = oracle.mul_mat(wt, Wq, n_out, n_in, X, n_threads=8)
+    return Y, ref, tolerance(wt, Wq, n_in, X)
+
+
+GEMV_SHAPES = [(1, 256, 1), (37, 512, 1), (300, 768, 2), (64, 2304, 3), (513, 1024, 4), (250, 4096, 8),
+               (129, 512, 11)]
+
+
+@pytest.mark.parametrize("wt", TYPES_W)
+@pytest.mark.parametrize("shape", GEMV_SHAPES)
+def test_mul_mat_gemv(syn, wt, shape):
+    n_out, n_in, n_tok = shape
+    Y, ref, bound = run_mul_mat(syn, wt, n_out, n_in, n_tok, 1000 + n_out, "gemv")
+    assert_close(Y, ref, bound, f"gemv {shape}")
+
+
+GEMM_SHAPES = [(128, 256, 16), (300, 1024, 40), (129, 512, 300), (1000, 2048, 256), (64, 4608, 33),
+               (257, 768, 513)]
+
+
+@pytest.mark.parametrize("wt", TYPES_W)
+@pytest.mark.parametrize("shape", GEMM_SHAPES)
+def test_mul_mat_gemm(syn, wt, shape):
+    n_out, n_in, n_tok = shape
+    Y, ref, bound = run_mul_mat(syn, wt, n_out, n_in, n_tok, 2000 + n_out, "gemm")
+    assert_close(Y, ref, bound, f"gemm {shape}")
+
+
+def test_mul_mat_q8_0_row_not_multiple_of_256(syn):
+    # Q8_0 rows need only 32-element blocks: 800 = 25 blocks (ragged last k-step)
+    for path in ("gemv", "gemm"):
+        Y, ref, bound = run_mul_mat(syn, oracle.Q8_0, 77, 800, 20, 77, path)
+        assert_close(Y, ref, bound, f"q8_0 n_in=800 {path}")
+
+
+def test_mul_mat_orientation_example_exact(syn):
+    """ggml_mul_mat(A, B^T) = C^T with the examples/simple integers, exact on both paths."""
+    A = np.array([[2, 8], [5, 1], [4, 2], [8, 6]], np.float32)
+    BT = np.array([[10, 5], [9, 9], [5, 4]], np.float32)
+    CT = np.array([[60, 55, 50, 110], [90, 54, 54, 126], [42, 29, 28, 64]], np.float32)
+    W = np.zeros((4, 32), np.float32); W[:, :2] = A; W[:, 30] = 127.0
+    X = np.zeros((3, 32), np.float32); X[:, :2] = BT; X[:, 31] = 127.0
+    Wq = oracle.quantize(oracle.Q8_0, W)
+    for n in (1 << 20, 0):
+        old = syn.set_gemv_max_tok(n)
+        try:
+            Y = host(syn.mul_mat(oracle.Q8_0, dev(Wq), 4, 32, dev(X)))
+        finally:
+            syn.set_gemv_max_tok(old)
+        assert np.array_equal(Y, CT)
+
+
+def test_gemv_and_gemm_agree(syn):
+    wt, n_out, n_in, n_tok = oracle.Q4_K, 384, 2048, 8
+    W = oracle.quantize(wt, synth.normal(5, (n_out, n_in), 0.02))
+    X = synth.normal(6, (n_tok, n_in))
+    outs = []
+    for n in (1 << 20, 0):
+        old = syn.set_gemv_max_tok(n)
+        try:
+            outs.append(host(syn.mul_mat(wt, dev(W), n_out, n_in, dev(X))))
+        finally:
+            syn.set_gemv_max_tok(old)
+    assert_close(outs[0], outs[1], 2 * tolerance(wt, W, n_in, X), "gemv vs gemm")
+
+
+def test_gemv_deterministic(syn):
+    wt, n_out, n_in = oracle.Q6_K, 1000, 4096
+    W = dev(oracle.quantize(wt, synth.normal(8, (n_out, n_in), 0.02)))
+    X = dev(synth.normal(9, (2, n_in)))
+    a = host(syn.mul_mat(wt, W, n_out, n_in, X))
+    b = host(syn.mul_mat(wt, W, n_out, n_in, X))
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_mul_mat_zero_and_degenerate(syn):
+    wt, n_out, n_in = oracle.Q4_K, 40, 512
+    Wq = oracle.quantize(wt, inputs_mixed(n_out, n_in, 3))
+    X = synth.normal(4, (5, n_in))
+    X[2] = 0.0
+    for n in (1 << 20, 0):
+        old = syn.set_gemv_max_tok(n)
+        try:
+            Y = host(syn.mul_mat(wt, dev(Wq), n_out, n_in, dev(X)))
+        finally:
+            syn.set_gemv_max_tok(old)
+        ref = oracle.mul_mat(wt, Wq, n_out, n_in, X)
+        assert_close(Y, ref, tolerance(wt, Wq, n_in, X), "degenerate rows")
+        assert np.all(Y[2] == 0.0) and np.all(Y[:, 1] == 0.0)
+    # n_tok == 0 is a no-op
+    Y = torch.full((0, n_out), 1.0, device="cuda")
+    syn.mul_mat(wt, dev(Wq), n_out, n_in, torch.zeros((0, n_in), device="cuda"), Y=Y)
+
+
+def test_mul_mat_error_codes(syn):
+    Wq = dev(oracle.quantize(oracle.Q4_K, synth.normal(1, (4, 256), 0.02)))
+    X = torch.zeros((1, 256), device="cuda")
+    Y = torch.zeros((1, 4), device="cuda")
+    s = 0
+    assert syn.syn_mul_mat(oracle.Q8_K, Wq.data_ptr(), 4, 256, X.data_ptr(), 1, Y.data_ptr(), s) == syn.ERR_TYPE
+    assert syn.syn_mul_mat(oracle.Q4_K, Wq.data_ptr(), 4, 100, X.data_ptr(), 1, Y.data_ptr(), s) == syn.ERR_SHAPE
+    assert syn.syn_mul_mat(oracle.Q4_K, None, 4, 256, X.data_ptr(), 1, Y.data_ptr(), s) == syn.ERR_NULL
+    assert syn.syn_mul_mat(oracle.Q4_K, Wq.data_ptr() + 2, 4, 256, X.data_ptr(), 1, Y.data_ptr(), s) == syn.ERR_ALIGN
+
+
+# ----------------------------------------------------------------------------------------
+# full-size workloads, in the launch configuration the benchmark times: sampled entries
+# ----------------------------------------------------------------------------------------
+
+def sampled_check(syn, m, n_tok, workload, index, n_rows=48, n_toks=4, path=None):
+    W32 = synth.weight(workload, index, m.n_out, m.n_in)
+    X = synth.activations(workload, index, n_tok, m.n_in)
+    Wq = oracle.quantize(m.wtype, W32)
+    old = syn.set_gemv_max_tok(8) if path is None else syn.set_gemv_max_tok(1 << 20 if path == "gemv" else 0)
+    try:
+        Y = host(syn.mul_mat(m.wtype, dev(Wq), m.n_out, m.n_in, dev(X)))
+    finally:
+        syn.set_gemv_max_tok(old)
+    rows = np.unique(np.concatenate([[0, m.n_out - 1], synth.integers(index, n_rows, 0, m.n_out)]))
+    toks = np.unique(np.concatenate([[0, n_tok - 1], synth.integers(index + 1, n_toks, 0, n_tok)]))
+    ref = oracle.mul_mat_sampled(m.wtype, Wq, m.n_out, m.n_in, X, rows, toks)
+    wd = oracle.dequantize(m.wtype, Wq[rows], m.n_in).astype(np.float64)
+    bound = TOL * np.sqrt((X[toks].astype(np.float64) ** 2).sum(1))[:, None] * np.sqrt((wd ** 2).sum(1))[None, :]
+    assert_close(Y[toks][:, rows], ref, bound, f"{m.name} n_tok={n_tok}")
+    assert np.isfinite(Y).all()
+
+
+@pytest.mark.parametrize("i", range(len(workloads.Q8_0_SQUARE)))
+def test_full_q8_0_square(syn, i):
+    sampled_check(syn, workloads.Q8_0_SQUARE[i], 1, 1, i, n_rows=2048)
+
+
+@pytest.mark.parametrize("i", range(len(workloads.LLAMA1B_LAYER)))
+def test_full_llama1b_layer_decode(syn, i):
+    sampled_check(syn, workloads.LLAMA1B_LAYER[i], 1, 2, i, n_rows=512)
+
+
+@pytest.mark.parametrize("n_tok", [1, 4])
+def test_full_lm_head(syn, n_tok):
+    sampled_check(syn, workloads.LM_HEAD_1B[0], n_tok, 3, 0, n_rows=96)
+
+
+@pytest.mark.parametrize("i", range(len(workloads.LLAMA8B_FFN)))
+def test_full_llama8b_ffn_prefill(syn, i):
+    sampled_check(syn, workloads.LLAMA8B_FFN[i], 512, 4, i, n_rows=48, n_toks=6)
