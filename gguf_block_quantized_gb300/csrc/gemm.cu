@@ -323,18 +323,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         my_tx += (uint32_t)nbytes[i];
                     }
                 }
-                uint32_t tx = my_tx;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) tx += __shfl_xor_sync(0xffffffffu, tx, o);
-                const uint32_t rfull = smem_u32(&raw_full[rs]);
-                if (lane == 0) mbar_arrive_expect_tx(rfull, tx);
-                __syncwarp();
                 uint8_t* rbase = sRaw + rs * RAW_STAGE;
-#pragma unroll
-                for (int i = 0; i < 4; i++)
-                    if (nbytes[i] > 0)
-                        bulk_g2s(smem_u32(rbase + (lane + 32 * i) * F::RAW_ROW), p.W + a0[i], (uint32_t)nbytes[i], rfull);
-                // the bytes of W past its last 16-byte boundary, by plain loads
+                // The bytes of W past its last 16-byte boundary (end of the last row only),
+                // by plain loads, before the arrive below publishes the stage.
 #pragma unroll
                 for (int i = 0; i < 4; i++) {
                     const int r = lane + 32 * i;
@@ -348,6 +339,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             rbase[r * F::RAW_ROW + (k - lo)] = p.W[k];
                     }
                 }
+                uint32_t tx = my_tx;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) tx += __shfl_xor_sync(0xffffffffu, tx, o);
+                const uint32_t rfull = smem_u32(&raw_full[rs]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_expect_tx(rfull, tx);
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    if (nbytes[i] > 0)
+                        bulk_g2s(smem_u32(rbase + (lane + 32 * i) * F::RAW_ROW), p.W + a0[i], (uint32_t)nbytes[i], rfull);
                 rc++;
                 // activation tiles of this super-step
                 const int nst = steps_in(ss);
