@@ -1,0 +1,47 @@
+"""One product, repeated a few times, for profiler captures of a single kernel.
+
+    python -m gguf_block_quantized_gb300.profile_case --case gemv_q6k_lm_head --reps 3
+
+Cases (synthetic weights ~N(0, 0.02), activations ~N(0, 1)):
+  gemv_q6k_lm_head   Q6_K 128256 x 2048, 1 token    (216 MB of weights: larger than L2)
+  gemv_q4k_wide      Q4_K 32768 x 8192, 1 token     (151 MB)
+  gemv_q8_0_wide     Q8_0 16384 x 8192, 1 token     (143 MB)
+  gemm_q4k_ffn_up    Q4_K 14336 x 4096, 512 tokens  (prefill, tensor cores)
+  gemm_q4k_ffn_down  Q4_K 4096 x 14336, 512 tokens
+"""
+from __future__ import annotations
+
+import argparse
+
+CASES = {
+    "gemv_q6k_lm_head": (3, 128256, 2048, 1),
+    "gemv_q4k_wide": (2, 32768, 8192, 1),
+    "gemv_q8_0_wide": (1, 16384, 8192, 1),
+    "gemm_q4k_ffn_up": (2, 14336, 4096, 512),
+    "gemm_q4k_ffn_down": (2, 4096, 14336, 512),
+}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--case", required=True, choices=sorted(CASES))
+    ap.add_argument("--reps", type=int, default=3)
+    args = ap.parse_args()
+    import torch
+
+    from gguf_block_quantized_gb300 import syn, synth
+
+    wt, n_out, n_in, n_tok = CASES[args.case]
+    W = syn.quantize(wt, torch.from_numpy(synth.normal(5, (n_out, n_in), 0.02)).cuda())
+    X = torch.from_numpy(synth.normal(6, (n_tok, n_in))).cuda()
+    Y = torch.empty((n_tok, n_out), device="cuda")
+    syn.syn_reserve(n_in, n_tok, torch.cuda.current_stream().cuda_stream)
+    for _ in range(args.reps):
+        syn.mul_mat(wt, W, n_out, n_in, X, Y=Y)
+    torch.cuda.synchronize()
+    assert syn.device_status() == syn.OK
+    print(f"{args.case}: {args.reps} products done")
+
+
+if __name__ == "__main__":
+    main()
