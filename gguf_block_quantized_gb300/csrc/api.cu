@@ -119,6 +119,10 @@ int workspace_for(cudaStream_t s, size_t need, void** out) {
 
 }  // namespace
 
+namespace syn {
+void note_launches(int n) { g_launches += n; }
+}  // namespace syn
+
 extern "C" {
 
 int64_t syn_block_elems(int type) { return known_type(type) ? elems(type) : -1; }
@@ -142,6 +146,7 @@ const char* syn_strerror(int status) {
     case SYN_ERR_TIMEOUT: return "a device-side wait timed out";
     case SYN_ERR_NOMEM: return "out of device memory";
     case SYN_ERR_DEVICE: return "device is not sm_103 (GB300)";
+    case SYN_ERR_TOO_LARGE: return "problem larger than the fixed scratch array";
     default: return "unknown status";
     }
 }

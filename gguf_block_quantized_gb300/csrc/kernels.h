@@ -25,4 +25,7 @@ cudaError_t launch_gemv(int type, const void* W, int64_t n_out, int64_t n_in, co
 cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, const void* xh,
                         int64_t n_tok, float* Y, int* err, int sms, cudaStream_t s);
 
+// Adds n to the count syn_launch_count reports.
+void note_launches(int n);
+
 }  // namespace syn

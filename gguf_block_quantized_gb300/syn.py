@@ -18,6 +18,8 @@ LIB_PATH = os.path.join(HERE, "libsyn.so")
 Q8_0, Q4_K, Q6_K, Q8_K = 1, 2, 3, 4
 OK, ERR_TYPE, ERR_SHAPE, ERR_NULL, ERR_ALIGN, ERR_RANGE, ERR_CUDA, ERR_TIMEOUT, ERR_NOMEM, ERR_DEVICE = \
     0, -1, -2, -3, -4, -5, -6, -7, -8, -9
+ERR_TOO_LARGE = -10
+STATIC_SCRATCH_BYTES = 32 << 20
 BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, Q8_K: 256}
 BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, Q8_K: 292}
 VEC_DOT_TYPE = {Q8_0: Q8_0, Q4_K: Q8_K, Q6_K: Q8_K}
@@ -45,6 +47,7 @@ EXPORTS = [
     ("syn_device_status", _i32, [_i32]),
     ("syn_launch_count", _i64, []),
     ("syn_strerror", ctypes.c_char_p, [_i32]),
+    ("syn_mul_mat_prefill_static", _i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
 ]
 
 for _name, _res, _args in EXPORTS:

@@ -68,6 +68,7 @@ enum {
     SYN_ERR_TIMEOUT = -7, /* a device-side wait gave up (bounded spin); results invalid */
     SYN_ERR_NOMEM = -8,   /* the workspace could not be allocated                       */
     SYN_ERR_DEVICE = -9,  /* the current device is not sm_103 / not usable              */
+    SYN_ERR_TOO_LARGE = -10, /* the problem needs more than the fixed scratch array holds */
 };
 
 /* Elements per block: 32 (Q8_0) or 256 (Q4_K, Q6_K, Q8_K); -1 for an unknown type. */
@@ -159,6 +160,28 @@ SYN_API int syn_device_status(int clear);
 
 /* Number of kernels this library has launched in this process (all devices). */
 SYN_API int64_t syn_launch_count(void);
+
+/* Bytes of the fixed device array behind syn_mul_mat_prefill_static: 32 MiB, enough for
+ * n_tok * n_in <= 16,777,216 (e.g. 4096 tokens of 4096 inputs, 1170 tokens of 14336). */
+#define SYN_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* The prefill product of syn_mul_mat (activation step, then the tensor-core GEMM) for any
+ * n_tok >= 1, for callers that cannot allocate device memory: code running inside a fixed
+ * memory arena or under an allocator or budget that forbids cudaMalloc, or that must not
+ * let a library call cudaMalloc/cudaFree (which can synchronize the device) on its path.
+ * The pages have no counterpart to this entry point; it exists for such callers.
+ * It allocates nothing: the fp16 activation scratch is a static device array of
+ * SYN_STATIC_SCRATCH_BYTES that the library holds on every device it is used on until
+ * the process exits.  Products with n_tok * n_in * 2 > SYN_STATIC_SCRATCH_BYTES are
+ * rejected with SYN_ERR_TOO_LARGE.  Arguments, layout, accuracy and the other error codes
+ * are those of syn_mul_mat.  The first call on a device sets up that device (looks up the
+ * array's device address, clears its status word, synchronizes the device): make it
+ * before any stream capture.  Every call on a device shares the one array and overwrites
+ * it, so calls that can overlap on the GPU (different streams without ordering between
+ * them) race and give wrong results; order them.  Asynchronous.  Its kernel launches are
+ * counted by syn_launch_count. */
+SYN_API int syn_mul_mat_prefill_static(int type, const void* W, int64_t n_out, int64_t n_in,
+                               const float* X, int64_t n_tok, float* Y, syn_stream_t stream);
 
 /* Static text for a status code. */
 SYN_API const char* syn_strerror(int status);
