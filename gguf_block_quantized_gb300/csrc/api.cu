@@ -255,7 +255,7 @@ int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in, const floa
     int rc = device_state(&st);
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (n_tok <= g_gemv_max_tok.load()) {
+    if (n_tok <= g_gemv_max_tok.load() && syn::gemv_act_bytes(type, n_in) <= syn::gemv_act_limit()) {
         rc = check_cuda(syn::launch_gemv(type, W, n_out, n_in, X, n_tok, Y, st->words, st->sms, s));
         if (rc == SYN_OK) g_launches++;
         return rc;
@@ -270,6 +270,61 @@ int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in, const floa
         return SYN_ERR_CUDA;
     g_launches++;
     return SYN_OK;
+}
+
+int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_stream_t stream) {
+    if (n < 0) return SYN_ERR_SHAPE;
+    if (n == 0 || n_tok == 0) return n_tok < 0 ? SYN_ERR_SHAPE : SYN_OK;
+    if (!descs) return SYN_ERR_NULL;
+    for (int i = 0; i < n; i++) {
+        const syn_mat_desc& d = descs[i];
+        if (d.type != SYN_TYPE_Q8_0 && d.type != SYN_TYPE_Q4_K && d.type != SYN_TYPE_Q6_K) return SYN_ERR_TYPE;
+        if (d.n_out <= 0 || d.n_in <= 0 || n_tok < 0 || d.n_in % elems(d.type) || d.n_out * d.n_in > kMaxElems ||
+            n_tok * d.n_in > kMaxElems || n_tok * d.n_out > kMaxElems || d.n_out > (int64_t(1) << 31))
+            return SYN_ERR_SHAPE;
+        if (!d.W || !d.X || !d.Y) return SYN_ERR_NULL;
+        if (!aligned16(d.W) || !aligned16(d.X) || !aligned16(d.Y)) return SYN_ERR_ALIGN;
+    }
+    DeviceState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n_tok > g_gemv_max_tok.load()) {
+        for (int i = 0; i < n; i++) {
+            rc = syn_mul_mat(descs[i].type, descs[i].W, descs[i].n_out, descs[i].n_in, descs[i].X, n_tok, descs[i].Y,
+                             stream);
+            if (rc) return rc;
+        }
+        return SYN_OK;
+    }
+    // pack the products into launches within the decode kernel's activation and job limits
+    syn::GemvDesc group[syn::GEMV_MAX_JOBS];
+    int ng = 0;
+    int64_t act = 0;
+    auto flush = [&]() -> int {
+        if (ng == 0) return SYN_OK;
+        const int r = check_cuda(syn::launch_gemv_batch(ng, group, n_tok, st->words, st->sms, s));
+        if (r == SYN_OK) g_launches++;
+        ng = 0;
+        act = 0;
+        return r;
+    };
+    for (int i = 0; i < n; i++) {
+        const syn_mat_desc& d = descs[i];
+        const int64_t a = syn::gemv_act_bytes(d.type, d.n_in);
+        if (a > syn::gemv_act_limit()) {  // too wide for the decode kernel: the prefill path
+            rc = syn_mul_mat(d.type, d.W, d.n_out, d.n_in, d.X, n_tok, d.Y, stream);
+            if (rc) return rc;
+            continue;
+        }
+        if (ng == syn::GEMV_MAX_JOBS || act + a > syn::gemv_act_limit()) {
+            rc = flush();
+            if (rc) return rc;
+        }
+        group[ng++] = syn::GemvDesc{d.type, d.W, d.n_out, d.n_in, d.X, d.Y};
+        act += a;
+    }
+    return flush();
 }
 
 int syn_block_sums(int type, const void* W, int64_t n_out, int64_t n_in, const void* Xq, int64_t n_tok, int32_t* S,

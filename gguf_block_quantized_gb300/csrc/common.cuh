@@ -101,6 +101,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the phase
+// completes or about a microsecond passes, instead of spinning on the issue slots.
+#ifndef SYN_WAIT_SLEEP_NS
+#define SYN_WAIT_SLEEP_NS 1000
+#endif
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    if (SYN_WAIT_SLEEP_NS == 0) return mbar_try_wait(bar, parity);
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"((uint32_t)SYN_WAIT_SLEEP_NS)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up after
 // SYN_WAIT_CYCLES, or as soon as *abort is set by another thread of the CTA; on
 // giving up it records the timeout, sets *abort and returns false.
@@ -109,7 +127,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* er
     if (mbar_try_wait(bar, parity)) return true;
     long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity)) return true;
         if (*abort) return false;
         if (clock64() - t0 > SYN_WAIT_CYCLES) {
             record_error(err, SYN_DEVERR_TIMEOUT);

@@ -20,6 +20,22 @@ cudaError_t launch_block_sums(int type, const void* W, int64_t n_out, int64_t nb
 cudaError_t launch_gemv(int type, const void* W, int64_t n_out, int64_t n_in, const float* X,
                         int64_t n_tok, float* Y, int* err, int sms, cudaStream_t s);
 
+// Decode products of up to GEMV_MAX_JOBS independent matrices in one launch.
+constexpr int GEMV_MAX_JOBS = 16;
+struct GemvDesc {
+    int type;
+    const void* W;
+    int64_t n_out, n_in;
+    const float* X;
+    float* Y;
+};
+cudaError_t launch_gemv_batch(int n, const GemvDesc* d, int64_t n_tok, int* err, int sms, cudaStream_t s);
+
+// Shared memory one token of a matrix's converted activations takes in the decode kernel;
+// a launch holds at most gemv_act_limit() bytes of them (all matrices, one token).
+int64_t gemv_act_bytes(int type, int64_t n_in);
+int64_t gemv_act_limit();
+
 // Prefill product on the tensor cores.  xh: n_tok x n_in fp16 activations (already
 // quantized and expanded).  Y is overwritten.
 cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, const void* xh,

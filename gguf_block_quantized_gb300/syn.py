@@ -50,6 +50,14 @@ EXPORTS = [
     ("syn_mul_mat_prefill_static", _i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
 ]
 
+class MatDesc(ctypes.Structure):
+    """syn_mat_desc: one product of a syn_mul_mat_batch group."""
+    _fields_ = [("type", ctypes.c_int), ("W", ctypes.c_void_p), ("n_out", ctypes.c_int64),
+                ("n_in", ctypes.c_int64), ("X", ctypes.c_void_p), ("Y", ctypes.c_void_p)]
+
+
+EXPORTS.append(("syn_mul_mat_batch", _i32, [_i32, ctypes.POINTER(MatDesc), _i64, _vp]))
+
 for _name, _res, _args in EXPORTS:
     _f = getattr(_L, _name)
     _f.restype = _res
@@ -135,6 +143,14 @@ def mul_mat(t: int, W, n_out: int, n_in: int, X, Y=None, stream=None):
         Y = torch.empty((n_tok, n_out), dtype=torch.float32, device=X.device)
     check(syn_mul_mat(t, _ptr(W), n_out, n_in, _ptr(X), n_tok, _ptr(Y), _stream(stream)), "syn_mul_mat")
     return Y
+
+
+def mul_mat_batch(items, n_tok: int, stream=None):
+    """items: list of (type, W, n_out, n_in, X, Y) with torch CUDA tensors; one grouped call."""
+    arr = (MatDesc * len(items))()
+    for k, (t, W, n_out, n_in, X, Y) in enumerate(items):
+        arr[k] = MatDesc(t, _ptr(W), n_out, n_in, _ptr(X), _ptr(Y))
+    check(syn_mul_mat_batch(len(items), arr, n_tok, _stream(stream)), "syn_mul_mat_batch")
 
 
 def block_sums(t: int, W, n_out: int, n_in: int, Xq, n_tok: int, stream=None):

@@ -131,6 +131,25 @@ SYN_API int syn_quantize_activations(int wtype, const float* X, int64_t n_tok, i
 SYN_API int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in,
                 const float* X, int64_t n_tok, float* Y, syn_stream_t stream);
 
+/* One product of a group (see syn_mul_mat_batch). */
+typedef struct {
+    int type;          /* SYN_TYPE_Q8_0, SYN_TYPE_Q4_K or SYN_TYPE_Q6_K */
+    const void* W;     /* n_out x n_in weights, 16-byte aligned */
+    int64_t n_out;
+    int64_t n_in;
+    const float* X;    /* n_tok x n_in activations, 16-byte aligned */
+    float* Y;          /* n_tok x n_out outputs, 16-byte aligned, not aliased */
+} syn_mat_desc;
+
+/* n independent products Y_i = ggml_mul_mat(W_i, X_i), all with n_tok tokens: the same
+ * result as n calls of syn_mul_mat.  In decode (n_tok <= the decode threshold) the group
+ * runs in as few launches as the decode kernel's limits allow (at most 16 matrices and
+ * 56 KiB of converted activations per launch), so the products of a layer (q, k, v, o,
+ * gate, up, down) share one launch and all SMs stream their weights together.  Larger
+ * n_tok runs each product on the prefill path.  Arguments are checked as for syn_mul_mat
+ * before anything is enqueued.  Asynchronous. */
+SYN_API int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_stream_t stream);
+
 /* Pre-size the prefill workspace of (current device, stream) for products with up to
  * max_n_in inputs and max_n_tok tokens, so that later syn_mul_mat calls allocate
  * nothing.  Synchronizes the device when it (re)allocates. */

@@ -207,6 +207,24 @@ def test_mul_mat_q8_0_row_not_multiple_of_256(syn):
         assert_close(Y, ref, bound, f"q8_0 n_in=800 {path}")
 
 
+@pytest.mark.parametrize("n_tok", [1, 3, 8])
+def test_mul_mat_batch_mixed_group(syn, n_tok):
+    """Grouped decode of matrices of all three formats and ragged shapes in one call."""
+    shapes = [(oracle.Q4_K, 300, 2048), (oracle.Q6_K, 77, 1024), (oracle.Q8_0, 129, 800),
+              (oracle.Q4_K, 5, 256), (oracle.Q6_K, 1000, 512), (oracle.Q8_0, 64, 4096)]
+    items, refs = [], []
+    for i, (wt, n_out, n_in) in enumerate(shapes):
+        Wq = oracle.quantize(wt, synth.normal(300 + i, (n_out, n_in), 0.02))
+        X = synth.normal(400 + i, (n_tok, n_in))
+        Yd = torch.full((n_tok, n_out), float("nan"), device="cuda")
+        items.append((wt, dev(Wq), n_out, n_in, dev(X), Yd))
+        refs.append((oracle.mul_mat(wt, Wq, n_out, n_in, X), tolerance(wt, Wq, n_in, X)))
+    syn.mul_mat_batch(items, n_tok)
+    for (wt, _, n_out, n_in, _, Yd), (ref, bound) in zip(items, refs):
+        assert_close(host(Yd), ref, bound, f"batch type {wt} {n_out}x{n_in}")
+    assert syn.device_status() == syn.OK
+
+
 def test_mul_mat_orientation_example_exact(syn):
     """ggml_mul_mat(A, B^T) = C^T with the examples/simple integers, exact on both paths."""
     A = np.array([[2, 8], [5, 1], [4, 2], [8, 6]], np.float32)
