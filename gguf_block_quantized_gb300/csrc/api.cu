@@ -256,8 +256,12 @@ int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in, const floa
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (n_tok <= g_gemv_max_tok.load() && syn::gemv_act_bytes(type, n_in) <= syn::gemv_act_limit()) {
-        rc = check_cuda(syn::launch_gemv(type, W, n_out, n_in, X, n_tok, Y, st->words, st->sms, s));
-        if (rc == SYN_OK) g_launches++;
+        const syn::GemvDesc d{type, W, n_out, n_in, X, Y};
+        void* ws;
+        rc = workspace_for(s, (size_t)syn::gemv_workspace_bytes(1, &d, n_tok), &ws);
+        if (rc) return rc;
+        rc = check_cuda(syn::launch_gemv_batch(1, &d, n_tok, ws, st->words, st->sms, s));
+        if (rc == SYN_OK) g_launches += 2;
         return rc;
     }
     void* ws;
@@ -303,8 +307,11 @@ int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_strea
     int64_t act = 0;
     auto flush = [&]() -> int {
         if (ng == 0) return SYN_OK;
-        const int r = check_cuda(syn::launch_gemv_batch(ng, group, n_tok, st->words, st->sms, s));
-        if (r == SYN_OK) g_launches++;
+        void* ws;
+        int r = workspace_for(s, (size_t)syn::gemv_workspace_bytes(ng, group, n_tok), &ws);
+        if (r) return r;
+        r = check_cuda(syn::launch_gemv_batch(ng, group, n_tok, ws, st->words, st->sms, s));
+        if (r == SYN_OK) g_launches += 2;
         ng = 0;
         act = 0;
         return r;

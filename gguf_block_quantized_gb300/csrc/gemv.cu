@@ -8,8 +8,8 @@
 // weight once per token group, so the kernel is bound by HBM bandwidth ("llama.cpp and
 // GGUF", CPU and Edge Inference: tokens/s <= bandwidth / model size).
 //
-// One CTA per SM.  The weight bytes of all matrices of the launch, row after row, are cut
-// at row boundaries into one contiguous range per warp of about equal size.
+// One CTA per SM.  The warps of the grid are dealt to the matrices of the launch in
+// proportion to their bytes; each warp streams a contiguous range of rows of one matrix.
 //   1. Each warp starts its 1-D bulk copies (cp.async.bulk, completion on an mbarrier)
 //      into its own 3-deep ring of shared-memory stages: a stage is a run of whole blocks,
 //      copied through a window widened to 16-byte boundaries (so 34- and 210-byte blocks
@@ -32,20 +32,21 @@ namespace syn {
 
 // Launch geometry (compile-time; the defaults are the measured best on GB300).
 #ifndef SYN_GV_WARPS
-#define SYN_GV_WARPS 8
+#define SYN_GV_WARPS 16
 #endif
 #ifndef SYN_GV_NS
-#define SYN_GV_NS 3
+#define SYN_GV_NS 2
 #endif
 #ifndef SYN_GV_STAGE
-#define SYN_GV_STAGE 8192
+#define SYN_GV_STAGE 4608
 #endif
 constexpr int GV_WARPS = SYN_GV_WARPS;
 constexpr int GV_NS = SYN_GV_NS;            // stages per warp ring
 constexpr int GV_STAGE = SYN_GV_STAGE;      // bytes of whole blocks per stage (at most)
 constexpr int GV_SLOT = GV_STAGE + 32;      // stage slot: data plus the alignment window
-// A stage must hold one warp step (32 blocks) of the widest block (Q6_K, 210 bytes).
-static_assert(GV_STAGE >= 32 * 210, "decode stage smaller than one warp step of blocks");
+// A stage must hold one warp step of every format: 16 blocks of Q4_K (144 bytes) or Q6_K
+// (210 bytes, two lanes per block), 64 blocks of Q8_0 (34 bytes, two blocks per lane).
+static_assert(GV_STAGE >= 16 * 210 && GV_STAGE >= 64 * 34, "decode stage smaller than one warp step");
 
 struct GemvJob {
     const uint8_t* W;
@@ -57,14 +58,22 @@ struct GemvJob {
     int64_t byte_begin;     // offset of this matrix in the concatenated weight bytes
     int n_in, type, nb, bb;
     int stage_blocks;       // blocks per stage
+    int bps;                // blocks per warp step: 16 (Q4_K, Q6_K: two lanes per block), 64 (Q8_0)
     int lg_nb;              // log2(nb) when rows are packed several per warp step, else -1
     int nbx;                // activation blocks per row
-    int act_q, act_d, act_s;  // shared-memory offsets of the converted activations
+    int units;              // conversion-kernel units (warp steps) per token
+    int unit_begin;         // first conversion unit of this matrix (all tokens of earlier ones)
+    int warp_begin, warp_end;  // the decode warps of this matrix
+    int ds;                 // per-token stride of the activation scales (floats, multiple of 4)
+    int act_q, act_d, act_s;  // shared-memory offsets of the converted activations (NT tokens)
+    uint8_t* actg;          // the same, for all n_tok tokens, in the global workspace:
+    int64_t g_d, g_s;       //   codes at actg, scales at actg + g_d, 16-sums at actg + g_s
 };
 
 struct GemvBatch {
     GemvJob job[GEMV_MAX_JOBS];
     int n_jobs;
+    int total_units;        // conversion-kernel units of all matrices and tokens
     int64_t total_bytes;
     int64_t n_tok;
     int* err;
@@ -104,98 +113,87 @@ __device__ __forceinline__ float group_sum(float v, int lg) {
 __device__ __forceinline__ int k_chunk(int B, int c) { return 256 * B + 16 * (c ^ (B & 7)); }
 __device__ __forceinline__ int q8_chunk(int B, int c) { return 32 * B + 16 * (c ^ ((B >> 2) & 1)); }
 
-// First row boundary at or after byte t of the concatenated weights: (job, row).
-__device__ __forceinline__ void row_at(const GemvBatch& b, int64_t t, int& j, int64_t& r) {
-    j = 0;
-    while (j < b.n_jobs - 1 && t >= b.job[j + 1].byte_begin) j++;
-    const GemvJob& J = b.job[j];
-    const int64_t off = t - J.byte_begin;
-    r = (off + J.row_bytes - 1) / J.row_bytes;
-    if (r >= J.n_out && j < b.n_jobs - 1) {
-        j++;
-        r = 0;
-    } else if (r > J.n_out) {
-        r = J.n_out;
-    }
-}
-
-// Convert activation rows t0 .. t0+NT-1 of jobs [ja, jb] into shared memory (swizzled).
-template <int NT>
-__device__ void act_to_smem(const GemvBatch& b, int ja, int jb, int64_t t0, uint8_t* smem) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int j = ja; j <= jb; j++) {
+// Convert every activation row of every matrix of the launch into the global workspace,
+// in the layout the decode kernel copies to shared memory: codes with swizzled 16-byte
+// chunks, block scales, 16-sums.  One warp per 256-block (K-quants) or per four 32-blocks
+// (Q8_0).  Lets the dependent decode launch start (programmatic dependent launch) at once.
+__global__ void __launch_bounds__(256) k_act_decode(const __grid_constant__ GemvBatch b) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int GW = (int)((gridDim.x * blockDim.x) >> 5);
+    // 32-bit index arithmetic only: 64-bit division runs on the (slow) fp64 pipe
+    for (int u = gw; u < b.total_units; u += GW) {
+        int j = 0;
+        while (j < b.n_jobs - 1 && u >= b.job[j + 1].unit_begin) j++;
+        const int r = u - b.job[j].unit_begin;
         const GemvJob& J = b.job[j];
-        int8_t* aq = reinterpret_cast<int8_t*>(smem + J.act_q);
-        float* ad = reinterpret_cast<float*>(smem + J.act_d);
-        int16_t* as = reinterpret_cast<int16_t*>(smem + J.act_s);
-        const int nbx = J.nbx;
+        int8_t* aq = reinterpret_cast<int8_t*>(J.actg);
+        float* ad = reinterpret_cast<float*>(J.actg + J.g_d);
+        int16_t* as = reinterpret_cast<int16_t*>(J.actg + J.g_s);
         if (J.type == SYN_Q8_0) {
-            const int steps = (nbx + 3) / 4;  // 4 blocks of 32 per warp step
-            for (int k = warp; k < NT * steps; k += GV_WARPS) {
-                const int t = k / steps, blk = (k % steps) * 4 + (lane >> 3), e = lane & 7;
-                float v[4] = {0.f, 0.f, 0.f, 0.f};
-                if (t0 + t < b.n_tok && blk < nbx) {
-                    const float4 x = *reinterpret_cast<const float4*>(J.X + (t0 + t) * J.n_in + blk * 32 + 4 * e);
-                    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-                }
-                uint16_t db;
-                bool fin;
-                const uint32_t q = q8_0_group(v, &db, &fin);
-                if (blk < nbx) {
-                    *reinterpret_cast<uint32_t*>(aq + t * J.n_in + q8_chunk(blk, e >> 2) + 4 * (e & 3)) = q;
-                    if (e == 0) ad[t * nbx + blk] = h2f_bits(db);
-                }
+            const int t = r / J.units;
+            const int blk = (r - t * J.units) * 4 + (lane >> 3), e = lane & 7;
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            if (blk < J.nbx) {
+                const float4 x = *reinterpret_cast<const float4*>(J.X + (int64_t)t * J.n_in + blk * 32 + 4 * e);
+                v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+            }
+            uint16_t db;
+            bool fin;
+            const uint32_t q = q8_0_group(v, &db, &fin);
+            if (blk < J.nbx) {
+                *reinterpret_cast<uint32_t*>(aq + (int64_t)t * J.n_in + q8_chunk(blk, e >> 2) + 4 * (e & 3)) = q;
+                if (e == 0) ad[(int64_t)t * J.ds + blk] = h2f_bits(db);
             }
         } else {
-            for (int k = warp; k < NT * nbx; k += GV_WARPS) {
-                const int t = k / nbx, blk = k % nbx;
-                float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                if (t0 + t < b.n_tok) {
-                    const float* x = J.X + (t0 + t) * J.n_in + blk * 256 + lane * 8;
-                    const float4 x0 = *reinterpret_cast<const float4*>(x);
-                    const float4 x1 = *reinterpret_cast<const float4*>(x + 4);
-                    v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
-                    v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
-                }
-                uint32_t w0, w1;
-                float dd;
-                int bs;
-                bool fin;
-                q8_k_warp(v, &w0, &w1, &dd, &bs, &fin);
-                *reinterpret_cast<uint2*>(aq + t * J.n_in + k_chunk(blk, lane >> 1) + 8 * (lane & 1)) =
-                    make_uint2(w0, w1);
-                if (lane == 0) ad[t * nbx + blk] = dd;
-                if ((lane & 1) == 0) as[(t * nbx + blk) * 16 + (lane >> 1)] = (int16_t)bs;
-            }
+            const int t = r / J.nbx;
+            const int blk = r - t * J.nbx;
+            const float* x = J.X + (int64_t)t * J.n_in + blk * 256 + lane * 8;
+            const float4 x0 = *reinterpret_cast<const float4*>(x);
+            const float4 x1 = *reinterpret_cast<const float4*>(x + 4);
+            const float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            uint32_t w0, w1;
+            float dd;
+            int bs;
+            bool fin;
+            q8_k_warp(v, &w0, &w1, &dd, &bs, &fin);
+            *reinterpret_cast<uint2*>(aq + (int64_t)t * J.n_in + k_chunk(blk, lane >> 1) + 8 * (lane & 1)) =
+                make_uint2(w0, w1);
+            if (lane == 0) ad[(int64_t)t * J.ds + blk] = dd;
+            if ((lane & 1) == 0) as[((int64_t)t * J.nbx + blk) * 16 + (lane >> 1)] = (int16_t)bs;
         }
     }
 }
 
 struct ActView {
     const int8_t* q;    // token 0 codes (swizzled chunks); token t at + t * n_in
-    const float* d;     // token 0 scales; token t at + t * nbx
+    const float* d;     // token 0 scales; token t at + t * ds
     const int16_t* s;   // token 0 16-sums; token t at + t * nbx * 16
-    int n_in, nbx;
+    int n_in, nbx, ds;
 };
 
-// ---- one whole block per lane: Q4_K (144 bytes, 16-byte aligned in shared memory) ----
+// ---- Q4_K: half a block per lane (h = 0: sub-blocks 0..3, h = 1: sub-blocks 4..7) ----
+// blk is 16-byte aligned in shared memory (144-byte blocks, 16-byte aligned rows).
 template <int NT>
-__device__ __forceinline__ void blk_q4_k(const uint8_t* blk, int B, const ActView& A, float acc[NT]) {
+__device__ __forceinline__ void lane_q4_k(const uint8_t* blk, int h, int B, const ActView& A, float acc[NT]) {
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
     const float D = h2f_bits(hdr.x & 0xFFFF), Dm = h2f_bits(hdr.x >> 16);
-    int sc[8], mn[8];
+    int sc[4], mn[4];
 #pragma unroll
     for (int j = 0; j < 4; j++) {
-        sc[j] = (hdr.y >> (8 * j)) & 63;
-        mn[j] = (hdr.z >> (8 * j)) & 63;
-        sc[j + 4] = ((hdr.w >> (8 * j)) & 15) | (((hdr.y >> (8 * j + 6)) & 3) << 4);
-        mn[j + 4] = ((hdr.w >> (8 * j + 4)) & 15) | (((hdr.z >> (8 * j + 6)) & 3) << 4);
+        const int lo_sc = (hdr.y >> (8 * j)) & 63, lo_mn = (hdr.z >> (8 * j)) & 63;
+        const int hi_sc = ((hdr.w >> (8 * j)) & 15) | (((hdr.y >> (8 * j + 6)) & 3) << 4);
+        const int hi_mn = ((hdr.w >> (8 * j + 4)) & 15) | (((hdr.z >> (8 * j + 6)) & 3) << 4);
+        sc[j] = h ? hi_sc : lo_sc;  // sub-block 4h + j
+        mn[j] = h ? hi_mn : lo_mn;
     }
     int At[NT];
 #pragma unroll
     for (int t = 0; t < NT; t++) At[t] = 0;
 #pragma unroll
-    for (int c = 0; c < 4; c++) {  // 32 code bytes: sub-block 2c (low nibbles), 2c+1 (high)
+    for (int cc = 0; cc < 2; cc++) {  // code chunk c = 2h + cc: sub-blocks 2c (low), 2c+1 (high)
+        const int c = 2 * h + cc;
         const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
         const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * c);
         const uint32_t q[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
@@ -214,110 +212,122 @@ __device__ __forceinline__ void blk_q4_k(const uint8_t* blk, int B, const ActVie
                 dl = dp4a(q[i] & 0x0F0F0F0Fu, xl[i], dl);
                 dh = dp4a((q[i] >> 4) & 0x0F0F0F0Fu, xh[i], dh);
             }
-            At[t] += sc[2 * c] * dl + sc[2 * c + 1] * dh;
+            At[t] += sc[2 * cc] * dl + sc[2 * cc + 1] * dh;
         }
     }
 #pragma unroll
     for (int t = 0; t < NT; t++) {
-        const uint4* sp = reinterpret_cast<const uint4*>(A.s + (t * A.nbx + B) * 16);
-        const uint4 s0 = sp[0], s1 = sp[1];
-        const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        // 16-sums of sub-blocks 4h .. 4h+3 (two per sub-block of 32)
+        const uint4 sv = *reinterpret_cast<const uint4*>(A.s + (t * A.nbx + B) * 16 + 8 * h);
+        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
         int Bm = 0;
 #pragma unroll
-        for (int j = 0; j < 8; j++)  // sub-block j of 32 = 16-sums 2j, 2j+1 = halves of word j
-            Bm += mn[j] * ((int)(int16_t)(sw[j] & 0xFFFF) + (int)(int16_t)(sw[j] >> 16));
-        acc[t] = fmaf(A.d[t * A.nbx + B], D * (float)At[t] - Dm * (float)Bm, acc[t]);
+        for (int j = 0; j < 4; j++) Bm += mn[j] * ((int)(int16_t)(sw[j] & 0xFFFF) + (int)(int16_t)(sw[j] >> 16));
+        acc[t] = fmaf(A.d[t * A.ds + B], D * (float)At[t] - Dm * (float)Bm, acc[t]);
     }
 }
 
-// ---- one whole block per lane: Q6_K (210 bytes, 2-byte aligned) ----
+// ---- Q6_K: half a block per lane (weights 128H .. 128H+127); blk 2-byte aligned ----
 template <int NT>
-__device__ __forceinline__ void blk_q6_k(const uint8_t* blk, int B, const ActView& A, float acc[NT]) {
+__device__ __forceinline__ void lane_q6_k(const uint8_t* blk, int H, int B, const ActView& A, float acc[NT]) {
     const float D = h2f_bits(*reinterpret_cast<const uint16_t*>(blk + 208));
-    uint32_t scw[4];
-    lds_words_any<4>(blk + 192, scw);
-    int Ct[NT];
-#pragma unroll
-    for (int t = 0; t < NT; t++) Ct[t] = 0;
-#pragma unroll
-    for (int H = 0; H < 2; H++) {
-        uint32_t ql[16], qh[8];
-        lds_words_any<16>(blk + 64 * H, ql);
-        lds_words_any<8>(blk + 128 + 32 * H, qh);
-        // quarter k of the half, l = 4w..4w+3 (w = 4*half + i): sub-block 8H + 2k + half
-#pragma unroll
-        for (int t = 0; t < NT; t++) {
-            const int8_t* xq = A.q + t * A.n_in;
-            int dot[8];
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-#pragma unroll
-                for (int half = 0; half < 2; half++) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(xq + k_chunk(B, 8 * H + 2 * k + half));
-                    const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-                    int dsum = 0;
-#pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        const int w = 4 * half + i;
-                        const uint32_t a = (k & 1) ? ql[8 + w] : ql[w];
-                        const uint32_t lo = (k >= 2) ? ((a >> 4) & 0x0F0F0F0Fu) : (a & 0x0F0F0F0Fu);
-                        const uint32_t hi = (k >= 2 ? (qh[w] >> (2 * k - 4)) : (qh[w] << (4 - 2 * k))) & 0x30303030u;
-                        dsum = dp4a(lo | hi, xw[i], dsum);
-                    }
-                    dot[2 * k + half] = dsum;
-                }
-            }
-            const uint4 s = *reinterpret_cast<const uint4*>(A.s + (t * A.nbx + B) * 16 + 8 * H);
-            const uint32_t sw[4] = {s.x, s.y, s.z, s.w};  // 16-sums of sub-blocks 8H .. 8H+7
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const int bs = (int)(int16_t)((sw[j >> 1] >> (16 * (j & 1))) & 0xFFFF);
-                const int scj = (int)(int8_t)(scw[(8 * H + j) >> 2] >> (8 * ((8 * H + j) & 3)));
-                Ct[t] += scj * (dot[j] - 32 * bs);
-            }
-        }
-    }
-#pragma unroll
-    for (int t = 0; t < NT; t++) acc[t] = fmaf(A.d[t * A.nbx + B] * D, (float)Ct[t], acc[t]);
-}
-
-// ---- one whole block per lane: Q8_0 (34 bytes, 2-byte aligned) ----
-template <int NT>
-__device__ __forceinline__ void blk_q8_0(const uint8_t* blk, int B, const ActView& A, float acc[NT]) {
-    const float Dw = h2f_bits(*reinterpret_cast<const uint16_t*>(blk));
-    uint32_t w[8];
-    lds_words_any<8>(blk + 2, w);
+    uint32_t scw[2], ql[16], qh[8];
+    lds_words_any<2>(blk + 192 + 8 * H, scw);  // scales of sub-blocks 8H .. 8H+7
+    lds_words_any<16>(blk + 64 * H, ql);
+    lds_words_any<8>(blk + 128 + 32 * H, qh);
 #pragma unroll
     for (int t = 0; t < NT; t++) {
         const int8_t* xq = A.q + t * A.n_in;
-        const uint4 x0 = *reinterpret_cast<const uint4*>(xq + q8_chunk(B, 0));
-        const uint4 x1 = *reinterpret_cast<const uint4*>(xq + q8_chunk(B, 1));
-        int I = dp4a(w[0], x0.x, 0);
-        I = dp4a(w[1], x0.y, I);
-        I = dp4a(w[2], x0.z, I);
-        I = dp4a(w[3], x0.w, I);
-        I = dp4a(w[4], x1.x, I);
-        I = dp4a(w[5], x1.y, I);
-        I = dp4a(w[6], x1.z, I);
-        I = dp4a(w[7], x1.w, I);
-        acc[t] = fmaf(Dw * A.d[t * A.nbx + B], (float)I, acc[t]);
+        // quarter k of the half, l = 4w..4w+3 (w = 4*half + i): sub-block 8H + 2k + half
+        int C = 0;
+        const uint4 sv = *reinterpret_cast<const uint4*>(A.s + (t * A.nbx + B) * 16 + 8 * H);
+        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+#pragma unroll
+            for (int half = 0; half < 2; half++) {
+                const int j = 2 * k + half;
+                const uint4 x = *reinterpret_cast<const uint4*>(xq + k_chunk(B, 8 * H + j));
+                const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+                int dsum = 0;
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const int w = 4 * half + i;
+                    const uint32_t a = (k & 1) ? ql[8 + w] : ql[w];
+                    const uint32_t lo = (k >= 2) ? ((a >> 4) & 0x0F0F0F0Fu) : (a & 0x0F0F0F0Fu);
+                    const uint32_t hi = (k >= 2 ? (qh[w] >> (2 * k - 4)) : (qh[w] << (4 - 2 * k))) & 0x30303030u;
+                    dsum = dp4a(lo | hi, xw[i], dsum);
+                }
+                const int bs = (int)(int16_t)((sw[j >> 1] >> (16 * (j & 1))) & 0xFFFF);
+                const int scj = (int)(int8_t)(scw[j >> 2] >> (8 * (j & 3)));
+                C += scj * (dsum - 32 * bs);
+            }
+        }
+        acc[t] = fmaf(A.d[t * A.ds + B] * D, (float)C, acc[t]);
     }
 }
 
+// ---- Q8_0: n (1 or 2) consecutive 34-byte blocks per lane; blk 2-byte aligned ----
 template <int NT>
-__device__ __forceinline__ void block_dot(int type, const uint8_t* blk, int B, const ActView& A, float acc[NT]) {
-    if (type == SYN_Q4_K) blk_q4_k<NT>(blk, B, A, acc);
-    else if (type == SYN_Q6_K) blk_q6_k<NT>(blk, B, A, acc);
-    else blk_q8_0<NT>(blk, B, A, acc);
+__device__ __forceinline__ void lane_q8_0(const uint8_t* blk, int n, int B, const ActView& A, float acc[NT]) {
+#pragma unroll
+    for (int e = 0; e < 2; e++) {
+        if (e >= n) break;
+        const uint8_t* p = blk + 34 * e;
+        const float Dw = h2f_bits(*reinterpret_cast<const uint16_t*>(p));
+        uint32_t w[8];
+        lds_words_any<8>(p + 2, w);
+#pragma unroll
+        for (int t = 0; t < NT; t++) {
+            const int8_t* xq = A.q + t * A.n_in;
+            const uint4 x0 = *reinterpret_cast<const uint4*>(xq + q8_chunk(B + e, 0));
+            const uint4 x1 = *reinterpret_cast<const uint4*>(xq + q8_chunk(B + e, 1));
+            int I = dp4a(w[0], x0.x, 0);
+            I = dp4a(w[1], x0.y, I);
+            I = dp4a(w[2], x0.z, I);
+            I = dp4a(w[3], x0.w, I);
+            I = dp4a(w[4], x1.x, I);
+            I = dp4a(w[5], x1.y, I);
+            I = dp4a(w[6], x1.z, I);
+            I = dp4a(w[7], x1.w, I);
+            acc[t] = fmaf(Dw * A.d[t * A.ds + B + e], (float)I, acc[t]);
+        }
+    }
 }
 
-// Position in a warp's range: matrix j, row, block column.  A stage is either whole rows
-// or (rows wider than a stage) a run of blocks of one row.
-struct Cursor {
-    int j;
-    int64_t row, rows_end;
-    int bcol;
-};
+// This lane's share of warp step `first` .. of a run of blocks: K-quants take half a block
+// per lane (block first + lane/2, part lane%2); Q8_0 takes two blocks per lane.
+// `avail` = blocks of the run from `first` on; the activation block of run block i is
+// (B0 + i) & bmask (bmask = nb - 1 when the run holds several whole rows).
+template <int NT>
+__device__ __forceinline__ void lane_step(int type, const uint8_t* base, int bb, int first, int avail, int B0,
+                                          int bmask, const ActView& A, float acc[NT]) {
+    const int lane = threadIdx.x & 31;
+    if (type == SYN_Q8_0) {
+        const int k = 2 * lane;
+        if (k < avail) lane_q8_0<NT>(base + (first + k) * bb, min(2, avail - k), (B0 + k) & bmask, A, acc);
+    } else {
+        const int k = lane >> 1;
+        if (k < avail) {
+            const int B = (B0 + k) & bmask;
+            if (type == SYN_Q4_K) lane_q4_k<NT>(base + (first + k) * bb, lane & 1, B, A, acc);
+            else lane_q6_k<NT>(base + (first + k) * bb, lane & 1, B, A, acc);
+        }
+    }
+}
+
+// The warps of the grid are dealt to the matrices in proportion to their bytes (at least
+// one each, boundaries computed on the host); a matrix's rows are split evenly among its
+// warps.  Returns this warp's matrix and rows [r0, r1) (empty when the matrix has fewer rows
+// than warps).  32-bit arithmetic only: 64-bit division runs on the (slow) fp64 pipe.
+__device__ __forceinline__ void warp_share(const GemvBatch& b, int gw, int& j, int64_t& r0, int64_t& r1) {
+    j = 0;
+    while (j < b.n_jobs - 1 && gw >= b.job[j].warp_end) j++;
+    const int nw = b.job[j].warp_end - b.job[j].warp_begin, i = gw - b.job[j].warp_begin;
+    const int n = (int)b.job[j].n_out, q = n / nw, rem = n - q * nw;
+    r0 = (int64_t)q * i + (rem * i) / nw;
+    r1 = (int64_t)q * (i + 1) + (rem * (i + 1)) / nw;
+}
 
 template <int NT>
 __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant__ GemvBatch b) {
@@ -330,85 +340,73 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
     const uint32_t bar0 = smem_u32(smem + b.off_bar) + warp * GV_NS * 8;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + b.off_flag);
 
-    if (threadIdx.x == 0) *abort_flag = 0;
+    const uint32_t act_bar = smem_u32(smem + b.off_flag + 8);
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        mbar_init(act_bar, 1);
+    }
     if (lane == 0)
         for (int s = 0; s < GV_NS; s++) mbar_init(bar0 + 8 * s, 1);
     fence_mbar_init();
 
-    // this warp's rows: from (j0, r0) up to (j1, r1), cut at row boundaries
-    int j0, j1, ja, jb;
-    int64_t r0, r1, ra, rb;
-    row_at(b, b.total_bytes * gw / GW, j0, r0);
-    row_at(b, b.total_bytes * (gw + 1) / GW, j1, r1);
-    // the matrices any warp of this CTA touches (their activations are converted below)
-    row_at(b, b.total_bytes * (blockIdx.x * GV_WARPS) / GW, ja, ra);
-    row_at(b, b.total_bytes * ((blockIdx.x + 1) * GV_WARPS) / GW, jb, rb);
-    if (rb == 0 && jb > ja) jb--;
-
+    // this warp's matrix and rows; the matrices of the CTA's first and last warps bound
+    // the activations the CTA converts
+    int jw, ja, jb;
+    int64_t r0, r1, t0_, t1_;
+    warp_share(b, gw, jw, r0, r1);
+    warp_share(b, blockIdx.x * GV_WARPS, ja, t0_, t1_);
+    warp_share(b, blockIdx.x * GV_WARPS + GV_WARPS - 1, jb, t0_, t1_);
     __syncthreads();
 
-    // start of the range; skips matrices with no rows in it; false when empty
-    auto begin = [&](Cursor& c) -> bool {
-        c.j = j0;
-        c.row = r0;
-        c.bcol = 0;
-        while (true) {
-            c.rows_end = c.j == j1 ? r1 : b.job[c.j].n_out;
-            if (c.row < c.rows_end) return true;
-            if (c.j >= j1) return false;
-            c.j++;
-            c.row = 0;
-        }
-    };
-    // blocks (and whole rows, or 0 for a run inside one row) of the stage at c
-    auto extent = [&](const Cursor& c, int& nblk, int& nrows) {
-        const GemvJob& J = b.job[c.j];
-        if (J.stage_blocks >= J.nb) {
-            nrows = (int)min((int64_t)(J.stage_blocks / J.nb), c.rows_end - c.row);
-            nblk = nrows * J.nb;
+    // the matrix, in registers for the whole launch
+    const GemvJob& Jp = b.job[jw];
+    const uint8_t* const W = Jp.W;
+    float* const Y = Jp.Y;
+    const int64_t n_out = Jp.n_out, total_floor16 = Jp.total_floor16;
+    const int type = Jp.type, nb = Jp.nb, bb = Jp.bb, lg = Jp.lg_nb, bps = Jp.bps;
+    const int sblk = Jp.stage_blocks;
+    const int rps = sblk >= nb ? sblk / nb : 0;  // whole rows per stage (0: runs of one row)
+    const ActView A{reinterpret_cast<const int8_t*>(smem + Jp.act_q), reinterpret_cast<const float*>(smem + Jp.act_d),
+                    reinterpret_cast<const int16_t*>(smem + Jp.act_s), Jp.n_in, Jp.nbx, Jp.ds};
+
+    // stage extent at (row, bcol): blocks and whole rows (0 for a run inside one row)
+    auto extent = [&](int64_t row, int bcol, int& nblk, int& nrows) {
+        if (rps > 0) {
+            nrows = (int)min((int64_t)rps, r1 - row);
+            nblk = nrows * nb;
         } else {
             nrows = 0;
-            nblk = min(J.stage_blocks, J.nb - c.bcol);
+            nblk = min(sblk, nb - bcol);
         }
     };
-    auto advance = [&](Cursor& c, int nblk, int nrows) -> bool {
+    auto advance = [&](int64_t& row, int& bcol, int nblk, int nrows) {
         if (nrows > 0) {
-            c.row += nrows;
+            row += nrows;
         } else {
-            c.bcol += nblk;
-            if (c.bcol == b.job[c.j].nb) {
-                c.bcol = 0;
-                c.row++;
+            bcol += nblk;
+            if (bcol == nb) {
+                bcol = 0;
+                row++;
             }
         }
-        while (c.row >= c.rows_end) {
-            if (c.j >= j1) return false;
-            c.j++;
-            c.row = 0;
-            c.bcol = 0;
-            c.rows_end = c.j == j1 ? r1 : b.job[c.j].n_out;
-        }
-        return true;
     };
-
-    // bulk copy of the stage at cursor c into ring slot s
-    auto issue = [&](const Cursor& c, int nblk, uint32_t s) {
-        const GemvJob& J = b.job[c.j];
-        const int64_t src = (c.row * J.nb + c.bcol) * (int64_t)J.bb;
-        const int64_t len = (int64_t)nblk * J.bb;
+    // bulk copy of the stage at (row, bcol) into ring slot s
+    auto issue = [&](int64_t row, int bcol, int nblk, uint32_t s) {
+        const int64_t src = (row * nb + bcol) * (int64_t)bb;
+        const int64_t len = (int64_t)nblk * bb;
         const int64_t a0 = src & ~int64_t(15);
         if (lane == 0) {
             fence_proxy_async_smem();
             int64_t a1 = (src + len + 15) & ~int64_t(15);
-            if (a1 > J.total_floor16) a1 = J.total_floor16;
+            if (a1 > total_floor16) a1 = total_floor16;
             const uint32_t bytes = a1 > a0 ? (uint32_t)(a1 - a0) : 0u;
             const uint32_t bar = bar0 + 8 * s;
             mbar_arrive_expect_tx(bar, bytes);
-            if (bytes) bulk_g2s(ring_addr + s * GV_SLOT, J.W + a0, bytes, bar);
+            if (bytes) bulk_g2s(ring_addr + s * GV_SLOT, W + a0, bytes, bar);
         }
-        if (src + len > J.total_floor16) {  // bytes past the last 16-byte boundary of W
-            const int64_t from = J.total_floor16 > a0 ? J.total_floor16 : a0;
-            for (int64_t k = from + lane; k < src + len; k += 32) ring[s * GV_SLOT + (k - a0)] = J.W[k];
+        if (src + len > total_floor16) {  // bytes past the last 16-byte boundary of W
+            const int64_t from = total_floor16 > a0 ? total_floor16 : a0;
+            for (int64_t k = from + lane; k < src + len; k += 32) ring[s * GV_SLOT + (k - a0)] = W[k];
             __syncwarp();
         }
     };
@@ -417,33 +415,53 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
     bool failed = false;
     for (int64_t t0 = 0; t0 < b.n_tok && !failed; t0 += NT) {
         // weights first: the copies are in flight while the activations are converted
-        Cursor ic;
-        bool more_i = begin(ic);
+        int64_t irow = r0;
+        int ibcol = 0;
         uint32_t qi = seq;
-        for (int k = 0; k < GV_NS - 1 && more_i; k++) {
+        for (int k = 0; k < GV_NS - 1 && irow < r1; k++) {
             int nblk, nrows;
-            extent(ic, nblk, nrows);
-            issue(ic, nblk, (qi++) % GV_NS);
-            more_i = advance(ic, nblk, nrows);
+            extent(irow, ibcol, nblk, nrows);
+            issue(irow, ibcol, nblk, (qi++) % GV_NS);
+            advance(irow, ibcol, nblk, nrows);
         }
+        // the converted activations of tokens t0.. of the CTA's matrices: written by the
+        // conversion kernel this launch depends on, so wait for it first
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         __syncthreads();  // every warp is done with the previous token group's activations
-        act_to_smem<NT>(b, ja, jb, t0, smem);
-        __syncthreads();
-        if (*abort_flag) break;
+        const uint32_t act_parity = (uint32_t)((t0 / NT) & 1);
+        if (threadIdx.x == 0) {
+            const int64_t nt = min((int64_t)NT, b.n_tok - t0);
+            uint32_t tx = 0;
+            for (int j = ja; j <= jb; j++) {
+                const GemvJob& J = b.job[j];
+                tx += (uint32_t)(nt * J.n_in + nt * J.ds * 4 + (J.type == SYN_Q8_0 ? 0 : nt * (J.n_in / 8)));
+            }
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(act_bar, tx);
+            for (int j = ja; j <= jb; j++) {
+                const GemvJob& J = b.job[j];
+                bulk_g2s(smem_u32(smem + J.act_q), J.actg + t0 * J.n_in, (uint32_t)(nt * J.n_in), act_bar);
+                bulk_g2s(smem_u32(smem + J.act_d), J.actg + J.g_d + t0 * J.ds * 4, (uint32_t)(nt * J.ds * 4), act_bar);
+                if (J.type != SYN_Q8_0)
+                    bulk_g2s(smem_u32(smem + J.act_s), J.actg + J.g_s + t0 * (J.n_in / 8), (uint32_t)(nt * (J.n_in / 8)),
+                             act_bar);
+            }
+        }
+        if (!mbar_wait(act_bar, act_parity, b.err, abort_flag)) break;
 
-        Cursor cc;
-        bool more_c = begin(cc);
         float acc[NT];
 #pragma unroll
         for (int t = 0; t < NT; t++) acc[t] = 0.f;
+        int64_t crow = r0;
+        int cbcol = 0;
         uint32_t qc = seq;
-        while (more_c) {
-            if (more_i) {
+        while (crow < r1) {
+            if (irow < r1) {
                 int nblk, nrows;
-                extent(ic, nblk, nrows);
+                extent(irow, ibcol, nblk, nrows);
                 __syncwarp();
-                issue(ic, nblk, (qi++) % GV_NS);
-                more_i = advance(ic, nblk, nrows);
+                issue(irow, ibcol, nblk, (qi++) % GV_NS);
+                advance(irow, ibcol, nblk, nrows);
             }
             const uint32_t s = qc % GV_NS;
             if (!mbar_wait(bar0 + 8 * s, (qc / GV_NS) & 1, b.err, abort_flag)) {
@@ -459,56 +477,49 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
                 break;
             }
             qc++;
-            const GemvJob& J = b.job[cc.j];
-            const int type = J.type, nb = J.nb, bb = J.bb, lg = J.lg_nb;
-            const ActView A{reinterpret_cast<const int8_t*>(smem + J.act_q),
-                            reinterpret_cast<const float*>(smem + J.act_d),
-                            reinterpret_cast<const int16_t*>(smem + J.act_s), J.n_in, J.nbx};
-            float* Y = J.Y;
-            const int64_t n_out = J.n_out;
             int nblk, nrows;
-            extent(cc, nblk, nrows);
+            extent(crow, cbcol, nblk, nrows);
             if (nblk <= 0) {  // cannot happen with a valid geometry; never spin without progress
                 failed = true;
                 break;
             }
-            const uint8_t* sbase = ring + s * GV_SLOT + (int)(((cc.row * nb + cc.bcol) * (int64_t)bb) & 15);
+            const uint8_t* sbase = ring + s * GV_SLOT + (int)(((crow * nb + cbcol) * (int64_t)bb) & 15);
             if (lg >= 0) {
-                // rows of 2^lg <= 32 blocks: 32 >> lg rows per warp step, lane = (row, block)
-                for (int s0 = 0; s0 < nblk; s0 += 32) {
-                    const int sidx = s0 + lane;
-                    if (sidx < nblk) block_dot<NT>(type, sbase + sidx * bb, sidx & (nb - 1), A, acc);
+                // rows of 2^lg <= bps blocks: bps >> lg rows per warp step; the lanes of a row
+                // form an aligned group of 2^lgl lanes
+                const int lgl = type == SYN_Q8_0 ? lg - 1 : lg + 1;
+                for (int s0 = 0; s0 < nblk; s0 += bps) {
+                    lane_step<NT>(type, sbase, bb, s0, nblk - s0, s0, nb - 1, A, acc);
+                    const int mine = s0 + (type == SYN_Q8_0 ? 2 * lane : lane >> 1);  // first block of this lane
 #pragma unroll
                     for (int t = 0; t < NT; t++) {
-                        const float v = group_sum(acc[t], lg);
-                        if ((lane & (nb - 1)) == 0 && sidx < nblk && t0 + t < b.n_tok)
-                            Y[(t0 + t) * n_out + cc.row + (sidx >> lg)] = v;
+                        const float v = group_sum(acc[t], lgl);
+                        if ((lane & ((1 << lgl) - 1)) == 0 && mine < nblk && t0 + t < b.n_tok)
+                            Y[(t0 + t) * n_out + crow + (mine >> lg)] = v;
                         acc[t] = 0.f;
                     }
                 }
             } else {
-                // wider rows: each row (or run of one row) takes ceil(blocks / 32) warp steps
+                // wider rows: each row (or run of one row) takes ceil(blocks / bps) warp steps
                 const int per_row = nrows > 0 ? nb : nblk;
                 const int rows = nrows > 0 ? nrows : 1;
-                const int bstart = nrows > 0 ? 0 : cc.bcol;
+                const int bstart = nrows > 0 ? 0 : cbcol;
                 for (int r = 0; r < rows; r++) {
                     const uint8_t* rowp = sbase + (int64_t)r * nb * bb;
-                    for (int s0 = 0; s0 < per_row; s0 += 32) {
-                        const int kb = s0 + lane;
-                        if (kb < per_row) block_dot<NT>(type, rowp + kb * bb, bstart + kb, A, acc);
-                    }
-                    if (nrows > 0 || cc.bcol + nblk == nb) {
+                    for (int s0 = 0; s0 < per_row; s0 += bps)
+                        lane_step<NT>(type, rowp, bb, s0, per_row - s0, bstart + s0, -1, A, acc);
+                    if (nrows > 0 || cbcol + nblk == nb) {
 #pragma unroll
                         for (int t = 0; t < NT; t++) {
                             const float v = warp_sum(acc[t]);
-                            if (lane == 0 && t0 + t < b.n_tok) Y[(t0 + t) * n_out + cc.row + r] = v;
+                            if (lane == 0 && t0 + t < b.n_tok) Y[(t0 + t) * n_out + crow + r] = v;
                             acc[t] = 0.f;
                         }
                     }
                 }
             }
             __syncwarp();
-            more_c = advance(cc, nblk, nrows);
+            advance(crow, cbcol, nblk, nrows);
         }
         seq = qi;
     }
@@ -526,8 +537,9 @@ static_assert(GEMV_ACT_BUDGET >= 8 * 1024, "decode ring leaves too little shared
 int64_t gemv_act_limit() { return GEMV_ACT_BUDGET; }
 
 static int64_t act_bytes_per_token(int type, int64_t n_in) {
-    if (type == SYN_Q8_0) return n_in + (n_in / 32) * 4;
-    return n_in + (n_in / 256) * 4 + (n_in / 16) * 2;
+    const int64_t nbx = n_in / (type == SYN_Q8_0 ? 32 : 256), ds = (nbx + 3) & ~int64_t(3);
+    if (type == SYN_Q8_0) return n_in + ds * 4;
+    return n_in + ds * 4 + (n_in / 16) * 2;
 }
 
 template <int NT>
@@ -538,7 +550,7 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
         J.act_q = (int)off;
         off = up16(off + (int64_t)NT * J.n_in);
         J.act_d = (int)off;
-        off = up16(off + (int64_t)NT * J.nbx * 4);
+        off = up16(off + (int64_t)NT * J.ds * 4);
         J.act_s = (int)off;
         off = up16(off + (J.type == SYN_Q8_0 ? 0 : (int64_t)NT * (J.n_in / 16) * 2));
     }
@@ -548,7 +560,7 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
     b.off_bar = (int)off;
     off += GV_WARPS * GV_NS * 8;
     b.off_flag = (int)off;
-    off += 16;
+    off += 16;  // abort flag, activation barrier
     const size_t smem = (size_t)off;
     if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
     auto kern = k_gemv<NT>;
@@ -558,8 +570,47 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    kern<<<sms, GV_WARPS * 32, smem, s>>>(b);
-    return cudaGetLastError();
+    // warps per matrix, in proportion to bytes, at least one each
+    const int GW = sms * GV_WARPS;
+    int w = 0;
+    int64_t cum = 0;
+    for (int j = 0; j < b.n_jobs; j++) {
+        GemvJob& J = b.job[j];
+        cum += J.n_out * J.row_bytes;
+        int we = (int)((double)cum * GW / (double)b.total_bytes);
+        we = std::max(we, w + 1);
+        we = std::min(we, GW - (b.n_jobs - 1 - j));
+        if (j == b.n_jobs - 1) we = GW;
+        J.warp_begin = w;
+        J.warp_end = we;
+        w = we;
+    }
+    // the conversion kernel: a plain launch, ordered after everything before it
+    int64_t units = 0;
+    for (int j = 0; j < b.n_jobs; j++) {
+        GemvJob& J = b.job[j];
+        J.units = J.type == SYN_Q8_0 ? (J.nbx + 3) / 4 : J.nbx;
+        J.unit_begin = (int)units;
+        units += b.n_tok * J.units;
+    }
+    b.total_units = (int)units;
+    const int64_t act_ctas = std::min<int64_t>((units + 7) / 8, (int64_t)sms * 4);
+    k_act_decode<<<(unsigned)std::max<int64_t>(act_ctas, 1), 256, 0, s>>>(b);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // the decode kernel, launched as its programmatic dependent: it streams weights (which the
+    // conversion kernel does not touch) before waiting for the converted activations
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sms);
+    cfg.blockDim = dim3(GV_WARPS * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, b);
 }
 
 // One matrix of a launch.  Rows of a power-of-two number of blocks up to 32 are packed
@@ -578,33 +629,52 @@ static void make_job(GemvJob& J, const GemvDesc& d, int64_t byte_begin) {
     J.total_floor16 = (d.n_out * J.row_bytes) & ~int64_t(15);
     J.byte_begin = byte_begin;
     J.nbx = (int)(d.n_in / (d.type == SYN_Q8_0 ? 32 : 256));
-    const int fit = GV_STAGE / J.bb;  // >= 32 for every format
+    J.ds = (J.nbx + 3) & ~3;
+    J.bps = d.type == SYN_Q8_0 ? 64 : 16;
+    const int fit = GV_STAGE / J.bb;  // >= bps for every format (static_assert above)
     J.lg_nb = -1;
-    if (fit < 32) {  // excluded by the static_assert on GV_STAGE; kept as a guard
-        J.stage_blocks = std::max(1, std::min(fit, J.nb));
-    } else if (J.nb <= 32 && (J.nb & (J.nb - 1)) == 0) {
+    const bool packed = J.nb <= J.bps && (J.nb & (J.nb - 1)) == 0 && !(d.type == SYN_Q8_0 && J.nb < 2);
+    if (packed) {
         int lg = 0;
         while ((1 << lg) < J.nb) lg++;
         J.lg_nb = lg;
-        J.stage_blocks = (fit / 32) * 32;  // whole rows, whole warp steps
+        J.stage_blocks = (fit / J.bps) * J.bps;  // whole rows, whole warp steps
     } else if (J.nb <= fit) {
         J.stage_blocks = (fit / J.nb) * J.nb;  // whole rows
     } else {
-        J.stage_blocks = (fit / 32) * 32;  // runs of one row
+        J.stage_blocks = (fit / J.bps) * J.bps;  // runs of one row
     }
 }
 
 int64_t gemv_act_bytes(int type, int64_t n_in) { return act_bytes_per_token(type, n_in) + 64; }
 
-cudaError_t launch_gemv_batch(int n, const GemvDesc* d, int64_t n_tok, int* err, int sms, cudaStream_t s) {
+// Global workspace of one matrix's converted activations (all tokens).
+static int64_t act_global_bytes(int type, int64_t n_in, int64_t n_tok) {
+    const int64_t nbx = n_in / (type == SYN_Q8_0 ? 32 : 256), ds = (nbx + 3) & ~int64_t(3);
+    return up16(n_tok * n_in) + up16(n_tok * ds * 4) + (type == SYN_Q8_0 ? 0 : up16(n_tok * (n_in / 8))) + 256;
+}
+
+int64_t gemv_workspace_bytes(int n, const GemvDesc* d, int64_t n_tok) {
+    int64_t bytes = 0;
+    for (int j = 0; j < n; j++) bytes += act_global_bytes(d[j].type, d[j].n_in, n_tok);
+    return bytes + 256;
+}
+
+cudaError_t launch_gemv_batch(int n, const GemvDesc* d, int64_t n_tok, void* ws, int* err, int sms, cudaStream_t s) {
     if (n < 1 || n > GEMV_MAX_JOBS) return cudaErrorInvalidValue;
     GemvBatch b{};
     b.n_jobs = n;
     b.n_tok = n_tok;
     b.err = err;
     int64_t bytes = 0, act = 0;
+    uint8_t* g = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255));
     for (int j = 0; j < n; j++) {
         make_job(b.job[j], d[j], bytes);
+        GemvJob& J = b.job[j];
+        J.actg = g;
+        J.g_d = up16(n_tok * J.n_in);
+        J.g_s = J.g_d + up16(n_tok * J.ds * 4);
+        g += (act_global_bytes(d[j].type, d[j].n_in, n_tok) + 255) & ~int64_t(255);
         bytes += d[j].n_out * b.job[j].row_bytes;
         act += gemv_act_bytes(d[j].type, d[j].n_in);
     }
@@ -621,9 +691,9 @@ cudaError_t launch_gemv_batch(int n, const GemvDesc* d, int64_t n_tok, int* err,
 }
 
 cudaError_t launch_gemv(int type, const void* W, int64_t n_out, int64_t n_in, const float* X, int64_t n_tok,
-                        float* Y, int* err, int sms, cudaStream_t s) {
+                        float* Y, void* ws, int* err, int sms, cudaStream_t s) {
     const GemvDesc d{type, W, n_out, n_in, X, Y};
-    return launch_gemv_batch(1, &d, n_tok, err, sms, s);
+    return launch_gemv_batch(1, &d, n_tok, ws, err, sms, s);
 }
 
 }  // namespace syn

@@ -8,6 +8,7 @@ Cases (synthetic weights ~N(0, 0.02), activations ~N(0, 1)):
   gemv_q8_0_wide     Q8_0 16384 x 8192, 1 token     (143 MB)
   gemm_q4k_ffn_up    Q4_K 14336 x 4096, 512 tokens  (prefill, tensor cores)
   gemm_q4k_ffn_down  Q4_K 4096 x 14336, 512 tokens
+  gemv_llama1b_layer the seven decode products of a Llama-1B-shaped layer, one grouped call
 """
 from __future__ import annotations
 
@@ -24,13 +25,25 @@ CASES = {
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", required=True, choices=sorted(CASES))
+    ap.add_argument("--case", required=True, choices=sorted(CASES) + ["gemv_llama1b_layer"])
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
     import torch
 
     from gguf_block_quantized_gb300 import syn, synth
 
+    if args.case == "gemv_llama1b_layer":
+        from gguf_block_quantized_gb300 import workloads
+        mats = workloads.LLAMA1B_LAYER
+        Ws = [syn.quantize(m.wtype, torch.from_numpy(synth.weight(2, i, m.n_out, m.n_in)).cuda()) for i, m in enumerate(mats)]
+        Xs = [torch.from_numpy(synth.activations(2, i, 1, m.n_in)).cuda() for i, m in enumerate(mats)]
+        Ys = [torch.empty((1, m.n_out), device="cuda") for m in mats]
+        for _ in range(args.reps):
+            syn.mul_mat_batch([(m.wtype, Ws[i], m.n_out, m.n_in, Xs[i], Ys[i]) for i, m in enumerate(mats)], 1)
+        torch.cuda.synchronize()
+        assert syn.device_status() == syn.OK
+        print(f"{args.case}: {args.reps} grouped calls done")
+        return
     wt, n_out, n_in, n_tok = CASES[args.case]
     W = syn.quantize(wt, torch.from_numpy(synth.normal(5, (n_out, n_in), 0.02)).cuda())
     X = torch.from_numpy(synth.normal(6, (n_tok, n_in))).cuda()
