@@ -268,6 +268,9 @@ int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in, const floa
     rc = workspace_for(s, prefill_ws_bytes(n_in, n_tok), &ws);
     if (rc) return rc;
     const int xt = type == SYN_TYPE_Q8_0 ? SYN_TYPE_Q8_0 : SYN_TYPE_Q8_K;
+    if (syn::gemm_needs_zero(n_out, n_in, n_tok, st->sms) &&
+        cudaMemsetAsync(Y, 0, (size_t)n_tok * n_out * sizeof(float), s) != cudaSuccess)
+        return SYN_ERR_CUDA;
     if (launch_act_half(xt, X, n_tok * (n_in / elems(xt)), ws, st->sms, s) != cudaSuccess) return SYN_ERR_CUDA;
     g_launches++;
     if (syn::launch_gemm(type, W, n_out, n_in, ws, n_tok, Y, st->words, st->sms, s) != cudaSuccess)

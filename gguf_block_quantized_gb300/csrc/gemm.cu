@@ -7,22 +7,25 @@
 // synapse fits", section 5) and x~ = fp16(d_x * q_x) is the activation after the
 // conversion to the vec_dot_type ("Products: weights against quantized activations").
 // The product of the quantized activations is what the pages define; only the fp16
-// rounding of the two operands and the fp32 summation order differ from it.  Prefill is
-// compute-bound at 2 * params * tokens FLOPs ("llama.cpp and GGUF", CPU and Edge
-// Inference), so this path feeds the tensor cores.
+// rounding of the operands (and of the sub-block scales) and the fp32 summation order
+// differ from it.  Prefill is compute-bound at 2 * params * tokens FLOPs ("llama.cpp and
+// GGUF", CPU and Edge Inference), so this path feeds the tensor cores.
 //
 // One persistent CTA per SM, warp-specialised, one 128 x BN output tile per work unit
 // (BN <= 256 tokens), optionally split along K:
-//   warp 0      producer: 1-D bulk copies of the raw weight super-blocks (128 rows x 256 k)
-//               into a 2-deep raw ring; 2-D TMA loads of x~ tiles (BN x 64, 128-byte
-//               swizzle) into a 3-deep operand ring;
+//   warp 0      raw-weight producer: 128 rows x 256 k of weight blocks per raw stage, by
+//               one 2-D TMA load when the row pitch is a multiple of 16 bytes (else one
+//               1-D bulk copy per row);
 //   warp 1      allocates 512 TMEM columns (two fp32 accumulators of 128 x 256) and issues
 //               tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16) from one thread;
-//   warps 2-9   dequantize: raw blocks -> fp16 A tile (128 x 64) in the canonical K-major
-//               128-byte-swizzled layout the MMA descriptor reads;
-//   warps 10-13 epilogue: tcgen05.ld 32x32b from TMEM, store (or add, when split) to Y.
+//   warp 2      activation producer: 2-D TMA loads of x~ tiles (BN x 64, 128-byte swizzle)
+//               into a 3-deep operand ring (it alone waits for the conversion kernel);
+//   warps 3-10  dequantize: raw blocks -> fp16 A tile (128 x 64) in the canonical K-major
+//               128-byte-swizzled layout the MMA descriptor reads, in half2 arithmetic;
+//   warps 11-14 epilogue: tcgen05.ld 32x32b from TMEM, store (or add, when split) to Y.
 // All hand-offs are mbarriers; every wait is bounded (clock64) and gives up with a
-// recorded error instead of hanging.
+// recorded error instead of hanging.  Index arithmetic is 32-bit: 64-bit division runs on
+// the fp64 pipe.
 #include <cuda.h>
 
 #include <algorithm>
@@ -36,17 +39,26 @@ constexpr int GEMM_BM = 128;
 constexpr int GEMM_BK = 64;           // one 128-byte swizzle row of fp16
 constexpr int GEMM_SUPER = 256;       // k per raw weight stage
 constexpr int GEMM_STAGES = 3;        // operand ring depth
-constexpr int GEMM_RAW_STAGES = 2;    // raw weight ring depth
-constexpr int GEMM_THREADS = 14 * 32;
+constexpr int GEMM_WARPS = 15;
+constexpr int GEMM_THREADS = GEMM_WARPS * 32;
+constexpr int GEMM_DEQ_WARP0 = 3, GEMM_DEQ_WARPS = 8, GEMM_EPI_WARP0 = 11;
 constexpr int GEMM_A_BYTES = GEMM_BM * GEMM_BK * 2;   // 16 KB
 constexpr int GEMM_B_BYTES = 256 * GEMM_BK * 2;       // 32 KB (BN <= 256)
 
 template <int T> struct GemmFmt;
-// raw_row: bytes reserved per weight row in a raw stage (a 256-k slice plus the 16-byte
-// alignment window); sb_bytes: bytes of that slice in memory.
-template <> struct GemmFmt<SYN_Q4_K> { static constexpr int BB = 144, SB_BYTES = 144, RAW_ROW = 144 + 16; };
-template <> struct GemmFmt<SYN_Q6_K> { static constexpr int BB = 210, SB_BYTES = 210, RAW_ROW = 240; };
-template <> struct GemmFmt<SYN_Q8_0> { static constexpr int BB = 34, SB_BYTES = 272, RAW_ROW = 288; };
+// SB_BYTES: bytes of a 256-k slice of one row; BOX: bytes per row of the 2-D TMA box that
+// covers the slice from the 16-byte boundary at or below it (ESIZE: the tensor map's
+// element size, 2 where the box is wider than 256 elements of one byte); RAW_ROW: bytes
+// reserved per row in a raw stage for the per-row copy windows; RAW_STAGES: ring depth.
+template <> struct GemmFmt<SYN_Q4_K> {
+    static constexpr int BB = 144, SB_BYTES = 144, BOX = 144, ESIZE = 1, RAW_ROW = 144, RAW_STAGES = 4;
+};
+template <> struct GemmFmt<SYN_Q6_K> {
+    static constexpr int BB = 210, SB_BYTES = 210, BOX = 240, ESIZE = 1, RAW_ROW = 240, RAW_STAGES = 2;
+};
+template <> struct GemmFmt<SYN_Q8_0> {
+    static constexpr int BB = 34, SB_BYTES = 272, BOX = 272, ESIZE = 2, RAW_ROW = 288, RAW_STAGES = 2;
+};
 
 struct GemmParams {
     const uint8_t* W;
@@ -59,8 +71,10 @@ struct GemmParams {
     int n_super;     // 256-k super-steps per row (last one may be partial for Q8_0)
     int bn;          // tokens per tile (multiple of 16, <= 256)
     int n_m, n_n, n_split;
-    int64_t n_units;
+    int n_units;
     int accumulate;  // 1: add into Y (split-K), 0: store
+    int raw_tma;     // 1: weight slices by one 2-D TMA load per stage (row_bytes % 16 == 0)
+    int raw_row;     // bytes per row in a raw stage: BOX (TMA) or RAW_ROW (per-row copies)
     uint32_t idesc;
 };
 
@@ -138,20 +152,31 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// 2^23 + b as a float for a byte b (selected from a word by __byte_perm): subtracting
-// 2^23 afterwards gives b exactly, at full FP32 rate (no integer-to-float conversion).
-__device__ __forceinline__ float byte_as_float_2p23(uint32_t word, int i) {
-    return __int_as_float((int)__byte_perm(word, 0x4B000000u, 0x7440u | (uint32_t)i));
+// ---------------------------------------------------------------------------------------
+// dequantize one thread's 32 consecutive k of one weight row into 16 packed halves, in
+// half2 arithmetic: a byte b becomes the fp16 1024 + b by a byte permute with 0x64 (the
+// upper byte of 1024.0) and the offset is subtracted exactly.  The sub-block scale S = d*sc
+// and min M = dmin*m are exact in fp32 but not in fp16; rounding them would bias every
+// weight of the sub-block the same way (for Q4_K the q*S and M terms nearly cancel, so a
+// relative 2^-12 on either is a large error on w).  They are therefore split into a head
+// and a tail scaled by 2^12 (both normal fp16 numbers, together exact):
+//     w = fp16( (q*S_hi - M_hi) + 2^-12 * (q*S_lo' - M_lo') )
+// three fma per pair of weights, each rounding relative to |w|, not to |S| or |M|.
+// ---------------------------------------------------------------------------------------
+
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// v (exact in fp32) -> head fp16(v) and tail fp16((v - head) * 2^12), both broadcast
+__device__ __forceinline__ void split_h2(float v, __half2& hi, __half2& lo) {
+    const __half h = __float2half_rn(v);
+    hi = __half2half2(h);
+    lo = __float2half2_rn((v - __half2float(h)) * 4096.0f);
 }
 
-__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
-    __half2 h = __floats2half2_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// ---------------------------------------------------------------------------------------
-// dequantize one thread's 32 consecutive k of one weight row into 16 packed halves
-// ---------------------------------------------------------------------------------------
+// bytes (b0, b1) of v -> half2(1024 + b0, 1024 + b1); bytes (b2, b3) likewise
+__device__ __forceinline__ __half2 bytes01_h2(uint32_t v) { return u32_as_h2(__byte_perm(v, 0x64646464u, 0x4140)); }
+__device__ __forceinline__ __half2 bytes23_h2(uint32_t v) { return u32_as_h2(__byte_perm(v, 0x64646464u, 0x4342)); }
 
 // Q4_K: 64-k step c of the super-block, half h (sub-block j = 2c + h).
 __device__ __forceinline__ void deq32_q4_k(const uint8_t* blk, int c, int h, uint32_t out[16]) {
@@ -166,18 +191,19 @@ __device__ __forceinline__ void deq32_q4_k(const uint8_t* blk, int c, int h, uin
         sc = ((hdr.w >> sh) & 15) | (((hdr.y >> (sh + 6)) & 3) << 4);
         mn = ((hdr.w >> (sh + 4)) & 15) | (((hdr.z >> (sh + 6)) & 3) << 4);
     }
-    const float S = D * (float)sc, M = Dm * (float)mn;
+    __half2 Sh, Sl, nMh, nMl;
+    split_h2(D * (float)sc, Sh, Sl);
+    split_h2(-(Dm * (float)mn), nMh, nMl);
+    const __half2 k1024 = __float2half2_rn(1024.0f), tail = __float2half2_rn(1.0f / 4096.0f);
     const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
     const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c + 16);
     const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
     for (int w = 0; w < 8; w++) {
         const uint32_t v = (qw[w] >> (4 * h)) & 0x0F0F0F0Fu;
-        float f[4];
-#pragma unroll
-        for (int i = 0; i < 4; i++) f[i] = fmaf(byte_as_float_2p23(v, i) - 8388608.0f, S, -M);
-        out[2 * w] = pack_half2(f[0], f[1]);
-        out[2 * w + 1] = pack_half2(f[2], f[3]);
+        const __half2 qa = __hsub2(bytes01_h2(v), k1024), qb = __hsub2(bytes23_h2(v), k1024);
+        out[2 * w] = h2_as_u32(__hfma2(__hfma2(qa, Sl, nMl), tail, __hfma2(qa, Sh, nMh)));
+        out[2 * w + 1] = h2_as_u32(__hfma2(__hfma2(qb, Sl, nMl), tail, __hfma2(qb, Sh, nMh)));
     }
 }
 
@@ -187,7 +213,11 @@ __device__ __forceinline__ void deq32_q6_k(const uint8_t* blk, int c, int h, uin
     const int H = c >> 1, qd = 2 * (c & 1) + h;
     const float D = h2f_bits(*reinterpret_cast<const uint16_t*>(blk + 208));
     const int8_t* scs = reinterpret_cast<const int8_t*>(blk + 192 + 8 * H + 2 * qd);
-    const float S0 = D * (float)scs[0], S1 = D * (float)scs[1];
+    __half2 S0h, S0l, S1h, S1l;
+    split_h2(D * (float)scs[0], S0h, S0l);
+    split_h2(D * (float)scs[1], S1h, S1l);
+    const __half2 k1056 = __float2half2_rn(1056.0f);  // 1024 + 32
+    const __half2 tail = __float2half2_rn(1.0f / 4096.0f);
     const uint8_t* ql = blk + 64 * H + ((qd & 1) ? 32 : 0);
     const uint8_t* qh = blk + 128 + 32 * H;
     const int nsh = (qd >= 2) ? 4 : 0, hsh = 2 * qd;
@@ -196,26 +226,22 @@ __device__ __forceinline__ void deq32_q6_k(const uint8_t* blk, int c, int h, uin
         const uint32_t lo = (lds_u32_any(ql + 4 * w) >> nsh) & 0x0F0F0F0Fu;
         const uint32_t hi = ((lds_u32_any(qh + 4 * w) >> hsh) & 0x03030303u) << 4;
         const uint32_t v = lo | hi;
-        const float S = (w < 4) ? S0 : S1;
-        float f[4];
-#pragma unroll
-        for (int i = 0; i < 4; i++) f[i] = (byte_as_float_2p23(v, i) - 8388640.0f) * S;
-        out[2 * w] = pack_half2(f[0], f[1]);
-        out[2 * w + 1] = pack_half2(f[2], f[3]);
+        const __half2 Sh = (w < 4) ? S0h : S1h, Sl = (w < 4) ? S0l : S1l;
+        const __half2 qa = __hsub2(bytes01_h2(v), k1056), qb = __hsub2(bytes23_h2(v), k1056);
+        out[2 * w] = h2_as_u32(__hfma2(__hmul2(qa, Sl), tail, __hmul2(qa, Sh)));
+        out[2 * w + 1] = h2_as_u32(__hfma2(__hmul2(qb, Sl), tail, __hmul2(qb, Sh)));
     }
 }
 
-// Q8_0: one 34-byte block (32 k).
+// Q8_0: one 34-byte block (32 k).  The scale is stored in fp16, so one rounding of q*D.
 __device__ __forceinline__ void deq32_q8_0(const uint8_t* blk, uint32_t out[16]) {
-    const float D = h2f_bits(*reinterpret_cast<const uint16_t*>(blk));
+    const __half2 D = u32_as_h2(__byte_perm(*reinterpret_cast<const uint16_t*>(blk), 0, 0x1010));
+    const __half2 k1152 = __float2half2_rn(1152.0f);  // 1024 + 128
 #pragma unroll
     for (int w = 0; w < 8; w++) {
         const uint32_t v = lds_u32_any(blk + 2 + 4 * w) ^ 0x80808080u;  // int8 -> offset binary
-        float f[4];
-#pragma unroll
-        for (int i = 0; i < 4; i++) f[i] = (byte_as_float_2p23(v, i) - 8388736.0f) * D;
-        out[2 * w] = pack_half2(f[0], f[1]);
-        out[2 * w + 1] = pack_half2(f[2], f[3]);
+        out[2 * w] = h2_as_u32(__hmul2(__hsub2(bytes01_h2(v), k1152), D));
+        out[2 * w + 1] = h2_as_u32(__hmul2(__hsub2(bytes23_h2(v), k1152), D));
     }
 }
 
@@ -230,41 +256,55 @@ struct GemmSmem {
     static constexpr int RAW = B + GEMM_STAGES * GEMM_B_BYTES;
 };
 
+// unit u -> tile (m, n) and k range [ss0, ss1) in 256-k super-steps (32-bit arithmetic)
+__device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& m, int& n, int& ss0, int& ss1) {
+    const int rest = u / p.n_n;
+    n = u - rest * p.n_n;
+    const int ks = rest / p.n_m;
+    m = rest - ks * p.n_m;
+    ss0 = (ks * p.n_super) / p.n_split;
+    ss1 = ((ks + 1) * p.n_super) / p.n_split;
+}
+
 template <int T>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    k_gemm(const __grid_constant__ CUtensorMap xmap, const GemmParams p) {
+    k_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap, const GemmParams p) {
     using F = GemmFmt<T>;
+    constexpr int RS = F::RAW_STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem + GemmSmem::A;
     uint8_t* sB = smem + GemmSmem::B;
     uint8_t* sRaw = smem + GemmSmem::RAW;
     constexpr int RAW_STAGE = GEMM_BM * F::RAW_ROW;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + GEMM_RAW_STAGES * RAW_STAGE);
-    // barrier slots
-    uint64_t* raw_full = bars;                              // [2]
-    uint64_t* raw_empty = bars + 2;                         // [2]
-    uint64_t* b_full = bars + 4;                            // [3]
-    uint64_t* a_full = bars + 7;                            // [3]
-    uint64_t* ab_empty = bars + 10;                         // [3]
-    uint64_t* acc_full = bars + 13;                         // [2]
-    uint64_t* acc_empty = bars + 15;                        // [2]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 18);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + RS * RAW_STAGE);
+    uint64_t* raw_full = bars;                              // [RS]
+    uint64_t* raw_empty = bars + RS;                        // [RS]
+    uint64_t* b_full = bars + 2 * RS;                       // [3]
+    uint64_t* a_full = b_full + GEMM_STAGES;                // [3]
+    uint64_t* a_empty = a_full + GEMM_STAGES;               // [3] (MMA done with A stage)
+    uint64_t* b_empty = a_empty + GEMM_STAGES;              // [3] (MMA done with B stage)
+    uint64_t* acc_full = b_empty + GEMM_STAGES;             // [2]
+    uint64_t* acc_empty = acc_full + 2;                     // [2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(acc_empty + 3);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; i++) {
+        for (int i = 0; i < RS; i++) {
             mbar_init(smem_u32(&raw_full[i]), 1);
-            mbar_init(smem_u32(&raw_empty[i]), 8);
+            mbar_init(smem_u32(&raw_empty[i]), GEMM_DEQ_WARPS);
+        }
+        for (int i = 0; i < 2; i++) {
             mbar_init(smem_u32(&acc_full[i]), 1);
             mbar_init(smem_u32(&acc_empty[i]), 4);
         }
         for (int i = 0; i < GEMM_STAGES; i++) {
             mbar_init(smem_u32(&b_full[i]), 1);
-            mbar_init(smem_u32(&a_full[i]), 8);
-            mbar_init(smem_u32(&ab_empty[i]), 1);
+            mbar_init(smem_u32(&a_full[i]), GEMM_DEQ_WARPS);
+            mbar_init(smem_u32(&a_empty[i]), 1);
+            mbar_init(smem_u32(&b_empty[i]), 1);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -275,52 +315,57 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int64_t n_units = p.n_units;
-
-    auto unit_coords = [&](int64_t u, int& m, int& n, int& ss0, int& ss1) {
-        n = (int)(u % p.n_n);
-        const int64_t rest = u / p.n_n;
-        m = (int)(rest % p.n_m);
-        const int ks = (int)(rest / p.n_m);
-        ss0 = (int)((int64_t)ks * p.n_super / p.n_split);
-        ss1 = (int)((int64_t)(ks + 1) * p.n_super / p.n_split);
-    };
+    const int n_units = p.n_units;
     // number of 64-k steps in super-step ss
     auto steps_in = [&](int ss) {
-        const int64_t k0 = (int64_t)ss * GEMM_SUPER;
-        const int64_t rem = p.n_in - k0;
+        const int64_t rem = p.n_in - (int64_t)ss * GEMM_SUPER;
         const int64_t st = (rem + GEMM_BK - 1) / GEMM_BK;
         return (int)(st < 4 ? st : 4);
     };
 
     if (warp == 0) {
-        // ------------------------------ producer ------------------------------
-        uint32_t rc = 0, kc = 0;
-        bool ok = true;
-        for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        // ------------------------------ raw weight producer ------------------------------
+        uint32_t rc = 0;
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
             int m, n, ss0, ss1;
-            unit_coords(u, m, n, ss0, ss1);
-            for (int ss = ss0; ss < ss1 && ok; ss++) {
-                const int rs = rc % GEMM_RAW_STAGES;
-                if (!mbar_wait(smem_u32(&raw_empty[rs]), ((rc / GEMM_RAW_STAGES) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
+            unit_coords(p, u, m, n, ss0, ss1);
+            bool ok = true;
+            for (int ss = ss0; ss < ss1; ss++) {
+                const int rs = rc % RS;
+                if (!mbar_wait(smem_u32(&raw_empty[rs]), ((rc / RS) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
+                if (p.raw_tma) {
+                    // the whole 128-row slice in one load; rows past n_out and bytes past the
+                    // row end are filled with zeros (and counted in the transaction bytes)
+                    if (lane == 0) {
+                        const uint32_t rfull = smem_u32(&raw_full[rs]);
+                        mbar_arrive_expect_tx(rfull, (uint32_t)(GEMM_BM * F::BOX));
+                        const int x = (int)((((int64_t)ss * F::SB_BYTES) & ~int64_t(15)) / F::ESIZE);
+                        tma_load_2d(smem_u32(sRaw + rs * RAW_STAGE), &wmap, x, m * GEMM_BM, rfull);
+                    }
+                    __syncwarp();
+                    rc++;
+                    continue;
+                }
                 // raw weight slice of 128 rows: per row one window-aligned bulk copy
                 const int nblk_sb = (T == SYN_Q8_0) ? min(8, p.nb - ss * 8) : 1;
                 const int64_t len = (int64_t)nblk_sb * F::BB;
                 uint32_t my_tx = 0;
-                int64_t a0[4], nbytes[4];
+                int64_t a0[4];
+                uint32_t nbytes[4];
 #pragma unroll
                 for (int i = 0; i < 4; i++) {
                     const int r = lane + 32 * i;
                     const int64_t o = (int64_t)m * GEMM_BM + r;
-                    a0[i] = 0; nbytes[i] = 0;
+                    a0[i] = 0;
+                    nbytes[i] = 0;
                     if (o < p.n_out) {
                         const int64_t src = o * p.row_bytes + (int64_t)ss * F::SB_BYTES;
                         const int64_t lo = src & ~int64_t(15);
                         int64_t hi = (src + len + 15) & ~int64_t(15);
                         if (hi > p.total_floor16) hi = p.total_floor16;
                         a0[i] = lo;
-                        nbytes[i] = hi > lo ? hi - lo : 0;
-                        my_tx += (uint32_t)nbytes[i];
+                        nbytes[i] = hi > lo ? (uint32_t)(hi - lo) : 0u;
+                        my_tx += nbytes[i];
                     }
                 }
                 uint8_t* rbase = sRaw + rs * RAW_STAGE;
@@ -336,7 +381,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     if (end > p.total_floor16) {
                         const int64_t lo = src & ~int64_t(15);
                         for (int64_t k = (lo > p.total_floor16 ? lo : p.total_floor16); k < end; k++)
-                            rbase[r * F::RAW_ROW + (k - lo)] = p.W[k];
+                            rbase[r * p.raw_row + (k - lo)] = p.W[k];
                     }
                 }
                 uint32_t tx = my_tx;
@@ -349,13 +394,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 4; i++)
                     if (nbytes[i] > 0)
-                        bulk_g2s(smem_u32(rbase + (lane + 32 * i) * F::RAW_ROW), p.W + a0[i], (uint32_t)nbytes[i], rfull);
+                        bulk_g2s(smem_u32(rbase + (lane + 32 * i) * p.raw_row), p.W + a0[i], nbytes[i], rfull);
                 rc++;
-                // activation tiles of this super-step
+            }
+            if (!ok) break;
+        }
+    } else if (warp == 2) {
+        // ------------------------------ activation producer ------------------------------
+        // x~ is written by the conversion kernel this launch may overlap with: wait for it
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        uint32_t kc = 0;
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+            int m, n, ss0, ss1;
+            unit_coords(p, u, m, n, ss0, ss1);
+            bool ok = true;
+            for (int ss = ss0; ss < ss1 && ok; ss++) {
                 const int nst = steps_in(ss);
                 for (int k4 = 0; k4 < nst; k4++) {
                     const int ks = kc % GEMM_STAGES;
-                    if (!mbar_wait(smem_u32(&ab_empty[ks]), ((kc / GEMM_STAGES) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(smem_u32(&b_empty[ks]), ((kc / GEMM_STAGES) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
                     if (lane == 0) {
                         const uint32_t bf = smem_u32(&b_full[ks]);
                         mbar_arrive_expect_tx(bf, (uint32_t)(p.bn * GEMM_BK * 2));
@@ -366,14 +423,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     kc++;
                 }
             }
+            if (!ok) break;
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         uint32_t kc = 0, ac = 0;
         bool ok = true;
-        for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             int m, n, ss0, ss1;
-            unit_coords(u, m, n, ss0, ss1);
+            unit_coords(p, u, m, n, ss0, ss1);
             const int a = ac & 1;
             if (!mbar_wait(smem_u32(&acc_empty[a]), ((ac >> 1) & 1) ^ 1, p.err, abort_flag)) break;
             tc_fence_after();
@@ -396,7 +454,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                     first ? 0u : 1u);
                             first = 0;
                         }
-                        mma_commit(smem_u32(&ab_empty[ks]));
+                        mma_commit(smem_u32(&a_empty[ks]));
+                        mma_commit(smem_u32(&b_empty[ks]));
                     }
                     __syncwarp();
                     kc++;
@@ -407,27 +466,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             __syncwarp();
             ac++;
         }
-    } else if (warp < 10) {
+    } else if (warp < GEMM_EPI_WARP0) {
         // ------------------------------ dequantize ------------------------------
-        const int dw = warp - 2;
+        const int dw = warp - GEMM_DEQ_WARP0;
         const int r = 32 * (dw & 3) + lane;   // row of the tile
         const int h = dw >> 2;                // k half of the 64-wide step
         uint32_t rc = 0, kc = 0;
         bool ok = true;
-        for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             int m, n, ss0, ss1;
-            unit_coords(u, m, n, ss0, ss1);
+            unit_coords(p, u, m, n, ss0, ss1);
             const int64_t o = (int64_t)m * GEMM_BM + r;
             const bool row_ok = o < p.n_out;
             for (int ss = ss0; ss < ss1 && ok; ss++) {
-                const int rs = rc % GEMM_RAW_STAGES;
-                if (!mbar_wait(smem_u32(&raw_full[rs]), (rc / GEMM_RAW_STAGES) & 1, p.err, abort_flag)) { ok = false; break; }
+                const int rs = rc % RS;
+                if (!mbar_wait(smem_u32(&raw_full[rs]), (rc / RS) & 1, p.err, abort_flag)) { ok = false; break; }
                 const int64_t src = o * p.row_bytes + (int64_t)ss * F::SB_BYTES;
-                const uint8_t* row = sRaw + rs * RAW_STAGE + r * F::RAW_ROW + (int)(src & 15);
+                const uint8_t* row = sRaw + rs * RAW_STAGE + r * p.raw_row + (int)(src & 15);
                 const int nst = steps_in(ss);
                 for (int k4 = 0; k4 < nst; k4++) {
                     const int ks = kc % GEMM_STAGES;
-                    if (!mbar_wait(smem_u32(&ab_empty[ks]), ((kc / GEMM_STAGES) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
                     uint32_t out[16];
                     const int64_t kglob = (int64_t)ss * GEMM_SUPER + k4 * GEMM_BK + h * 32;
                     if (row_ok && kglob < p.n_in) {
@@ -438,6 +496,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
                         for (int i = 0; i < 16; i++) out[i] = 0u;
                     }
+                    if (!mbar_wait(smem_u32(&a_empty[ks]), ((kc / GEMM_STAGES) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
                     // 128-byte swizzle: 16-byte chunk j of row r lands at chunk j ^ (r % 8)
                     uint8_t* arow = sA + ks * GEMM_A_BYTES + r * 128;
 #pragma unroll
@@ -460,9 +519,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // ------------------------------ epilogue ------------------------------
         const int quarter = warp & 3;
         uint32_t ac = 0;
-        for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
             int m, n, ss0, ss1;
-            unit_coords(u, m, n, ss0, ss1);
+            unit_coords(p, u, m, n, ss0, ss1);
             const int a = ac & 1;
             if (!mbar_wait(smem_u32(&acc_full[a]), (ac >> 1) & 1, p.err, abort_flag)) break;
             tc_fence_after();
@@ -523,12 +582,19 @@ static PFN_encodeTiled get_encode() {
     return fn;
 }
 
-static size_t gemm_smem_bytes(int raw_row) {
-    return 1024 /* alignment slack */ + GemmSmem::RAW + (size_t)GEMM_RAW_STAGES * GEMM_BM * raw_row + 256;
+template <int T>
+static size_t gemm_smem_bytes() {
+    using F = GemmFmt<T>;
+    return 1024 /* alignment slack */ + GemmSmem::RAW + (size_t)F::RAW_STAGES * GEMM_BM * F::RAW_ROW + 256;
 }
 
+#ifndef SYN_GEMM_SPLIT_PENALTY
+#define SYN_GEMM_SPLIT_PENALTY 0.15
+#endif
+
 // Pick the K split so that units fill the SMs in whole waves: minimise
-// ceil(tiles * S / sms) / S, preferring the smaller S on ties (each split keeps >= 2
+// ceil(tiles * S / sms) / S, with a penalty for splitting (the partial tiles are added
+// into Y with atomics), preferring the smaller S on ties (each split keeps >= 2
 // super-steps).
 static int pick_split(int64_t tiles, int n_super, int sms) {
     int best = 1;
@@ -536,7 +602,7 @@ static int pick_split(int64_t tiles, int n_super, int sms) {
     for (int S = 1; S <= 16; S++) {
         if (S > 1 && n_super / S < 2) break;
         const int64_t waves = (tiles * S + sms - 1) / sms;
-        const double t = (double)waves / S + (S > 1 ? 0.02 : 0.0);
+        const double t = (double)waves / S + (S > 1 ? SYN_GEMM_SPLIT_PENALTY : 0.0);
         if (t < best_t - 1e-9) {
             best_t = t;
             best = S;
@@ -546,15 +612,36 @@ static int pick_split(int64_t tiles, int n_super, int sms) {
 }
 
 template <int T>
-static cudaError_t run_gemm(GemmParams p, const CUtensorMap& map, int sms, cudaStream_t s) {
-    using F = GemmFmt<T>;
-    const size_t smem = gemm_smem_bytes(F::RAW_ROW);
+static cudaError_t run_gemm(GemmParams p, const CUtensorMap& map, const CUtensorMap& wmap, int sms,
+                           cudaStream_t s) {
+    const size_t smem = gemm_smem_bytes<T>();
     auto kern = k_gemm<T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int64_t grid = std::min<int64_t>(p.n_units, sms);
-    kern<<<(unsigned)grid, GEMM_THREADS, smem, s>>>(map, p);
-    return cudaGetLastError();
+    const int grid = std::min(p.n_units, sms);
+    // launched as the programmatic dependent of the activation conversion: the weight
+    // producer and the dequantizers start before the conversion has finished
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, map, wmap, p);
+}
+
+static int gemm_bn(int64_t n_tok) { return (int)std::min<int64_t>(256, (n_tok + 15) / 16 * 16); }
+
+// Whether the product splits along K: its Y must then be zeroed before the activation
+// conversion is enqueued (the product kernel overlaps the conversion).
+bool gemm_needs_zero(int64_t n_out, int64_t n_in, int64_t n_tok, int sms) {
+    const int bn = gemm_bn(n_tok);
+    const int64_t tiles = ((n_out + GEMM_BM - 1) / GEMM_BM) * ((n_tok + bn - 1) / bn);
+    return pick_split(tiles, (int)((n_in + GEMM_SUPER - 1) / GEMM_SUPER), sms) > 1;
 }
 
 cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, const void* xh, int64_t n_tok,
@@ -572,11 +659,14 @@ cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, co
     p.row_bytes = (int64_t)p.nb * block_bytes(type);
     p.total_floor16 = (n_out * p.row_bytes) & ~int64_t(15);
     p.n_super = (int)((n_in + GEMM_SUPER - 1) / GEMM_SUPER);
-    p.bn = (int)std::min<int64_t>(256, (n_tok + 15) / 16 * 16);
+    p.bn = gemm_bn(n_tok);
     p.n_m = (int)((n_out + GEMM_BM - 1) / GEMM_BM);
     p.n_n = (int)((n_tok + p.bn - 1) / p.bn);
-    p.n_split = pick_split((int64_t)p.n_m * p.n_n, p.n_super, sms);
-    p.n_units = (int64_t)p.n_m * p.n_n * p.n_split;
+    const int64_t tiles = (int64_t)p.n_m * p.n_n;
+    if (tiles * 16 > (int64_t(1) << 30) || (int64_t)p.n_super * 16 > (int64_t(1) << 30))
+        return cudaErrorInvalidValue;  // 32-bit unit and super-step arithmetic
+    p.n_split = pick_split(tiles, p.n_super, sms);
+    p.n_units = (int)(tiles * p.n_split);
     p.accumulate = p.n_split > 1 ? 1 : 0;
     // kind::f16 instruction descriptor: D fp32, A and B fp16, both K-major, N, M = 128
     p.idesc = (1u << 4) | ((uint32_t)(p.bn >> 3) << 17) | ((uint32_t)(GEMM_BM >> 4) << 24);
@@ -590,14 +680,34 @@ cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, co
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    if (p.accumulate) {
-        cudaError_t e = cudaMemsetAsync(Y, 0, (size_t)n_tok * n_out * sizeof(float), s);
-        if (e != cudaSuccess) return e;
+
+    // weights: one 2-D TMA box (128 rows x BOX bytes) per raw stage when the row pitch
+    // allows it (W itself is 16-byte aligned); otherwise per-row copy windows
+    int box_bytes, esize, raw_row;
+    switch (type) {
+    case SYN_Q4_K: box_bytes = GemmFmt<SYN_Q4_K>::BOX; esize = GemmFmt<SYN_Q4_K>::ESIZE; raw_row = GemmFmt<SYN_Q4_K>::RAW_ROW; break;
+    case SYN_Q6_K: box_bytes = GemmFmt<SYN_Q6_K>::BOX; esize = GemmFmt<SYN_Q6_K>::ESIZE; raw_row = GemmFmt<SYN_Q6_K>::RAW_ROW; break;
+    case SYN_Q8_0: box_bytes = GemmFmt<SYN_Q8_0>::BOX; esize = GemmFmt<SYN_Q8_0>::ESIZE; raw_row = GemmFmt<SYN_Q8_0>::RAW_ROW; break;
+    default: return cudaErrorInvalidValue;
+    }
+    CUtensorMap wmap = map;  // placeholder when unused
+    p.raw_tma = 0;
+    p.raw_row = raw_row;
+    if (p.row_bytes % 16 == 0 && p.row_bytes < (int64_t(1) << 31)) {
+        cuuint64_t wdims[2] = {(cuuint64_t)(p.row_bytes / esize), (cuuint64_t)n_out};
+        cuuint64_t wstrides[1] = {(cuuint64_t)p.row_bytes};
+        cuuint32_t wbox[2] = {(cuuint32_t)(box_bytes / esize), (cuuint32_t)GEMM_BM};
+        cr = encode(&wmap, esize == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+                    const_cast<void*>(W), wdims, wstrides, wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        p.raw_tma = 1;
+        p.raw_row = box_bytes;
     }
     switch (type) {
-    case SYN_Q4_K: return run_gemm<SYN_Q4_K>(p, map, sms, s);
-    case SYN_Q6_K: return run_gemm<SYN_Q6_K>(p, map, sms, s);
-    case SYN_Q8_0: return run_gemm<SYN_Q8_0>(p, map, sms, s);
+    case SYN_Q4_K: return run_gemm<SYN_Q4_K>(p, map, wmap, sms, s);
+    case SYN_Q6_K: return run_gemm<SYN_Q6_K>(p, map, wmap, sms, s);
+    case SYN_Q8_0: return run_gemm<SYN_Q8_0>(p, map, wmap, sms, s);
     default: return cudaErrorInvalidValue;
     }
 }

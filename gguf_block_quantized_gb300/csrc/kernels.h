@@ -39,10 +39,13 @@ int64_t gemv_workspace_bytes(int n, const GemvDesc* d, int64_t n_tok);
 int64_t gemv_act_bytes(int type, int64_t n_in);
 int64_t gemv_act_limit();
 
-// Prefill product on the tensor cores.  xh: n_tok x n_in fp16 activations (already
-// quantized and expanded).  Y is overwritten.
+// Prefill product on the tensor cores.  xh: n_tok x n_in fp16 activations, written by
+// launch_act_half immediately before on the same stream (the product kernel is its
+// programmatic dependent).  Y is overwritten, or, when gemm_needs_zero() is true, added
+// into: the caller then zeroes Y before launch_act_half.
 cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, const void* xh,
                         int64_t n_tok, float* Y, int* err, int sms, cudaStream_t s);
+bool gemm_needs_zero(int64_t n_out, int64_t n_in, int64_t n_tok, int sms);
 
 // Adds n to the count syn_launch_count reports.
 void note_launches(int n);

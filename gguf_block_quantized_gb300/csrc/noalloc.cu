@@ -82,6 +82,9 @@ extern "C" int syn_mul_mat_prefill_static(int type, const void* W, int64_t n_out
     int* err = reinterpret_cast<int*>(d->scratch);
     void* xh = d->scratch + kHeader;
     const int xt = type == SYN_TYPE_Q8_0 ? SYN_TYPE_Q8_0 : SYN_TYPE_Q8_K;
+    if (syn::gemm_needs_zero(n_out, n_in, n_tok, d->sms) &&
+        cudaMemsetAsync(Y, 0, (size_t)n_tok * n_out * sizeof(float), s) != cudaSuccess)
+        return SYN_ERR_CUDA;
     if (syn::launch_act_half(xt, X, n_tok * (n_in / be), xh, d->sms, s) != cudaSuccess) return SYN_ERR_CUDA;
     syn::note_launches(1);
     if (syn::launch_gemm(type, W, n_out, n_in, xh, n_tok, Y, err, d->sms, s) != cudaSuccess) return SYN_ERR_CUDA;

@@ -271,6 +271,8 @@ __global__ void __launch_bounds__(256) k_quantize_act(const float* __restrict__ 
 template <int XT>
 __global__ void __launch_bounds__(256) k_act_half(const float* __restrict__ X, int64_t n_rows_blocks,
                                                   __half* __restrict__ xh) {
+    // the product kernel that follows is launched as this kernel's programmatic dependent
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
