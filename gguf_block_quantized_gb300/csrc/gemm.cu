@@ -38,26 +38,51 @@ namespace syn {
 constexpr int GEMM_BM = 128;
 constexpr int GEMM_BK = 64;           // one 128-byte swizzle row of fp16
 constexpr int GEMM_SUPER = 256;       // k per raw weight stage
-constexpr int GEMM_STAGES = 3;        // operand ring depth
-constexpr int GEMM_WARPS = 15;
+#ifndef SYN_GEMM_DEQ_FOLD
+#define SYN_GEMM_DEQ_FOLD 0
+#endif
+// dequantizer teams: team t handles the 64-k steps with step index = t (mod teams); each
+// team is 8 warps (128 rows x two 32-k halves)
+#ifndef SYN_GEMM_DEQ_TEAMS
+#define SYN_GEMM_DEQ_TEAMS 2
+#endif
+constexpr int GEMM_DEQ_TEAMS = SYN_GEMM_DEQ_TEAMS;
+constexpr int GEMM_DEQ_WARP0 = 3, GEMM_DEQ_WARPS = 8 * GEMM_DEQ_TEAMS, GEMM_EPI_WARP0 = 3 + GEMM_DEQ_WARPS;
+constexpr int GEMM_WARPS = GEMM_EPI_WARP0 + 4;
 constexpr int GEMM_THREADS = GEMM_WARPS * 32;
-constexpr int GEMM_DEQ_WARP0 = 3, GEMM_DEQ_WARPS = 8, GEMM_EPI_WARP0 = 11;
 constexpr int GEMM_A_BYTES = GEMM_BM * GEMM_BK * 2;   // 16 KB
 constexpr int GEMM_B_BYTES = 256 * GEMM_BK * 2;       // 32 KB (BN <= 256)
+constexpr int GEMM_OUT_TOK = 16;                      // tokens per output staging chunk
+constexpr int GEMM_OUT_BYTES = GEMM_BM * GEMM_OUT_TOK * 4;  // four warps x 32 outputs x 16 tokens, fp32
 
 template <int T> struct GemmFmt;
 // SB_BYTES: bytes of a 256-k slice of one row; BOX: bytes per row of the 2-D TMA box that
 // covers the slice from the 16-byte boundary at or below it (ESIZE: the tensor map's
 // element size, 2 where the box is wider than 256 elements of one byte); RAW_ROW: bytes
 // reserved per row in a raw stage for the per-row copy windows; RAW_STAGES: ring depth.
-template <> struct GemmFmt<SYN_Q4_K> {
-    static constexpr int BB = 144, SB_BYTES = 144, BOX = 144, ESIZE = 1, RAW_ROW = 144, RAW_STAGES = 4;
+// A_STAGES / B_STAGES: depths of the dequantized-weight and activation rings.  The
+// activation tiles come from L2 with the longest latency, so their ring gets what the
+// shared memory allows.
+#ifndef SYN_GEMM_Q4K_RAW
+#define SYN_GEMM_Q4K_RAW 2
+#endif
+#ifndef SYN_GEMM_Q4K_A
+#define SYN_GEMM_Q4K_A 3
+#endif
+#ifndef SYN_GEMM_Q4K_B
+#define SYN_GEMM_Q4K_B 4
+#endif
+template <int R, int A, int B> struct GemmDepth {
+    static constexpr int RAW_STAGES = R, A_STAGES = A, B_STAGES = B;
 };
-template <> struct GemmFmt<SYN_Q6_K> {
-    static constexpr int BB = 210, SB_BYTES = 210, BOX = 240, ESIZE = 1, RAW_ROW = 240, RAW_STAGES = 2;
+template <> struct GemmFmt<SYN_Q4_K> : GemmDepth<SYN_GEMM_Q4K_RAW, SYN_GEMM_Q4K_A, SYN_GEMM_Q4K_B> {
+    static constexpr int BB = 144, SB_BYTES = 144, BOX = 144, ESIZE = 1, RAW_ROW = 144;
 };
-template <> struct GemmFmt<SYN_Q8_0> {
-    static constexpr int BB = 34, SB_BYTES = 272, BOX = 272, ESIZE = 2, RAW_ROW = 288, RAW_STAGES = 2;
+template <> struct GemmFmt<SYN_Q6_K> : GemmDepth<2, 3, 3> {
+    static constexpr int BB = 210, SB_BYTES = 210, BOX = 240, ESIZE = 1, RAW_ROW = 240;
+};
+template <> struct GemmFmt<SYN_Q8_0> : GemmDepth<2, 3, 3> {
+    static constexpr int BB = 34, SB_BYTES = 272, BOX = 272, ESIZE = 2, RAW_ROW = 288;
 };
 
 struct GemmParams {
@@ -75,6 +100,7 @@ struct GemmParams {
     int accumulate;  // 1: add into Y (split-K), 0: store
     int raw_tma;     // 1: weight slices by one 2-D TMA load per stage (row_bytes % 16 == 0)
     int raw_row;     // bytes per row in a raw stage: BOX (TMA) or RAW_ROW (per-row copies)
+    int y_tma;       // 1: Y written by 2-D TMA stores / reduce-adds (n_out % 4 == 0)
     uint32_t idesc;
 };
 
@@ -136,6 +162,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// shared -> global 2-D tile store and reduce-add (fp32 add, performed at L2), bulk-group
+// completion
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int c0, int c1, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map),
+                 "r"(c0), "r"(c1), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, int c0, int c1, uint32_t src) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map),
+                 "r"(c0), "r"(c1), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 #define TMEM_LD32(taddr, r)                                                                            \
     asm volatile(                                                                                      \
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"  \
@@ -191,13 +234,28 @@ __device__ __forceinline__ void deq32_q4_k(const uint8_t* blk, int c, int h, uin
         sc = ((hdr.w >> sh) & 15) | (((hdr.y >> (sh + 6)) & 3) << 4);
         mn = ((hdr.w >> (sh + 4)) & 15) | (((hdr.z >> (sh + 6)) & 3) << 4);
     }
-    __half2 Sh, Sl, nMh, nMl;
-    split_h2(D * (float)sc, Sh, Sl);
-    split_h2(-(Dm * (float)mn), nMh, nMl);
-    const __half2 k1024 = __float2half2_rn(1024.0f), tail = __float2half2_rn(1.0f / 4096.0f);
+    const __half2 tail = __float2half2_rn(1.0f / 4096.0f);
     const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
     const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c + 16);
     const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const float S = D * (float)sc, M = Dm * (float)mn;
+#if SYN_GEMM_DEQ_FOLD
+    // fold the 1024 of the byte permute into the offset: w = S*(1024 + q) - (1024*S + M)
+    __half2 Sh, Sl, nCh, nCl;
+    split_h2(S, Sh, Sl);
+    split_h2(-fmaf(1024.0f, S, M), nCh, nCl);
+#pragma unroll
+    for (int w = 0; w < 8; w++) {
+        const uint32_t v = (qw[w] >> (4 * h)) & 0x0F0F0F0Fu;
+        const __half2 qa = bytes01_h2(v), qb = bytes23_h2(v);
+        out[2 * w] = h2_as_u32(__hfma2(__hfma2(qa, Sl, nCl), tail, __hfma2(qa, Sh, nCh)));
+        out[2 * w + 1] = h2_as_u32(__hfma2(__hfma2(qb, Sl, nCl), tail, __hfma2(qb, Sh, nCh)));
+    }
+#else
+    __half2 Sh, Sl, nMh, nMl;
+    split_h2(S, Sh, Sl);
+    split_h2(-M, nMh, nMl);
+    const __half2 k1024 = __float2half2_rn(1024.0f);
 #pragma unroll
     for (int w = 0; w < 8; w++) {
         const uint32_t v = (qw[w] >> (4 * h)) & 0x0F0F0F0Fu;
@@ -205,6 +263,7 @@ __device__ __forceinline__ void deq32_q4_k(const uint8_t* blk, int c, int h, uin
         out[2 * w] = h2_as_u32(__hfma2(__hfma2(qa, Sl, nMl), tail, __hfma2(qa, Sh, nMh)));
         out[2 * w + 1] = h2_as_u32(__hfma2(__hfma2(qb, Sl, nMl), tail, __hfma2(qb, Sh, nMh)));
     }
+#endif
 }
 
 // Q6_K: 64-k step c of the super-block (half H = c/2), thread half h: quarter
@@ -249,11 +308,14 @@ __device__ __forceinline__ void deq32_q8_0(const uint8_t* blk, uint32_t out[16])
 // the kernel
 // ---------------------------------------------------------------------------------------
 
+template <int T>
 struct GemmSmem {
     // offsets from the 1024-aligned dynamic shared-memory base
     static constexpr int A = 0;
-    static constexpr int B = A + GEMM_STAGES * GEMM_A_BYTES;
-    static constexpr int RAW = B + GEMM_STAGES * GEMM_B_BYTES;
+    static constexpr int B = A + GemmFmt<T>::A_STAGES * GEMM_A_BYTES;
+    static constexpr int RAW = B + GemmFmt<T>::B_STAGES * GEMM_B_BYTES;
+    static constexpr int OUT = RAW + GemmFmt<T>::RAW_STAGES * GEMM_BM * GemmFmt<T>::RAW_ROW;
+    static constexpr int BARS = OUT + GEMM_OUT_BYTES;
 };
 
 // unit u -> tile (m, n) and k range [ss0, ss1) in 256-k super-steps (32-bit arithmetic)
@@ -268,23 +330,27 @@ __device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& m, 
 
 template <int T>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    k_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap, const GemmParams p) {
+    k_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+           const __grid_constant__ CUtensorMap ymap, const GemmParams p) {
     using F = GemmFmt<T>;
+    using L = GemmSmem<T>;
     constexpr int RS = F::RAW_STAGES;
+    constexpr int GEMM_A_STAGES = F::A_STAGES;
+    constexpr int GEMM_B_STAGES = F::B_STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sA = smem + GemmSmem::A;
-    uint8_t* sB = smem + GemmSmem::B;
-    uint8_t* sRaw = smem + GemmSmem::RAW;
+    uint8_t* sA = smem + L::A;
+    uint8_t* sB = smem + L::B;
+    uint8_t* sRaw = smem + L::RAW;
     constexpr int RAW_STAGE = GEMM_BM * F::RAW_ROW;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + RS * RAW_STAGE);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BARS);
     uint64_t* raw_full = bars;                              // [RS]
     uint64_t* raw_empty = bars + RS;                        // [RS]
-    uint64_t* b_full = bars + 2 * RS;                       // [3]
-    uint64_t* a_full = b_full + GEMM_STAGES;                // [3]
-    uint64_t* a_empty = a_full + GEMM_STAGES;               // [3] (MMA done with A stage)
-    uint64_t* b_empty = a_empty + GEMM_STAGES;              // [3] (MMA done with B stage)
-    uint64_t* acc_full = b_empty + GEMM_STAGES;             // [2]
+    uint64_t* b_full = bars + 2 * RS;                       // [B stages]
+    uint64_t* b_empty = b_full + GEMM_B_STAGES;             // [B stages] (MMA done with B stage)
+    uint64_t* a_full = b_empty + GEMM_B_STAGES;             // [A stages]
+    uint64_t* a_empty = a_full + GEMM_A_STAGES;             // [A stages] (MMA done with A stage)
+    uint64_t* acc_full = a_empty + GEMM_A_STAGES;           // [2]
     uint64_t* acc_empty = acc_full + 2;                     // [2]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(acc_empty + 3);
@@ -300,11 +366,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             mbar_init(smem_u32(&acc_full[i]), 1);
             mbar_init(smem_u32(&acc_empty[i]), 4);
         }
-        for (int i = 0; i < GEMM_STAGES; i++) {
+        for (int i = 0; i < GEMM_B_STAGES; i++) {
             mbar_init(smem_u32(&b_full[i]), 1);
-            mbar_init(smem_u32(&a_full[i]), GEMM_DEQ_WARPS);
-            mbar_init(smem_u32(&a_empty[i]), 1);
             mbar_init(smem_u32(&b_empty[i]), 1);
+        }
+        for (int i = 0; i < GEMM_A_STAGES; i++) {
+            mbar_init(smem_u32(&a_full[i]), 8);
+            mbar_init(smem_u32(&a_empty[i]), 1);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -411,8 +479,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int ss = ss0; ss < ss1 && ok; ss++) {
                 const int nst = steps_in(ss);
                 for (int k4 = 0; k4 < nst; k4++) {
-                    const int ks = kc % GEMM_STAGES;
-                    if (!mbar_wait(smem_u32(&b_empty[ks]), ((kc / GEMM_STAGES) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
+                    const int ks = kc % GEMM_B_STAGES;
+                    if (!mbar_wait(smem_u32(&b_empty[ks]), ((kc / GEMM_B_STAGES) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
                     if (lane == 0) {
                         const uint32_t bf = smem_u32(&b_full[ks]);
                         mbar_arrive_expect_tx(bf, (uint32_t)(p.bn * GEMM_BK * 2));
@@ -440,22 +508,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int ss = ss0; ss < ss1 && ok; ss++) {
                 const int nst = steps_in(ss);
                 for (int k4 = 0; k4 < nst; k4++) {
-                    const int ks = kc % GEMM_STAGES;
-                    const uint32_t par = (kc / GEMM_STAGES) & 1;
-                    if (!mbar_wait(smem_u32(&a_full[ks]), par, p.err, abort_flag) ||
-                        !mbar_wait(smem_u32(&b_full[ks]), par, p.err, abort_flag)) { ok = false; break; }
+                    const int ka = kc % GEMM_A_STAGES, kb = kc % GEMM_B_STAGES;
+                    if (!mbar_wait(smem_u32(&a_full[ka]), (kc / GEMM_A_STAGES) & 1, p.err, abort_flag) ||
+                        !mbar_wait(smem_u32(&b_full[kb]), (kc / GEMM_B_STAGES) & 1, p.err, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t a_addr = smem_u32(sA + ks * GEMM_A_BYTES);
-                        const uint32_t b_addr = smem_u32(sB + ks * GEMM_B_BYTES);
+                        const uint32_t a_addr = smem_u32(sA + ka * GEMM_A_BYTES);
+                        const uint32_t b_addr = smem_u32(sB + kb * GEMM_B_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < GEMM_BK / 16; kk++) {
                             mma_f16(d_tmem, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32), p.idesc,
                                     first ? 0u : 1u);
                             first = 0;
                         }
-                        mma_commit(smem_u32(&a_empty[ks]));
-                        mma_commit(smem_u32(&b_empty[ks]));
+                        mma_commit(smem_u32(&a_empty[ka]));
+                        mma_commit(smem_u32(&b_empty[kb]));
                     }
                     __syncwarp();
                     kc++;
@@ -470,7 +537,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // ------------------------------ dequantize ------------------------------
         const int dw = warp - GEMM_DEQ_WARP0;
         const int r = 32 * (dw & 3) + lane;   // row of the tile
-        const int h = dw >> 2;                // k half of the 64-wide step
+        const int h = (dw >> 2) & 1;          // k half of the 64-wide step
+        const uint32_t team = (uint32_t)(dw >> 3);
         uint32_t rc = 0, kc = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -484,8 +552,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const int64_t src = o * p.row_bytes + (int64_t)ss * F::SB_BYTES;
                 const uint8_t* row = sRaw + rs * RAW_STAGE + r * p.raw_row + (int)(src & 15);
                 const int nst = steps_in(ss);
-                for (int k4 = 0; k4 < nst; k4++) {
-                    const int ks = kc % GEMM_STAGES;
+                for (int k4 = 0; k4 < nst; k4++, kc++) {
+                    if (kc % GEMM_DEQ_TEAMS != team) continue;
+                    const int ks = kc % GEMM_A_STAGES;
                     uint32_t out[16];
                     const int64_t kglob = (int64_t)ss * GEMM_SUPER + k4 * GEMM_BK + h * 32;
                     if (row_ok && kglob < p.n_in) {
@@ -496,7 +565,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
                         for (int i = 0; i < 16; i++) out[i] = 0u;
                     }
-                    if (!mbar_wait(smem_u32(&a_empty[ks]), ((kc / GEMM_STAGES) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(smem_u32(&a_empty[ks]), ((kc / GEMM_A_STAGES) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
                     // 128-byte swizzle: 16-byte chunk j of row r lands at chunk j ^ (r % 8)
                     uint8_t* arow = sA + ks * GEMM_A_BYTES + r * 128;
 #pragma unroll
@@ -508,7 +577,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&a_full[ks]));
-                    kc++;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&raw_empty[rs]));
@@ -517,7 +585,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
     } else {
         // ------------------------------ epilogue ------------------------------
+        // TMEM -> registers (32 columns per load); then either through a per-warp staging
+        // buffer of 32 outputs x 16 tokens and one 2-D TMA store (or reduce-add, for split
+        // products) per buffer, clipped by the tensor map at n_out / n_tok, the four warps
+        // independent of each other, or (rows whose pitch is not a multiple of 16 bytes)
+        // per-element stores / atomic adds.
         const int quarter = warp & 3;
+        float* stage = reinterpret_cast<float*>(smem + L::OUT + quarter * (GEMM_OUT_BYTES / 4));
+        const uint32_t stage_s = smem_u32(stage);
         uint32_t ac = 0;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
             int m, n, ss0, ss1;
@@ -525,17 +600,41 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const int a = ac & 1;
             if (!mbar_wait(smem_u32(&acc_full[a]), (ac >> 1) & 1, p.err, abort_flag)) break;
             tc_fence_after();
-            const int64_t o = (int64_t)m * GEMM_BM + 32 * quarter + lane;
-            const int64_t t0 = (int64_t)n * p.bn;
+            const int o0 = m * GEMM_BM + 32 * quarter;
+            const int64_t o = (int64_t)o0 + lane;
+            const int t0 = n * p.bn;
             for (int cb = 0; cb < p.bn; cb += 32) {
                 uint32_t v[32];
                 const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(a * 256 + cb);
                 TMEM_LD32(taddr, v);
                 tmem_ld_wait();
-                if (o < p.n_out) {
+                if (cb + 32 >= p.bn) {
+                    // the accumulator is in registers: hand it back to the MMA warp
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&acc_empty[a]));
+                }
+                if (p.y_tma) {
+#pragma unroll
+                    for (int hh = 0; hh < 2; hh++) {
+                        const int tt = t0 + cb + GEMM_OUT_TOK * hh;
+                        if (cb + GEMM_OUT_TOK * hh >= p.bn || tt >= p.n_tok || o0 >= p.n_out) continue;
+                        if (lane == 0) bulk_wait_read<0>();  // the previous buffer has left the stage
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < GEMM_OUT_TOK; i++) stage[i * 32 + lane] = __uint_as_float(v[GEMM_OUT_TOK * hh + i]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (p.accumulate) tma_reduce_add_2d(&ymap, o0, tt, stage_s);
+                            else tma_store_2d(&ymap, o0, tt, stage_s);
+                            bulk_commit();
+                        }
+                    }
+                } else if (o < p.n_out) {
 #pragma unroll
                     for (int i = 0; i < 32; i++) {
-                        const int64_t t = t0 + cb + i;
+                        const int64_t t = (int64_t)t0 + cb + i;
                         if (cb + i < p.bn && t < p.n_tok) {
                             float* dst = p.Y + t * p.n_out + o;
                             if (p.accumulate) atomicAdd(dst, __uint_as_float(v[i]));
@@ -544,11 +643,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[a]));
             ac++;
         }
+        if (lane == 0) bulk_wait_all();  // Y written before the CTA (and its staging) goes away
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -583,10 +681,17 @@ static PFN_encodeTiled get_encode() {
 }
 
 template <int T>
-static size_t gemm_smem_bytes() {
-    using F = GemmFmt<T>;
-    return 1024 /* alignment slack */ + GemmSmem::RAW + (size_t)F::RAW_STAGES * GEMM_BM * F::RAW_ROW + 256;
+constexpr size_t gemm_smem_bytes() {
+    return 1024 /* alignment slack */ + GemmSmem<T>::BARS + 256 /* barriers, TMEM slot, abort flag */;
 }
+static_assert(gemm_smem_bytes<SYN_Q4_K>() <= 232448 && gemm_smem_bytes<SYN_Q6_K>() <= 232448 &&
+                  gemm_smem_bytes<SYN_Q8_0>() <= 232448,
+              "shared memory per CTA exceeds 227 KB");
+template <int T>
+constexpr bool gemm_bars_fit() {
+    return 8 * (2 * GemmFmt<T>::RAW_STAGES + 2 * GemmFmt<T>::A_STAGES + 2 * GemmFmt<T>::B_STAGES + 4) + 16 <= 256;
+}
+static_assert(gemm_bars_fit<SYN_Q4_K>() && gemm_bars_fit<SYN_Q6_K>() && gemm_bars_fit<SYN_Q8_0>(), "barrier area");
 
 #ifndef SYN_GEMM_SPLIT_PENALTY
 #define SYN_GEMM_SPLIT_PENALTY 0.15
@@ -612,8 +717,8 @@ static int pick_split(int64_t tiles, int n_super, int sms) {
 }
 
 template <int T>
-static cudaError_t run_gemm(GemmParams p, const CUtensorMap& map, const CUtensorMap& wmap, int sms,
-                           cudaStream_t s) {
+static cudaError_t run_gemm(GemmParams p, const CUtensorMap& map, const CUtensorMap& wmap, const CUtensorMap& ymap,
+                           int sms, cudaStream_t s) {
     const size_t smem = gemm_smem_bytes<T>();
     auto kern = k_gemm<T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -631,7 +736,7 @@ static cudaError_t run_gemm(GemmParams p, const CUtensorMap& map, const CUtensor
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, map, wmap, p);
+    return cudaLaunchKernelEx(&cfg, kern, map, wmap, ymap, p);
 }
 
 static int gemm_bn(int64_t n_tok) { return (int)std::min<int64_t>(256, (n_tok + 15) / 16 * 16); }
@@ -704,10 +809,24 @@ cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, co
         p.raw_tma = 1;
         p.raw_row = box_bytes;
     }
+    // outputs: 2-D TMA box of 32 outputs x 16 tokens when the Y row pitch is a multiple of
+    // 16 bytes (Y itself is 16-byte aligned)
+    CUtensorMap ymap = map;  // placeholder when unused
+    p.y_tma = 0;
+    if (n_out % 4 == 0) {
+        cuuint64_t ydims[2] = {(cuuint64_t)n_out, (cuuint64_t)n_tok};
+        cuuint64_t ystrides[1] = {(cuuint64_t)n_out * 4};
+        cuuint32_t ybox[2] = {32, (cuuint32_t)GEMM_OUT_TOK};
+        cr = encode(&ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, Y, ydims, ystrides, ybox, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        p.y_tma = 1;
+    }
     switch (type) {
-    case SYN_Q4_K: return run_gemm<SYN_Q4_K>(p, map, wmap, sms, s);
-    case SYN_Q6_K: return run_gemm<SYN_Q6_K>(p, map, wmap, sms, s);
-    case SYN_Q8_0: return run_gemm<SYN_Q8_0>(p, map, wmap, sms, s);
+    case SYN_Q4_K: return run_gemm<SYN_Q4_K>(p, map, wmap, ymap, sms, s);
+    case SYN_Q6_K: return run_gemm<SYN_Q6_K>(p, map, wmap, ymap, sms, s);
+    case SYN_Q8_0: return run_gemm<SYN_Q8_0>(p, map, wmap, ymap, sms, s);
     default: return cudaErrorInvalidValue;
     }
 }
