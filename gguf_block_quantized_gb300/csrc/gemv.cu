@@ -109,8 +109,11 @@ __device__ __forceinline__ float group_sum(float v, int lg) {
     return v;
 }
 
-// Swizzled activation chunks: byte offset of chunk c (16 bytes) of block B.
-__device__ __forceinline__ int k_chunk(int B, int c) { return 256 * B + 16 * (c ^ (B & 7)); }
+// Swizzled activation chunks: byte offset of chunk c (16 bytes) of block B.  The two lanes
+// of a K-quant block read chunks c and c + 8 of it, and the four blocks of a quarter-warp
+// are consecutive: chunk c of block B goes to 16-byte bank group (c ^ B ^ 4*(c >= 8)) % 8,
+// so the eight 16-byte reads of a quarter-warp fall in eight different bank groups.
+__device__ __forceinline__ int k_chunk(int B, int c) { return 256 * B + 16 * (c ^ (B & 7) ^ ((c >> 3) << 2)); }
 __device__ __forceinline__ int q8_chunk(int B, int c) { return 32 * B + 16 * (c ^ ((B >> 2) & 1)); }
 
 // Convert every activation row of every matrix of the launch into the global workspace,
@@ -179,15 +182,9 @@ template <int NT>
 __device__ __forceinline__ void lane_q4_k(const uint8_t* blk, int h, int B, const ActView& A, float acc[NT]) {
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
     const float D = h2f_bits(hdr.x & 0xFFFF), Dm = h2f_bits(hdr.x >> 16);
-    int sc[4], mn[4];
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-        const int lo_sc = (hdr.y >> (8 * j)) & 63, lo_mn = (hdr.z >> (8 * j)) & 63;
-        const int hi_sc = ((hdr.w >> (8 * j)) & 15) | (((hdr.y >> (8 * j + 6)) & 3) << 4);
-        const int hi_mn = ((hdr.w >> (8 * j + 4)) & 15) | (((hdr.z >> (8 * j + 6)) & 3) << 4);
-        sc[j] = h ? hi_sc : lo_sc;  // sub-block 4h + j
-        mn[j] = h ? hi_mn : lo_mn;
-    }
+    // the 6-bit scales and mins of sub-blocks 4h .. 4h+3, one per byte (all four at once)
+    const uint32_t scw = h ? ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u)) : (hdr.y & 0x3F3F3F3Fu);
+    const uint32_t mnw = h ? (((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u)) : (hdr.z & 0x3F3F3F3Fu);
     int At[NT];
 #pragma unroll
     for (int t = 0; t < NT; t++) At[t] = 0;
@@ -197,6 +194,7 @@ __device__ __forceinline__ void lane_q4_k(const uint8_t* blk, int h, int B, cons
         const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
         const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * c);
         const uint32_t q[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        const int sl = (int)__byte_perm(scw, 0, 0x4440 | (2 * cc)), sh = (int)__byte_perm(scw, 0, 0x4441 | (2 * cc));
 #pragma unroll
         for (int t = 0; t < NT; t++) {
             const int8_t* xq = A.q + t * A.n_in;
@@ -212,17 +210,19 @@ __device__ __forceinline__ void lane_q4_k(const uint8_t* blk, int h, int B, cons
                 dl = dp4a(q[i] & 0x0F0F0F0Fu, xl[i], dl);
                 dh = dp4a((q[i] >> 4) & 0x0F0F0F0Fu, xh[i], dh);
             }
-            At[t] += sc[2 * cc] * dl + sc[2 * cc + 1] * dh;
+            At[t] += sl * dl + sh * dh;
         }
     }
+    // min term: sum_j m_j * (16-sum 2j + 16-sum 2j+1) of sub-blocks 4h+j, as four 16x8-bit
+    // dot products (dp2a) against the mins duplicated per byte pair
+    const int m01 = (int)__byte_perm(mnw, 0, 0x1100), m23 = (int)__byte_perm(mnw, 0, 0x3322);
 #pragma unroll
     for (int t = 0; t < NT; t++) {
-        // 16-sums of sub-blocks 4h .. 4h+3 (two per sub-block of 32)
         const uint4 sv = *reinterpret_cast<const uint4*>(A.s + (t * A.nbx + B) * 16 + 8 * h);
-        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
-        int Bm = 0;
-#pragma unroll
-        for (int j = 0; j < 4; j++) Bm += mn[j] * ((int)(int16_t)(sw[j] & 0xFFFF) + (int)(int16_t)(sw[j] >> 16));
+        int Bm = __dp2a_lo((int)sv.x, m01, 0);
+        Bm = __dp2a_hi((int)sv.y, m01, Bm);
+        Bm = __dp2a_lo((int)sv.z, m23, Bm);
+        Bm = __dp2a_hi((int)sv.w, m23, Bm);
         acc[t] = fmaf(A.d[t * A.ds + B], D * (float)At[t] - Dm * (float)Bm, acc[t]);
     }
 }
@@ -232,16 +232,18 @@ template <int NT>
 __device__ __forceinline__ void lane_q6_k(const uint8_t* blk, int H, int B, const ActView& A, float acc[NT]) {
     const float D = h2f_bits(*reinterpret_cast<const uint16_t*>(blk + 208));
     uint32_t scw[2], ql[16], qh[8];
-    lds_words_any<2>(blk + 192 + 8 * H, scw);  // scales of sub-blocks 8H .. 8H+7
+    lds_words_any<2>(blk + 192 + 8 * H, scw);  // int8 scales of sub-blocks 8H .. 8H+7
     lds_words_any<16>(blk + 64 * H, ql);
     lds_words_any<8>(blk + 128 + 32 * H, qh);
+    // sub-block j's scale, sign-extended
+    int scj[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) scj[j] = (int)(int8_t)(scw[j >> 2] >> (8 * (j & 3)));
 #pragma unroll
     for (int t = 0; t < NT; t++) {
         const int8_t* xq = A.q + t * A.n_in;
         // quarter k of the half, l = 4w..4w+3 (w = 4*half + i): sub-block 8H + 2k + half
         int C = 0;
-        const uint4 sv = *reinterpret_cast<const uint4*>(A.s + (t * A.nbx + B) * 16 + 8 * H);
-        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
         for (int k = 0; k < 4; k++) {
 #pragma unroll
@@ -258,12 +260,16 @@ __device__ __forceinline__ void lane_q6_k(const uint8_t* blk, int H, int B, cons
                     const uint32_t hi = (k >= 2 ? (qh[w] >> (2 * k - 4)) : (qh[w] << (4 - 2 * k))) & 0x30303030u;
                     dsum = dp4a(lo | hi, xw[i], dsum);
                 }
-                const int bs = (int)(int16_t)((sw[j >> 1] >> (16 * (j & 1))) & 0xFFFF);
-                const int scj = (int)(int8_t)(scw[j >> 2] >> (8 * (j & 3)));
-                C += scj * (dsum - 32 * bs);
+                C += scj[j] * dsum;
             }
         }
-        acc[t] = fmaf(A.d[t * A.ds + B] * D, (float)C, acc[t]);
+        // the stored codes are q + 32: subtract 32 * sum_j sc_j * (16-sum j), by dp2a
+        const uint4 sv = *reinterpret_cast<const uint4*>(A.s + (t * A.nbx + B) * 16 + 8 * H);
+        int SB = __dp2a_lo((int)sv.x, (int)scw[0], 0);
+        SB = __dp2a_hi((int)sv.y, (int)scw[0], SB);
+        SB = __dp2a_lo((int)sv.z, (int)scw[1], SB);
+        SB = __dp2a_hi((int)sv.w, (int)scw[1], SB);
+        acc[t] = fmaf(A.d[t * A.ds + B] * D, (float)(C - 32 * SB), acc[t]);
     }
 }
 
