@@ -44,6 +44,7 @@ constexpr int GV_WARPS = SYN_GV_WARPS;
 constexpr int GV_NS = SYN_GV_NS;            // stages per warp ring
 constexpr int GV_STAGE = SYN_GV_STAGE;      // bytes of whole blocks per stage (at most)
 constexpr int GV_SLOT = GV_STAGE + 32;      // stage slot: data plus the alignment window
+constexpr int GV_MAX_SMS = 160;             // grid bound of the per-warp matrix table
 // A stage must hold one warp step of every format: 16 blocks of Q4_K (144 bytes) or Q6_K
 // (210 bytes, two lanes per block), 64 blocks of Q8_0 (34 bytes, two blocks per lane).
 static_assert(GV_STAGE >= 16 * 210 && GV_STAGE >= 64 * 34, "decode stage smaller than one warp step");
@@ -78,6 +79,9 @@ struct GemvBatch {
     int64_t n_tok;
     int* err;
     int off_stage, off_bar, off_flag;
+    // matrix of each decode warp of the grid: one parameter-space load instead of a
+    // dependent walk over the job table
+    uint8_t warp_job[GV_MAX_SMS * GV_WARPS];
 };
 
 // N 32-bit words starting at any even shared-memory address (aligned loads, funnel shift).
@@ -120,17 +124,17 @@ __device__ __forceinline__ int q8_chunk(int B, int c) { return 32 * B + 16 * (c 
 // in the layout the decode kernel copies to shared memory: codes with swizzled 16-byte
 // chunks, block scales, 16-sums.  One warp per 256-block (K-quants) or per four 32-blocks
 // (Q8_0).  Lets the dependent decode launch start (programmatic dependent launch) at once.
-__global__ void __launch_bounds__(256) k_act_decode(const __grid_constant__ GemvBatch b) {
+__global__ void __launch_bounds__(128) k_act_decode(const __grid_constant__ GemvBatch b) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int GW = (int)((gridDim.x * blockDim.x) >> 5);
-    // 32-bit index arithmetic only: 64-bit division runs on the (slow) fp64 pipe
-    for (int u = gw; u < b.total_units; u += GW) {
-        int j = 0;
-        while (j < b.n_jobs - 1 && u >= b.job[j + 1].unit_begin) j++;
-        const int r = u - b.job[j].unit_begin;
-        const GemvJob& J = b.job[j];
+    // one row of CTAs per matrix (blockIdx.y); 32-bit index arithmetic only (64-bit
+    // division runs on the slow fp64 pipe)
+    const int j = blockIdx.y;
+    const GemvJob& J = b.job[j];
+    const int n_units = (int)b.n_tok * J.units;
+    for (int r = gw; r < n_units; r += GW) {
         int8_t* aq = reinterpret_cast<int8_t*>(J.actg);
         float* ad = reinterpret_cast<float*>(J.actg + J.g_d);
         int16_t* as = reinterpret_cast<int16_t*>(J.actg + J.g_s);
@@ -323,12 +327,11 @@ __device__ __forceinline__ void lane_step(int type, const uint8_t* base, int bb,
 }
 
 // The warps of the grid are dealt to the matrices in proportion to their bytes (at least
-// one each, boundaries computed on the host); a matrix's rows are split evenly among its
+// one each, computed on the host into warp_job); a matrix's rows are split evenly among its
 // warps.  Returns this warp's matrix and rows [r0, r1) (empty when the matrix has fewer rows
 // than warps).  32-bit arithmetic only: 64-bit division runs on the (slow) fp64 pipe.
 __device__ __forceinline__ void warp_share(const GemvBatch& b, int gw, int& j, int64_t& r0, int64_t& r1) {
-    j = 0;
-    while (j < b.n_jobs - 1 && gw >= b.job[j].warp_end) j++;
+    j = b.warp_job[gw];
     const int nw = b.job[j].warp_end - b.job[j].warp_begin, i = gw - b.job[j].warp_begin;
     const int n = (int)b.job[j].n_out, q = n / nw, rem = n - q * nw;
     r0 = (int64_t)q * i + (rem * i) / nw;
@@ -357,11 +360,10 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
 
     // this warp's matrix and rows; the matrices of the CTA's first and last warps bound
     // the activations the CTA converts
-    int jw, ja, jb;
-    int64_t r0, r1, t0_, t1_;
+    int jw;
+    int64_t r0, r1;
     warp_share(b, gw, jw, r0, r1);
-    warp_share(b, blockIdx.x * GV_WARPS, ja, t0_, t1_);
-    warp_share(b, blockIdx.x * GV_WARPS + GV_WARPS - 1, jb, t0_, t1_);
+    const int ja = b.warp_job[blockIdx.x * GV_WARPS], jb = b.warp_job[blockIdx.x * GV_WARPS + GV_WARPS - 1];
     __syncthreads();
 
     // the matrix, in registers for the whole launch
@@ -550,6 +552,7 @@ static int64_t act_bytes_per_token(int type, int64_t n_in) {
 
 template <int NT>
 static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
+    sms = std::min(sms, GV_MAX_SMS);  // one CTA per SM, up to the size of the warp table
     int64_t off = 0;
     for (int j = 0; j < b.n_jobs; j++) {
         GemvJob& J = b.job[j];
@@ -589,6 +592,7 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
         if (j == b.n_jobs - 1) we = GW;
         J.warp_begin = w;
         J.warp_end = we;
+        for (int k = w; k < we; k++) b.warp_job[k] = (uint8_t)j;
         w = we;
     }
     // the conversion kernel: a plain launch, ordered after everything before it
@@ -600,8 +604,11 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
         units += b.n_tok * J.units;
     }
     b.total_units = (int)units;
-    const int64_t act_ctas = std::min<int64_t>((units + 7) / 8, (int64_t)sms * 4);
-    k_act_decode<<<(unsigned)std::max<int64_t>(act_ctas, 1), 256, 0, s>>>(b);
+    // one row of 4-warp CTAs per matrix, a warp per unit (up to four SMs' worth of CTAs)
+    int64_t max_units = 1;
+    for (int j = 0; j < b.n_jobs; j++) max_units = std::max<int64_t>(max_units, b.n_tok * b.job[j].units);
+    const int64_t act_x = std::min<int64_t>((max_units + 3) / 4, std::max<int64_t>(1, (int64_t)sms * 4 / b.n_jobs));
+    k_act_decode<<<dim3((unsigned)act_x, (unsigned)b.n_jobs), 128, 0, s>>>(b);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // the decode kernel, launched as its programmatic dependent: it streams weights (which the
