@@ -119,6 +119,22 @@ def build_weights(torch, syn, workloads, synth, mats, wl_id, n_copies):
     return copies
 
 
+def recorded_traffic(summary: str, source: str):
+    """DRAM bytes per launch from an ncu summary under profiles/, or None when the kernel
+    source has changed since the counters were taken (the summary records its sha256)."""
+    import hashlib
+    import re
+    try:
+        text = open(os.path.join(ROOT, "profiles", summary)).read()
+        src = open(os.path.join(ROOT, source), "rb").read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch: (\d+) \(source: (\S+) sha256 prefix ([0-9a-f]+)\)", text)
+    if not m or m.group(2) != source or not hashlib.sha256(src).hexdigest().startswith(m.group(3)):
+        return None
+    return int(m.group(1))
+
+
 def time_graphs(torch, graphs, steps, stream):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -306,7 +322,10 @@ def gpu_arm(args, rank, world, dist):
         "roofline": {"bound": "hbm", "kernel": "k_gemv<1>: one grouped decode launch of the 7 matrices "
                                                "(activation conversion fused)",
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src, "traffic": None,
+                     "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
+                     "traffic": recorded_traffic("k_gemv_llama1b_layer.md", "gguf_block_quantized_gb300/csrc/gemv.cu"),
+                     "traffic_note": "dram__bytes_read+write of k_gemv from one ncu capture (profiles/); "
+                                     "achieved/launch_us cover the conversion + decode launch pair",
                      "launch_us": round(k_time * 1e6, 3),
                      "single_launch_us": {m.name: round(tm * 1e6, 3) for m, tm in per_mat}},
         "single_call_value": {"value": round(single_value, 2), "unit": "GB/s",
