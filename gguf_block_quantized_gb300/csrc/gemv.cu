@@ -40,6 +40,12 @@ namespace syn {
 #ifndef SYN_GV_STAGE
 #define SYN_GV_STAGE 4608
 #endif
+#ifndef SYN_GV_COST_Q6_K
+#define SYN_GV_COST_Q6_K 130
+#endif
+#ifndef SYN_GV_COST_Q8_0
+#define SYN_GV_COST_Q8_0 100
+#endif
 constexpr int GV_WARPS = SYN_GV_WARPS;
 constexpr int GV_NS = SYN_GV_NS;            // stages per warp ring
 constexpr int GV_STAGE = SYN_GV_STAGE;      // bytes of whole blocks per stage (at most)
@@ -65,6 +71,11 @@ struct GemvJob {
     int units;              // conversion-kernel units (warp steps) per token
     int unit_begin;         // first conversion unit of this matrix (all tokens of earlier ones)
     int warp_begin, warp_end;  // the decode warps of this matrix
+    int upr;                // work units per row: 1 (whole rows), or 2 for rows of two stages
+                            // runs: the two runs may go to different warps and are then added
+                            // into Y (zeroed by the conversion kernel; a sum of two partials
+                            // onto zero does not depend on their order)
+    int n_units;            // n_out * upr
     int ds;                 // per-token stride of the activation scales (floats, multiple of 4)
     int act_q, act_d, act_s;  // shared-memory offsets of the converted activations (NT tokens)
     uint8_t* actg;          // the same, for all n_tok tokens, in the global workspace:
@@ -133,6 +144,10 @@ __global__ void __launch_bounds__(128) k_act_decode(const __grid_constant__ Gemv
     // division runs on the slow fp64 pipe)
     const int j = blockIdx.y;
     const GemvJob& J = b.job[j];
+    if (J.upr > 1) {  // runs of this matrix's rows are added into Y by different warps
+        const int ny = (int)b.n_tok * (int)J.n_out;
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ny; i += gridDim.x * blockDim.x) J.Y[i] = 0.f;
+    }
     const int n_units = (int)b.n_tok * J.units;
     for (int r = gw; r < n_units; r += GW) {
         int8_t* aq = reinterpret_cast<int8_t*>(J.actg);
@@ -326,16 +341,17 @@ __device__ __forceinline__ void lane_step(int type, const uint8_t* base, int bb,
     }
 }
 
-// The warps of the grid are dealt to the matrices in proportion to their bytes (at least
-// one each, computed on the host into warp_job); a matrix's rows are split evenly among its
-// warps.  Returns this warp's matrix and rows [r0, r1) (empty when the matrix has fewer rows
-// than warps).  32-bit arithmetic only: 64-bit division runs on the (slow) fp64 pipe.
-__device__ __forceinline__ void warp_share(const GemvBatch& b, int gw, int& j, int64_t& r0, int64_t& r1) {
+// The warps of the grid are dealt to the matrices so that the largest per-warp byte count is
+// as small as it can be (computed on the host into warp_job); a matrix's work units (rows, or
+// runs of rows wider than a stage) are split evenly among its warps.  Returns this warp's
+// matrix and units [u0, u1) (empty when the matrix has fewer units than warps).  32-bit
+// arithmetic only: 64-bit division runs on the (slow) fp64 pipe.
+__device__ __forceinline__ void warp_share(const GemvBatch& b, int gw, int& j, int& u0, int& u1) {
     j = b.warp_job[gw];
     const int nw = b.job[j].warp_end - b.job[j].warp_begin, i = gw - b.job[j].warp_begin;
-    const int n = (int)b.job[j].n_out, q = n / nw, rem = n - q * nw;
-    r0 = (int64_t)q * i + (rem * i) / nw;
-    r1 = (int64_t)q * (i + 1) + (rem * (i + 1)) / nw;
+    const int n = b.job[j].n_units, q = n / nw, rem = n - q * nw;
+    u0 = q * i + (rem * i) / nw;
+    u1 = q * (i + 1) + (rem * (i + 1)) / nw;
 }
 
 template <int NT>
@@ -360,9 +376,8 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
 
     // this warp's matrix and rows; the matrices of the CTA's first and last warps bound
     // the activations the CTA converts
-    int jw;
-    int64_t r0, r1;
-    warp_share(b, gw, jw, r0, r1);
+    int jw, u0, u1;
+    warp_share(b, gw, jw, u0, u1);
     const int ja = b.warp_job[blockIdx.x * GV_WARPS], jb = b.warp_job[blockIdx.x * GV_WARPS + GV_WARPS - 1];
     __syncthreads();
 
@@ -374,13 +389,19 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
     const int type = Jp.type, nb = Jp.nb, bb = Jp.bb, lg = Jp.lg_nb, bps = Jp.bps;
     const int sblk = Jp.stage_blocks;
     const int rps = sblk >= nb ? sblk / nb : 0;  // whole rows per stage (0: runs of one row)
+    const int upr = Jp.upr;
+    const bool split = upr > 1;                   // each run is a unit, added into Y
+    // first row and block column of this warp's units; units end at u1
+    const int64_t r0 = split ? u0 / upr : u0;
+    const int b0 = split ? (u0 - (u0 / upr) * upr) * sblk : 0;
+    const int64_t r1 = u1;  // unsplit matrices: units are rows
     const ActView A{reinterpret_cast<const int8_t*>(smem + Jp.act_q), reinterpret_cast<const float*>(smem + Jp.act_d),
                     reinterpret_cast<const int16_t*>(smem + Jp.act_s), Jp.n_in, Jp.nbx, Jp.ds};
 
     // stage extent at (row, bcol): blocks and whole rows (0 for a run inside one row)
     auto extent = [&](int64_t row, int bcol, int& nblk, int& nrows) {
         if (rps > 0) {
-            nrows = (int)min((int64_t)rps, r1 - row);
+            nrows = (int)min((int64_t)rps, r1 - row);  // whole-row matrices only
             nblk = nrows * nb;
         } else {
             nrows = 0;
@@ -424,13 +445,16 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
     for (int64_t t0 = 0; t0 < b.n_tok && !failed; t0 += NT) {
         // weights first: the copies are in flight while the activations are converted
         int64_t irow = r0;
-        int ibcol = 0;
+        int ibcol = b0;
+        int iu = u0;  // units issued so far (rows, or runs of split matrices)
         uint32_t qi = seq;
-        for (int k = 0; k < GV_NS - 1 && irow < r1; k++) {
+        auto more = [&](int64_t row, int u) { return split ? u < u1 : row < r1; };
+        for (int k = 0; k < GV_NS - 1 && more(irow, iu); k++) {
             int nblk, nrows;
             extent(irow, ibcol, nblk, nrows);
             issue(irow, ibcol, nblk, (qi++) % GV_NS);
             advance(irow, ibcol, nblk, nrows);
+            iu++;
         }
         // the converted activations of tokens t0.. of the CTA's matrices: written by the
         // conversion kernel this launch depends on, so wait for it first
@@ -461,15 +485,17 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
 #pragma unroll
         for (int t = 0; t < NT; t++) acc[t] = 0.f;
         int64_t crow = r0;
-        int cbcol = 0;
+        int cbcol = b0;
+        int cu = u0;
         uint32_t qc = seq;
-        while (crow < r1) {
-            if (irow < r1) {
+        while (more(crow, cu)) {
+            if (more(irow, iu)) {
                 int nblk, nrows;
                 extent(irow, ibcol, nblk, nrows);
                 __syncwarp();
                 issue(irow, ibcol, nblk, (qi++) % GV_NS);
                 advance(irow, ibcol, nblk, nrows);
+                iu++;
             }
             const uint32_t s = qc % GV_NS;
             if (!mbar_wait(bar0 + 8 * s, (qc / GV_NS) & 1, b.err, abort_flag)) {
@@ -516,11 +542,14 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
                     const uint8_t* rowp = sbase + (int64_t)r * nb * bb;
                     for (int s0 = 0; s0 < per_row; s0 += bps)
                         lane_step<NT>(type, rowp, bb, s0, per_row - s0, bstart + s0, -1, A, acc);
-                    if (nrows > 0 || cbcol + nblk == nb) {
+                    if (nrows > 0 || split || cbcol + nblk == nb) {
 #pragma unroll
                         for (int t = 0; t < NT; t++) {
                             const float v = warp_sum(acc[t]);
-                            if (lane == 0 && t0 + t < b.n_tok) Y[(t0 + t) * n_out + crow + r] = v;
+                            if (lane == 0 && t0 + t < b.n_tok) {
+                                if (split) atomicAdd(Y + (t0 + t) * n_out + crow + r, v);
+                                else Y[(t0 + t) * n_out + crow + r] = v;
+                            }
                             acc[t] = 0.f;
                         }
                     }
@@ -528,6 +557,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
             }
             __syncwarp();
             advance(crow, cbcol, nblk, nrows);
+            cu++;
         }
         seq = qi;
     }
@@ -579,22 +609,52 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    // warps per matrix, in proportion to bytes, at least one each
+    // Warps per matrix: the smallest per-warp byte bound T for which ceil(units / units per
+    // warp) warps of every matrix fit in the grid (units per warp = floor(T / unit bytes)),
+    // found by bisection; the warps left over go to the matrices in proportion to bytes.
     const int GW = sms * GV_WARPS;
+    // cost of a unit: its bytes, weighted by the format's decode work per byte (percent)
+    auto unit_bytes = [&](const GemvJob& J) {
+        const int64_t by = J.upr > 1 ? (int64_t)J.stage_blocks * J.bb : J.row_bytes;
+        const int64_t w = J.type == SYN_Q6_K ? SYN_GV_COST_Q6_K : J.type == SYN_Q8_0 ? SYN_GV_COST_Q8_0 : 100;
+        return by * w / 100;
+    };
+    auto warps_for = [&](const GemvJob& J, int64_t T) {
+        const int64_t per = std::max<int64_t>(1, T / unit_bytes(J));
+        return (J.n_units + per - 1) / per;
+    };
+    int64_t lo = 1, hi = 1;
+    for (int j = 0; j < b.n_jobs; j++) hi = std::max<int64_t>(hi, (int64_t)b.job[j].n_units * unit_bytes(b.job[j]));
+    while (lo < hi) {
+        const int64_t T = lo + (hi - lo) / 2;
+        int64_t need = 0;
+        for (int j = 0; j < b.n_jobs; j++) need += warps_for(b.job[j], T);
+        if (need <= GW) hi = T;
+        else lo = T + 1;
+    }
+    int64_t nw[GEMV_MAX_JOBS], used = 0;
+    for (int j = 0; j < b.n_jobs; j++) {
+        nw[j] = std::min<int64_t>(warps_for(b.job[j], lo), b.job[j].n_units);
+        nw[j] = std::max<int64_t>(nw[j], 1);
+        used += nw[j];
+    }
+    if (used > GW) return cudaErrorInvalidConfiguration;  // more matrices than warps
+    const int64_t spare = GW - used;
+    for (int j = 0; j < b.n_jobs && spare > 0; j++) {
+        const GemvJob& J = b.job[j];
+        const int64_t extra = (int64_t)((double)spare * (double)(J.n_out * J.row_bytes) / (double)b.total_bytes);
+        nw[j] = std::min<int64_t>(nw[j] + extra, std::max<int64_t>(nw[j], J.n_units));
+    }
     int w = 0;
-    int64_t cum = 0;
     for (int j = 0; j < b.n_jobs; j++) {
         GemvJob& J = b.job[j];
-        cum += J.n_out * J.row_bytes;
-        int we = (int)((double)cum * GW / (double)b.total_bytes);
-        we = std::max(we, w + 1);
-        we = std::min(we, GW - (b.n_jobs - 1 - j));
-        if (j == b.n_jobs - 1) we = GW;
         J.warp_begin = w;
-        J.warp_end = we;
-        for (int k = w; k < we; k++) b.warp_job[k] = (uint8_t)j;
-        w = we;
+        J.warp_end = w + (int)nw[j];
+        for (int k = J.warp_begin; k < J.warp_end; k++) b.warp_job[k] = (uint8_t)j;
+        w = J.warp_end;
     }
+    for (int k = w; k < GW; k++) b.warp_job[k] = (uint8_t)(b.n_jobs - 1);  // idle: share of the last
+    if (w < GW) b.job[b.n_jobs - 1].warp_end = GW;
     // the conversion kernel: a plain launch, ordered after everything before it
     int64_t units = 0;
     for (int j = 0; j < b.n_jobs; j++) {
@@ -657,6 +717,8 @@ static void make_job(GemvJob& J, const GemvDesc& d, int64_t byte_begin) {
     } else {
         J.stage_blocks = (fit / J.bps) * J.bps;  // runs of one row
     }
+    J.upr = (J.nb > J.stage_blocks && J.nb <= 2 * J.stage_blocks) ? 2 : 1;
+    J.n_units = (int)(d.n_out * J.upr);
 }
 
 int64_t gemv_act_bytes(int type, int64_t n_in) { return act_bytes_per_token(type, n_in) + 64; }

@@ -176,8 +176,10 @@ def run_mul_mat(syn, wt, n_out, n_in, n_tok, seed, path, wstd=0.02):
     return Y, ref, tolerance(wt, Wq, n_in, X)
 
 
+# (77, 8192) and (40, 12288): rows of two stages' worth of blocks (split across warps, added into
+# Y) and wider rows (several runs in one warp), per format
 GEMV_SHAPES = [(1, 256, 1), (37, 512, 1), (300, 768, 2), (64, 2304, 3), (513, 1024, 4), (250, 4096, 8),
-               (129, 512, 11)]
+               (129, 512, 11), (77, 8192, 1), (40, 12288, 2)]
 
 
 @pytest.mark.parametrize("wt", TYPES_W)
@@ -263,6 +265,27 @@ def test_gemv_deterministic(syn):
     a = host(syn.mul_mat(wt, W, n_out, n_in, X))
     b = host(syn.mul_mat(wt, W, n_out, n_in, X))
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_gemv_split_rows_deterministic(syn):
+    """Rows whose two runs go to different warps are added into Y: the result must not depend
+    on the order of the two additions (bit-identical across calls) and must match the oracle."""
+    shapes = [(oracle.Q6_K, 600, 8192), (oracle.Q4_K, 200, 12288), (oracle.Q8_0, 333, 8192)]
+    items, refs = [], []
+    for i, (wt, n_out, n_in) in enumerate(shapes):
+        Wq = oracle.quantize(wt, synth.normal(500 + i, (n_out, n_in), 0.02))
+        X = synth.normal(600 + i, (2, n_in))
+        items.append((wt, dev(Wq), n_out, n_in, dev(X), torch.full((2, n_out), float("nan"), device="cuda")))
+        refs.append((oracle.mul_mat(wt, Wq, n_out, n_in, X), tolerance(wt, Wq, n_in, X)))
+    outs = []
+    for _ in range(3):
+        syn.mul_mat_batch(items, 2)
+        outs.append([host(it[5]).copy() for it in items])
+    for k in range(len(shapes)):
+        assert_close(outs[0][k], refs[k][0], refs[k][1], f"split rows {shapes[k]}")
+        for o in outs[1:]:
+            assert np.array_equal(o[k].view(np.uint32), outs[0][k].view(np.uint32))
+    assert syn.device_status() == syn.OK
 
 
 def test_mul_mat_zero_and_degenerate(syn):
