@@ -300,6 +300,8 @@ def gpu_arm(args, rank, world, dist):
     pre_time = sum(r["ms"] for r in pre_res) / 1e3
     pre_tflops = pre_flops / pre_time / 1e12
 
+    configs = other_configs(torch, syn, synth, workloads, stream, l2, hbm_peak, tc_peak, args.quick)
+
     clocks = clk.summary()
     out = {
         "metric": METRIC,
@@ -340,7 +342,116 @@ def gpu_arm(args, rank, world, dist):
                                  "frac": round(pre_tflops / tc_peak, 4), "peak_source": peak_src,
                                  "note": "fp16 operands; bf16 measured peak used (same nominal rate)"},
                     "matrices": pre_res},
+        "configs": configs,
     }
+    return out
+
+
+def time_calls(torch, stream, fn, n_variants, reps, trials=5):
+    """Median time of one fn(c) call (c cycles over n_variants) in graphs of `reps` calls."""
+    for c in range(n_variants):
+        fn(c)
+    torch.cuda.synchronize()
+    gs = []
+    for g0 in range(min(4, n_variants)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(reps):
+                fn((g0 * reps + r) % n_variants)
+        gs.append(g)
+    for g in gs:
+        g.replay()
+    ts = []
+    for _ in range(trials):
+        ts.append(time_graphs(torch, gs, len(gs), stream) / (len(gs) * reps))
+    return sorted(ts)[len(ts) // 2]
+
+
+def other_configs(torch, syn, synth, workloads, stream, l2, hbm_peak, tc_peak, quick):
+    """The workloads besides the headline one: Q8_0 2048x2048 and the Q6_K lm_head as decode
+    products (rotating copies >= 4x L2), and the Llama-8B Q4_K_M weight sweep (every
+    projection of 32 layers + lm_head) as decode at 1 token and as prefill at 2048 tokens.
+    The sweep's 4.6 GB of weights are drawn on the device (torch's Philox generator, seeds
+    5000 + i) and quantized with syn_quantize; numpy on the host would take minutes."""
+    out = {}
+
+    def gemv_cfg(name, mats, wl_id, n_tok):
+        set_bytes = sum(m.weight_bytes for m in mats)
+        n_cop = max(2, -(-4 * l2 // set_bytes))
+        W = build_weights(torch, syn, workloads, synth, mats, wl_id, n_cop)
+        X = [torch.from_numpy(synth.activations(wl_id, i, n_tok, m.n_in)).cuda() for i, m in enumerate(mats)]
+        Y = [torch.empty((n_tok, m.n_out), device="cuda") for m in mats]
+
+        def fn(c):
+            for i, m in enumerate(mats):
+                syn.mul_mat(m.wtype, W[c][i], m.n_out, m.n_in, X[i], Y=Y[i], stream=stream)
+        t = time_calls(torch, stream, fn, n_cop, 20)
+        alg = sum(workloads.gemv_bytes(m, n_tok) for m in mats)
+        out[name] = {"value": round(alg / t / 1e9, 1), "unit": "GB/s", "frac": round(alg / t / 1e9 / hbm_peak, 4),
+                     "us": round(t * 1e6, 3), "n_tok": n_tok, "alg_bytes": alg}
+        del W
+
+    gemv_cfg("q8_0_2048x2048_decode", workloads.Q8_0_SQUARE, 1, 1)
+    gemv_cfg("q6_k_lm_head_decode_1tok", workloads.LM_HEAD_1B, 3, 1)
+    gemv_cfg("q6_k_lm_head_decode_4tok", workloads.LM_HEAD_1B, 3, 4)
+    torch.cuda.empty_cache()
+    if quick:
+        return out
+
+    # Llama-8B Q4_K_M sweep
+    mats = workloads.llama8b_q4_k_m()
+    gen = torch.Generator(device="cuda")
+    W = []
+    for i, m in enumerate(mats):
+        gen.manual_seed(5000 + i)
+        w32 = torch.randn((m.n_out, m.n_in), generator=gen, device="cuda") * 0.02
+        W.append(syn.quantize(m.wtype, w32))
+        del w32
+    torch.cuda.empty_cache()
+    dims = sorted({m.n_in for m in mats})
+    layers = [mats[7 * k:7 * k + 7] for k in range(len(mats) // 7)]
+    head = mats[-1]
+    wsum = sum(m.weight_bytes for m in mats)
+
+    def inputs(n_tok, seed):
+        gen.manual_seed(seed)
+        return {d: torch.randn((n_tok, d), generator=gen, device="cuda") for d in dims}
+
+    # decode: one syn_mul_mat_batch per layer (its seven projections) + the lm_head
+    X1 = inputs(1, 4999)
+    Y1 = [torch.empty((1, m.n_out), device="cuda") for m in mats]
+
+    def token(_c):
+        for k, lay in enumerate(layers):
+            syn.mul_mat_batch([(m.wtype, W[7 * k + i], m.n_out, m.n_in, X1[m.n_in], Y1[7 * k + i])
+                               for i, m in enumerate(lay)], 1, stream=stream)
+        syn.mul_mat(head.wtype, W[-1], head.n_out, head.n_in, X1[head.n_in], Y=Y1[-1], stream=stream)
+    t = time_calls(torch, stream, token, 1, 1)
+    alg = sum(workloads.gemv_bytes(m, 1) for m in mats)
+    out["llama8b_q4_k_m_decode_1tok"] = {"value": round(alg / t / 1e9, 1), "unit": "GB/s",
+                                         "frac": round(alg / t / 1e9 / hbm_peak, 4), "ms_per_token": round(t * 1e3, 4),
+                                         "weight_bytes": wsum, "matrices": len(mats),
+                                         "api": "syn_mul_mat_batch per layer + syn_mul_mat for the lm_head"}
+    del X1, Y1
+    # prefill at 2048 tokens: one syn_mul_mat per matrix
+    p_tok = 2048
+    XP = inputs(p_tok, 4998)
+    YP = {}
+    for m in mats:
+        if m.n_out not in YP:
+            YP[m.n_out] = torch.empty((p_tok, m.n_out), device="cuda")
+    syn.syn_reserve(max(dims), p_tok, stream.cuda_stream)
+
+    def prefill(_c):
+        for i, m in enumerate(mats):
+            syn.mul_mat(m.wtype, W[i], m.n_out, m.n_in, XP[m.n_in], Y=YP[m.n_out], stream=stream)
+    t = time_calls(torch, stream, prefill, 1, 1, trials=3)
+    fl = sum(workloads.gemm_flops(m, p_tok) for m in mats)
+    out["llama8b_q4_k_m_prefill_2048tok"] = {"value": round(fl / t / 1e12, 1), "unit": "TFLOP/s",
+                                             "frac": round(fl / t / 1e12 / tc_peak, 4), "ms": round(t * 1e3, 3),
+                                             "flops": fl, "matrices": len(mats)}
+    del W, XP, YP
+    torch.cuda.empty_cache()
     return out
 
 
@@ -379,6 +490,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="syn", choices=["syn", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--quick", action="store_true", help="skip the Llama-8B weight sweep")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -358,3 +358,31 @@ def test_full_lm_head(syn, n_tok):
 @pytest.mark.parametrize("i", range(len(workloads.LLAMA8B_FFN)))
 def test_full_llama8b_ffn_prefill(syn, i):
     sampled_check(syn, workloads.LLAMA8B_FFN[i], 512, 4, i, n_rows=48, n_toks=6)
+
+
+# the Llama-8B Q4_K_M sweep: one matrix of every distinct (format, shape) in the mix, as the
+# decode product (1 token) and as the prefill product (2048 tokens), sampled entries
+def _llama8b_distinct():
+    mats = workloads.llama8b_q4_k_m()
+    seen, picks = set(), []
+    for i, m in enumerate(mats):
+        key = (m.wtype, m.n_out, m.n_in)
+        if key not in seen:
+            seen.add(key)
+            picks.append((i, m))
+    return picks
+
+
+LLAMA8B_DISTINCT = _llama8b_distinct()
+
+
+@pytest.mark.parametrize("k", range(len(LLAMA8B_DISTINCT)))
+def test_full_llama8b_sweep_decode(syn, k):
+    i, m = LLAMA8B_DISTINCT[k]
+    sampled_check(syn, m, 1, 5, i, n_rows=96, path="gemv")
+
+
+@pytest.mark.parametrize("k", range(len(LLAMA8B_DISTINCT)))
+def test_full_llama8b_sweep_prefill(syn, k):
+    i, m = LLAMA8B_DISTINCT[k]
+    sampled_check(syn, m, 2048, 5, i, n_rows=32, n_toks=4, path="gemm")
