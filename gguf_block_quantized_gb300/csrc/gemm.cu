@@ -38,9 +38,6 @@ namespace syn {
 constexpr int GEMM_BM = 128;
 constexpr int GEMM_BK = 64;           // one 128-byte swizzle row of fp16
 constexpr int GEMM_SUPER = 256;       // k per raw weight stage
-#ifndef SYN_GEMM_DEQ_FOLD
-#define SYN_GEMM_DEQ_FOLD 0
-#endif
 // dequantizer teams: team t handles the 64-k steps with step index = t (mod teams); each
 // team is 8 warps (128 rows x two 32-k halves)
 #ifndef SYN_GEMM_DEQ_TEAMS
@@ -221,29 +218,40 @@ __device__ __forceinline__ void split_h2(float v, __half2& hi, __half2& lo) {
 __device__ __forceinline__ __half2 bytes01_h2(uint32_t v) { return u32_as_h2(__byte_perm(v, 0x64646464u, 0x4140)); }
 __device__ __forceinline__ __half2 bytes23_h2(uint32_t v) { return u32_as_h2(__byte_perm(v, 0x64646464u, 0x4342)); }
 
-// Q4_K: 64-k step c of the super-block, half h (sub-block j = 2c + h).
-__device__ __forceinline__ void deq32_q4_k(const uint8_t* blk, int c, int h, uint32_t out[16]) {
+// The scales a dequantizing thread needs in one 256-k super-step are decoded once, when the
+// raw stage arrives: a thread expands row r, k-half h of the two 64-k steps c0 and c0 + 2 of
+// the super-step that its team takes (c0 = 0 or 1).
+
+// Q4_K: the thread's sub-blocks are j = 2c + h: j0 = 2*c0 + h (scales in the low words)
+// and j0 + 4 (high words).  The 1024 of the byte permute is folded into the offset:
+// w = S*(1024 + q) - (1024*S + M).
+struct Q4Prep {
+    __half2 Sh[2], Sl[2], nCh[2], nCl[2];
+};
+__device__ __forceinline__ void prep_q4_k(const uint8_t* blk, int c0, int h, Q4Prep& P) {
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
     const float D = h2f_bits(hdr.x & 0xFFFF), Dm = h2f_bits(hdr.x >> 16);
-    const int j = 2 * c + h, jj = j & 3, sh = 8 * jj;
-    int sc, mn;
-    if (j < 4) {
-        sc = (hdr.y >> sh) & 63;
-        mn = (hdr.z >> sh) & 63;
-    } else {
-        sc = ((hdr.w >> sh) & 15) | (((hdr.y >> (sh + 6)) & 3) << 4);
-        mn = ((hdr.w >> (sh + 4)) & 15) | (((hdr.z >> (sh + 6)) & 3) << 4);
-    }
+    // 6-bit scales / mins of sub-blocks 0..3 and 4..7, one per byte
+    const uint32_t sc_lo = hdr.y & 0x3F3F3F3Fu, mn_lo = hdr.z & 0x3F3F3F3Fu;
+    const uint32_t sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+    const uint32_t mn_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+    const uint32_t sel = 0x4440u | (uint32_t)(2 * c0 + h);
+    const float S0 = D * (float)__byte_perm(sc_lo, 0, sel), M0 = Dm * (float)__byte_perm(mn_lo, 0, sel);
+    const float S1 = D * (float)__byte_perm(sc_hi, 0, sel), M1 = Dm * (float)__byte_perm(mn_hi, 0, sel);
+    split_h2(S0, P.Sh[0], P.Sl[0]);
+    split_h2(-fmaf(1024.0f, S0, M0), P.nCh[0], P.nCl[0]);
+    split_h2(S1, P.Sh[1], P.Sl[1]);
+    split_h2(-fmaf(1024.0f, S1, M1), P.nCh[1], P.nCl[1]);
+}
+// step c = c0 + 2i of the super-block
+__device__ __forceinline__ void deq32_q4_k(const uint8_t* blk, int c, int h, const Q4Prep& P, int i, uint32_t out[16]) {
     const __half2 tail = __float2half2_rn(1.0f / 4096.0f);
+    // (selects, not indexing: a runtime index would put the struct in local memory)
+    const __half2 Sh = i ? P.Sh[1] : P.Sh[0], Sl = i ? P.Sl[1] : P.Sl[0];
+    const __half2 nCh = i ? P.nCh[1] : P.nCh[0], nCl = i ? P.nCl[1] : P.nCl[0];
     const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
     const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c + 16);
     const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    const float S = D * (float)sc, M = Dm * (float)mn;
-#if SYN_GEMM_DEQ_FOLD
-    // fold the 1024 of the byte permute into the offset: w = S*(1024 + q) - (1024*S + M)
-    __half2 Sh, Sl, nCh, nCl;
-    split_h2(S, Sh, Sl);
-    split_h2(-fmaf(1024.0f, S, M), nCh, nCl);
 #pragma unroll
     for (int w = 0; w < 8; w++) {
         const uint32_t v = (qw[w] >> (4 * h)) & 0x0F0F0F0Fu;
@@ -251,39 +259,38 @@ __device__ __forceinline__ void deq32_q4_k(const uint8_t* blk, int c, int h, uin
         out[2 * w] = h2_as_u32(__hfma2(__hfma2(qa, Sl, nCl), tail, __hfma2(qa, Sh, nCh)));
         out[2 * w + 1] = h2_as_u32(__hfma2(__hfma2(qb, Sl, nCl), tail, __hfma2(qb, Sh, nCh)));
     }
-#else
-    __half2 Sh, Sl, nMh, nMl;
-    split_h2(S, Sh, Sl);
-    split_h2(-M, nMh, nMl);
-    const __half2 k1024 = __float2half2_rn(1024.0f);
-#pragma unroll
-    for (int w = 0; w < 8; w++) {
-        const uint32_t v = (qw[w] >> (4 * h)) & 0x0F0F0F0Fu;
-        const __half2 qa = __hsub2(bytes01_h2(v), k1024), qb = __hsub2(bytes23_h2(v), k1024);
-        out[2 * w] = h2_as_u32(__hfma2(__hfma2(qa, Sl, nMl), tail, __hfma2(qa, Sh, nMh)));
-        out[2 * w + 1] = h2_as_u32(__hfma2(__hfma2(qb, Sl, nMl), tail, __hfma2(qb, Sh, nMh)));
-    }
-#endif
 }
 
-// Q6_K: 64-k step c of the super-block (half H = c/2), thread half h: quarter
-// qd = 2*(c%2) + h of the half, weights l + 32*qd for l = 0..31.
-__device__ __forceinline__ void deq32_q6_k(const uint8_t* blk, int c, int h, uint32_t out[16]) {
-    const int H = c >> 1, qd = 2 * (c & 1) + h;
+// Q6_K: step c covers half H = c / 2 of the block; the thread expands quarter
+// qd = 2*(c % 2) + h of that half (weights l + 32*qd, l = 0..31, sub-blocks 2*qd and
+// 2*qd + 1 of the half).  For steps c0 and c0 + 2: qd = 2*c0 + h in halves 0 and 1.
+struct Q6Prep {
+    __half2 Sh[2][2], Sl[2][2];
+};
+__device__ __forceinline__ void prep_q6_k(const uint8_t* blk, int c0, int h, Q6Prep& P) {
     const float D = h2f_bits(*reinterpret_cast<const uint16_t*>(blk + 208));
-    const int8_t* scs = reinterpret_cast<const int8_t*>(blk + 192 + 8 * H + 2 * qd);
-    __half2 S0h, S0l, S1h, S1l;
-    split_h2(D * (float)scs[0], S0h, S0l);
-    split_h2(D * (float)scs[1], S1h, S1l);
+    const int8_t* scs = reinterpret_cast<const int8_t*>(blk + 192);
+    const int qd = 2 * c0 + h;
+    const int s00 = scs[2 * qd], s01 = scs[2 * qd + 1], s10 = scs[8 + 2 * qd], s11 = scs[9 + 2 * qd];
+    split_h2(D * (float)s00, P.Sh[0][0], P.Sl[0][0]);
+    split_h2(D * (float)s01, P.Sh[0][1], P.Sl[0][1]);
+    split_h2(D * (float)s10, P.Sh[1][0], P.Sl[1][0]);
+    split_h2(D * (float)s11, P.Sh[1][1], P.Sl[1][1]);
+}
+__device__ __forceinline__ void deq32_q6_k(const uint8_t* blk, int c, int h, const Q6Prep& P, int i, uint32_t out[16]) {
+    const int H = c >> 1, qd = 2 * (c & 1) + h;
     const __half2 k1056 = __float2half2_rn(1056.0f);  // 1024 + 32
     const __half2 tail = __float2half2_rn(1.0f / 4096.0f);
-    const uint8_t* ql = blk + 64 * H + ((qd & 1) ? 32 : 0);
-    const uint8_t* qh = blk + 128 + 32 * H;
+    uint32_t ql[8], qh[8];
+    lds_words_any<8>(blk + 64 * H + ((qd & 1) ? 32 : 0), ql);
+    lds_words_any<8>(blk + 128 + 32 * H, qh);
     const int nsh = (qd >= 2) ? 4 : 0, hsh = 2 * qd;
+    const __half2 S0h = i ? P.Sh[1][0] : P.Sh[0][0], S0l = i ? P.Sl[1][0] : P.Sl[0][0];
+    const __half2 S1h = i ? P.Sh[1][1] : P.Sh[0][1], S1l = i ? P.Sl[1][1] : P.Sl[0][1];
 #pragma unroll
     for (int w = 0; w < 8; w++) {
-        const uint32_t lo = (lds_u32_any(ql + 4 * w) >> nsh) & 0x0F0F0F0Fu;
-        const uint32_t hi = ((lds_u32_any(qh + 4 * w) >> hsh) & 0x03030303u) << 4;
+        const uint32_t lo = (ql[w] >> nsh) & 0x0F0F0F0Fu;
+        const uint32_t hi = ((qh[w] >> hsh) & 0x03030303u) << 4;
         const uint32_t v = lo | hi;
         const __half2 Sh = (w < 4) ? S0h : S1h, Sl = (w < 4) ? S0l : S1l;
         const __half2 qa = __hsub2(bytes01_h2(v), k1056), qb = __hsub2(bytes23_h2(v), k1056);
@@ -296,9 +303,11 @@ __device__ __forceinline__ void deq32_q6_k(const uint8_t* blk, int c, int h, uin
 __device__ __forceinline__ void deq32_q8_0(const uint8_t* blk, uint32_t out[16]) {
     const __half2 D = u32_as_h2(__byte_perm(*reinterpret_cast<const uint16_t*>(blk), 0, 0x1010));
     const __half2 k1152 = __float2half2_rn(1152.0f);  // 1024 + 128
+    uint32_t q[8];
+    lds_words_any<8>(blk + 2, q);
 #pragma unroll
     for (int w = 0; w < 8; w++) {
-        const uint32_t v = lds_u32_any(blk + 2 + 4 * w) ^ 0x80808080u;  // int8 -> offset binary
+        const uint32_t v = q[w] ^ 0x80808080u;  // int8 -> offset binary
         out[2 * w] = h2_as_u32(__hmul2(__hsub2(bytes01_h2(v), k1152), D));
         out[2 * w + 1] = h2_as_u32(__hmul2(__hsub2(bytes23_h2(v), k1152), D));
     }
@@ -552,14 +561,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const int64_t src = o * p.row_bytes + (int64_t)ss * F::SB_BYTES;
                 const uint8_t* row = sRaw + rs * RAW_STAGE + r * p.raw_row + (int)(src & 15);
                 const int nst = steps_in(ss);
+                // this team's steps of the super-step: c0 and c0 + 2 (K-quants: 4 steps each)
+                const int c0 = (int)((team + GEMM_DEQ_TEAMS - kc % GEMM_DEQ_TEAMS) % GEMM_DEQ_TEAMS);
+                Q4Prep p4;
+                Q6Prep p6;
+                if (T == SYN_Q4_K && row_ok) prep_q4_k(row, c0, h, p4);
+                if (T == SYN_Q6_K && row_ok) prep_q6_k(row, c0, h, p6);
                 for (int k4 = 0; k4 < nst; k4++, kc++) {
                     if (kc % GEMM_DEQ_TEAMS != team) continue;
                     const int ks = kc % GEMM_A_STAGES;
                     uint32_t out[16];
                     const int64_t kglob = (int64_t)ss * GEMM_SUPER + k4 * GEMM_BK + h * 32;
                     if (row_ok && kglob < p.n_in) {
-                        if (T == SYN_Q4_K) deq32_q4_k(row, k4, h, out);
-                        else if (T == SYN_Q6_K) deq32_q6_k(row, k4, h, out);
+                        if (T == SYN_Q4_K) deq32_q4_k(row, k4, h, p4, k4 >> 1, out);
+                        else if (T == SYN_Q6_K) deq32_q6_k(row, k4, h, p6, k4 >> 1, out);
                         else deq32_q8_0(row + (2 * k4 + h) * 34, out);
                     } else {
 #pragma unroll

@@ -95,21 +95,6 @@ struct GemvBatch {
     uint8_t warp_job[GV_MAX_SMS * GV_WARPS];
 };
 
-// N 32-bit words starting at any even shared-memory address (aligned loads, funnel shift).
-template <int N>
-__device__ __forceinline__ void lds_words_any(const uint8_t* p, uint32_t* out) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-    const uint32_t sh = static_cast<uint32_t>(a & 3) * 8;
-    uint32_t prev = w[0];
-#pragma unroll
-    for (int i = 0; i < N; i++) {
-        const uint32_t nxt = w[i + 1];
-        out[i] = __funnelshift_r(prev, nxt, sh);
-        prev = nxt;
-    }
-}
-
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
