@@ -14,6 +14,7 @@ Parity status per function (see the tests under tests/test_oracle_*.py for the p
   quantize Q8_0/Q8_K     pinned (hand blocks, error bound, fixed point, bsum invariant)
   quantize Q4_K/Q6_K     pinned to error bounds, fixed point and hand blocks; the encoders
                          themselves are the plain readings of the format table
+  quantize Q4_0/Q5_0     pinned to error bounds, the exact extreme, hand blocks
   dequantize             pinned (hand-written block bytes against the format formulas)
   block sums / mul_mat   pinned (fp64 brute force over dequantized blocks, the
                          ggml_mul_mat orientation example with exact integers)
@@ -29,11 +30,11 @@ import threading
 
 import numpy as np
 
-Q8_0, Q4_K, Q6_K, Q8_K = 1, 2, 3, 4
-BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, Q8_K: 256}
-BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, Q8_K: 292}
-VEC_DOT_TYPE = {Q8_0: Q8_0, Q4_K: Q8_K, Q6_K: Q8_K}
-NAMES = {Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K", Q8_K: "Q8_K"}
+Q8_0, Q4_K, Q6_K, Q8_K, Q4_0, Q5_0 = 1, 2, 3, 4, 5, 6
+BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, Q8_K: 256, Q4_0: 32, Q5_0: 32}
+BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, Q8_K: 292, Q4_0: 18, Q5_0: 22}
+VEC_DOT_TYPE = {Q8_0: Q8_0, Q4_K: Q8_K, Q6_K: Q8_K, Q4_0: Q8_0, Q5_0: Q8_0}
+NAMES = {Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K", Q8_K: "Q8_K", Q4_0: "Q4_0", Q5_0: "Q5_0"}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "syn_oracle.c")
@@ -85,6 +86,8 @@ def lib():
             L.orc_dequantize.restype = i32
             L.orc_unpack_q4_k.argtypes = [vp, vp, vp, vp, vp, vp]
             L.orc_unpack_q6_k.argtypes = [vp, vp, vp, vp]
+            L.orc_unpack_qx_0.argtypes = [i32, vp, vp, vp]
+            L.orc_unpack_qx_0.restype = i32
             L.orc_block_sums.argtypes = [i32, vp, i64, i64, vp, i64, vp]
             L.orc_block_sums.restype = i32
             L.orc_mul_mat.argtypes = [i32, vp, i64, i64, vp, i64, vp, i32]
@@ -163,6 +166,14 @@ def unpack_q6_k(block: np.ndarray):
     d = np.zeros(1, np.uint16); sc = np.zeros(16, np.int8); q = np.zeros(256, np.uint8)
     lib().orc_unpack_q6_k(_p(block), _p(d), _p(sc), _p(q))
     return int(d[0]), sc, q
+
+
+def unpack_qx_0(t: int, block: np.ndarray):
+    """Q4_0 / Q5_0 block -> (d bits, 32 codes)."""
+    block = np.ascontiguousarray(block, dtype=np.uint8)
+    d = np.zeros(1, np.uint16); q = np.zeros(32, np.uint8)
+    _check(lib().orc_unpack_qx_0(t, _p(block), _p(d), _p(q)), "unpack_qx_0")
+    return int(d[0]), q
 
 
 def quantize_activations(wtype: int, x: np.ndarray) -> np.ndarray:

@@ -30,6 +30,9 @@
  *  - Q4_K: plain min-max encoder (per 32-sub-block range / 15, mins clamped to <= 0);
  *    super-scales d = fp16(max s / 63), dmin = fp16(max m / 63).
  *  - Q6_K: symmetric encoder, codes q' in [-32, 31] stored as q' + 32; d = fp16(max s/127).
+ *  - Q4_0 / Q5_0 (same table: 32 weights, fp16 d, w = d*(q - 8) / d*(q - 16), q 4 / 5 bits):
+ *    d = m / -8 (Q4_0) or m / -16 (Q5_0), m the block's value of largest magnitude with
+ *    its sign, so that m itself maps to q = 0; q = clamp(round(x / D) + 8 (16), 0, 15 (31)).
  *  - byte layout inside the blocks: the public GGUF on-disk layout (see the pack/unpack
  *    routines for the field order).
  *  - non-finite input, or a scale that overflows fp16, is rejected (status -5).
@@ -44,6 +47,8 @@
 #define ORC_Q4_K 2
 #define ORC_Q6_K 3
 #define ORC_Q8_K 4
+#define ORC_Q4_0 5
+#define ORC_Q5_0 6
 
 #define ORC_OK 0
 #define ORC_ERR_TYPE (-1)
@@ -120,7 +125,7 @@ void orc_fp16_to_fp32_array(const uint16_t* src, float* dst, int64_t n) {
 
 int64_t orc_block_elems(int type) {
     switch (type) {
-    case ORC_Q8_0: return 32;
+    case ORC_Q8_0: case ORC_Q4_0: case ORC_Q5_0: return 32;
     case ORC_Q4_K: case ORC_Q6_K: case ORC_Q8_K: return 256;
     default: return -1;
     }
@@ -135,6 +140,8 @@ int64_t orc_block_bytes(int type) {
     case ORC_Q4_K: return 2 + 2 + 12 + 128;
     case ORC_Q6_K: return 128 + 64 + 16 + 2;
     case ORC_Q8_K: return 4 + 256 + 2 * 16;
+    case ORC_Q4_0: return 2 + 16;
+    case ORC_Q5_0: return 2 + 4 + 16;
     default: return -1;
     }
 }
@@ -147,6 +154,7 @@ typedef struct { uint16_t d; int8_t q[32]; } q8_0_u;
 typedef struct { uint16_t d, dmin; uint8_t sc[8], mn[8]; uint8_t q[256]; } q4_k_u;  /* q in 0..15 */
 typedef struct { uint16_t d; int8_t sc[16]; uint8_t q[256]; } q6_k_u;                /* q in 0..63 */
 typedef struct { float d; int8_t q[256]; int16_t bsums[16]; } q8_k_u;
+typedef struct { uint16_t d; uint8_t q[32]; } qx_0_u;  /* Q4_0: q in 0..15; Q5_0: q in 0..31 */
 
 static float clampf(float v, float lo, float hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
@@ -387,6 +395,65 @@ static void deq_q6_k(const q6_k_u* b, float* y) {
 /* row-level quantize / dequantize                                                       */
 /* ------------------------------------------------------------------------------------ */
 
+/* ---- Q4_0 / Q5_0: 32 weights, w = D * (q - off), off = 8 (4-bit) or 16 (5-bit) ---- */
+
+static int quant_qx_0(const float* x, qx_0_u* b, int off) {
+    float m = 0.0f, amax = 0.0f;
+    for (int i = 0; i < 32; i++) {
+        if (!isfinite(x[i])) return ORC_ERR_RANGE;
+        float a = fabsf(x[i]);
+        if (a > amax) { amax = a; m = x[i]; }
+    }
+    float d = m / -(float)off;
+    b->d = orc_fp32_to_fp16(d);
+    if ((b->d & 0x7C00u) == 0x7C00u) return ORC_ERR_RANGE;
+    float D = orc_fp16_to_fp32(b->d);
+    for (int i = 0; i < 32; i++)
+        b->q[i] = (D == 0.0f) ? (uint8_t)off
+                              : (uint8_t)clampf(roundf(x[i] / D) + (float)off, 0.0f, (float)(2 * off - 1));
+    return ORC_OK;
+}
+
+/* Q4_0 bytes: d, then qs[16]: byte l holds q[l] (low nibble) and q[l + 16] (high nibble). */
+static void pack_q4_0(const qx_0_u* b, uint8_t* p) {
+    p[0] = (uint8_t)(b->d & 0xFF);
+    p[1] = (uint8_t)(b->d >> 8);
+    for (int l = 0; l < 16; l++) p[2 + l] = (uint8_t)((b->q[l] & 15) | ((b->q[l + 16] & 15) << 4));
+}
+
+static void unpack_q4_0(const uint8_t* p, qx_0_u* b) {
+    b->d = (uint16_t)(p[0] | (p[1] << 8));
+    for (int l = 0; l < 16; l++) {
+        b->q[l] = p[2 + l] & 15;
+        b->q[l + 16] = p[2 + l] >> 4;
+    }
+}
+
+/* Q5_0 bytes: d, then qh (32 bits, little endian: bit i = the fifth bit of q[i]), then
+ * qs[16] holding the low four bits as in Q4_0. */
+static void pack_q5_0(const qx_0_u* b, uint8_t* p) {
+    p[0] = (uint8_t)(b->d & 0xFF);
+    p[1] = (uint8_t)(b->d >> 8);
+    uint32_t qh = 0;
+    for (int i = 0; i < 32; i++) qh |= (uint32_t)((b->q[i] >> 4) & 1) << i;
+    for (int k = 0; k < 4; k++) p[2 + k] = (uint8_t)(qh >> (8 * k));
+    for (int l = 0; l < 16; l++) p[6 + l] = (uint8_t)((b->q[l] & 15) | ((b->q[l + 16] & 15) << 4));
+}
+
+static void unpack_q5_0(const uint8_t* p, qx_0_u* b) {
+    b->d = (uint16_t)(p[0] | (p[1] << 8));
+    uint32_t qh = (uint32_t)p[2] | ((uint32_t)p[3] << 8) | ((uint32_t)p[4] << 16) | ((uint32_t)p[5] << 24);
+    for (int l = 0; l < 16; l++) {
+        b->q[l] = (uint8_t)((p[6 + l] & 15) | (((qh >> l) & 1) << 4));
+        b->q[l + 16] = (uint8_t)((p[6 + l] >> 4) | (((qh >> (l + 16)) & 1) << 4));
+    }
+}
+
+static void deq_qx_0(const qx_0_u* b, int off, float* y) {
+    float D = orc_fp16_to_fp32(b->d);
+    for (int i = 0; i < 32; i++) y[i] = D * (float)((int)b->q[i] - off);
+}
+
 static int check_shape(int type, int64_t n_rows, int64_t n_per_row) {
     int64_t be = orc_block_elems(type);
     if (be < 0) return ORC_ERR_TYPE;
@@ -407,6 +474,8 @@ int orc_quantize(int type, const float* src, uint8_t* dst, int64_t n_rows, int64
         case ORC_Q8_K: { q8_k_u b; if ((st = quant_q8_k(x, &b))) return st; pack_q8_k(&b, p); break; }
         case ORC_Q4_K: { q4_k_u b; if ((st = quant_q4_k(x, &b))) return st; pack_q4_k(&b, p); break; }
         case ORC_Q6_K: { q6_k_u b; if ((st = quant_q6_k(x, &b))) return st; pack_q6_k(&b, p); break; }
+        case ORC_Q4_0: { qx_0_u b; if ((st = quant_qx_0(x, &b, 8))) return st; pack_q4_0(&b, p); break; }
+        case ORC_Q5_0: { qx_0_u b; if ((st = quant_qx_0(x, &b, 16))) return st; pack_q5_0(&b, p); break; }
         }
     }
     return ORC_OK;
@@ -425,6 +494,8 @@ int orc_dequantize(int type, const uint8_t* src, float* dst, int64_t n_rows, int
         case ORC_Q8_K: { q8_k_u b; unpack_q8_k(p, &b); deq_q8_k(&b, y); break; }
         case ORC_Q4_K: { q4_k_u b; unpack_q4_k(p, &b); deq_q4_k(&b, y); break; }
         case ORC_Q6_K: { q6_k_u b; unpack_q6_k(p, &b); deq_q6_k(&b, y); break; }
+        case ORC_Q4_0: { qx_0_u b; unpack_q4_0(p, &b); deq_qx_0(&b, 8, y); break; }
+        case ORC_Q5_0: { qx_0_u b; unpack_q5_0(p, &b); deq_qx_0(&b, 16, y); break; }
         }
     }
     return ORC_OK;
@@ -434,6 +505,15 @@ int orc_dequantize(int type, const uint8_t* src, float* dst, int64_t n_rows, int
 int orc_unpack_q4_k(const uint8_t* p, uint16_t* d, uint16_t* dmin, uint8_t* sc, uint8_t* mn, uint8_t* q) {
     q4_k_u b; unpack_q4_k(p, &b);
     *d = b.d; *dmin = b.dmin; memcpy(sc, b.sc, 8); memcpy(mn, b.mn, 8); memcpy(q, b.q, 256);
+    return ORC_OK;
+}
+
+int orc_unpack_qx_0(int type, const uint8_t* p, uint16_t* d, uint8_t* q) {
+    qx_0_u b;
+    if (type == ORC_Q4_0) unpack_q4_0(p, &b);
+    else if (type == ORC_Q5_0) unpack_q5_0(p, &b);
+    else return ORC_ERR_TYPE;
+    *d = b.d; memcpy(q, b.q, 32);
     return ORC_OK;
 }
 
@@ -447,10 +527,10 @@ int orc_unpack_q6_k(const uint8_t* p, uint16_t* d, int8_t* sc, uint8_t* q) {
 /* integer block sums and the product                                                    */
 /* ------------------------------------------------------------------------------------ */
 
-/* vec_dot_type of a weight format: Q8_0 for Q8_0, Q8_K for the K-quants. */
+/* vec_dot_type of a weight format: Q8_0 for Q8_0, Q4_0 and Q5_0, Q8_K for the K-quants. */
 static int vec_dot_type(int wtype) {
     switch (wtype) {
-    case ORC_Q8_0: return ORC_Q8_0;
+    case ORC_Q8_0: case ORC_Q4_0: case ORC_Q5_0: return ORC_Q8_0;
     case ORC_Q4_K: case ORC_Q6_K: return ORC_Q8_K;
     default: return -1;
     }
@@ -462,7 +542,8 @@ int orc_vec_dot_type(int wtype) { return vec_dot_type(wtype); }
  *  Q8_0: I  = sum_i qw_i * qx_i                                       -> s[0] = I
  *  Q4_K: A  = sum_j sc_j * sum_{i in j} q_i * qx_i                    -> s[0] = A
  *        Bm = sum_j mn_j * (bsum_{2j} + bsum_{2j+1})                  -> s[1] = Bm
- *  Q6_K: C  = sum_j sc_j * sum_{i in j} (q_i - 32) * qx_i             -> s[0] = C */
+ *  Q6_K: C  = sum_j sc_j * sum_{i in j} (q_i - 32) * qx_i             -> s[0] = C
+ *  Q4_0 / Q5_0: I = sum_i (q_i - 8 / 16) * qx_i                       -> s[0] = I */
 static void block_sums(int wtype, const uint8_t* wp, const uint8_t* xp, int32_t s[2]) {
     s[0] = 0; s[1] = 0;
     if (wtype == ORC_Q8_0) {
@@ -489,13 +570,21 @@ static void block_sums(int wtype, const uint8_t* wp, const uint8_t* xp, int32_t 
             C += (int32_t)w.sc[j] * dot;
         }
         s[0] = C;
+    } else if (wtype == ORC_Q4_0 || wtype == ORC_Q5_0) {
+        qx_0_u w; q8_0_u x;
+        int off = wtype == ORC_Q4_0 ? 8 : 16;
+        if (wtype == ORC_Q4_0) unpack_q4_0(wp, &w); else unpack_q5_0(wp, &w);
+        unpack_q8_0(xp, &x);
+        int32_t I = 0;
+        for (int i = 0; i < 32; i++) I += ((int32_t)w.q[i] - off) * (int32_t)x.q[i];
+        s[0] = I;
     }
 }
 
 /* fp64 contribution of one block pair:
- *  Q8_0: D_w * D_x * I;   Q4_K: D * d_x * A - Dm * d_x * Bm;   Q6_K: D * d_x * C. */
+ *  Q8_0, Q4_0, Q5_0: D_w * D_x * I;   Q4_K: D * d_x * A - Dm * d_x * Bm;   Q6_K: D * d_x * C. */
 static double block_value(int wtype, const uint8_t* wp, const uint8_t* xp, const int32_t s[2]) {
-    if (wtype == ORC_Q8_0) {
+    if (wtype == ORC_Q8_0 || wtype == ORC_Q4_0 || wtype == ORC_Q5_0) {
         double Dw = orc_fp16_to_fp32((uint16_t)(wp[0] | (wp[1] << 8)));
         double Dx = orc_fp16_to_fp32((uint16_t)(xp[0] | (xp[1] << 8)));
         return Dw * Dx * (double)s[0];

@@ -5,7 +5,8 @@ following the in-block layout the library and the oracle both use (the public GG
 layout).  This script does not call the oracle or the library; the tests decode the bytes
 with the oracle and compare against the format formulas of "The GGML ecosystem, and
 where synapse fits", section 5 (Q8_0: w = d*q; Q4_K: w = d*sc*q - dmin*m;
-Q6_K: w = d*sc*(q - 32); Q8_K: w = d*q with bsums = sums of 16 codes).
+Q6_K: w = d*sc*(q - 32); Q8_K: w = d*q with bsums = sums of 16 codes; Q4_0: w = d*(q - 8);
+Q5_0: w = d*(q - 16) with the fifth bits in a 32-bit qh).
 
 Run: python tests/golden/make_hand_blocks.py   (rewrites hand_blocks.txt beside it)
 """
@@ -84,13 +85,37 @@ def q8_k_block():
     return bytes(buf), dict(d=d, q=q, bsums=bsums)
 
 
+def q4_0_block():
+    d = 0x3A00  # fp16 0.75
+    q = [(3 * i + 1) % 16 for i in range(32)]
+    buf = bytearray(18)
+    buf[0:2] = struct.pack("<H", d)
+    for i in range(32):
+        l, high = i % 16, i // 16              # weights l (low nibble) and l + 16 (high)
+        bits_set(buf, 8 * (2 + l) + 4 * high, q[i], 4)
+    return bytes(buf), dict(d=d, q=q)
+
+
+def q5_0_block():
+    d = 0x3100  # fp16 0.15625
+    q = [(7 * i + 5) % 32 for i in range(32)]
+    buf = bytearray(22)
+    buf[0:2] = struct.pack("<H", d)
+    for i in range(32):
+        bits_set(buf, 8 * 2 + i, q[i] >> 4, 1)  # qh: bit i of a little-endian 32-bit word
+        l, high = i % 16, i // 16
+        bits_set(buf, 8 * (6 + l) + 4 * high, q[i] & 15, 4)
+    return bytes(buf), dict(d=d, q=q)
+
+
 def main():
     out = os.path.join(os.path.dirname(os.path.abspath(__file__)), "hand_blocks.txt")
     lines = ["# Hand-made blocks (inputs) written by make_hand_blocks.py; fields then hex bytes.",
              "# Formulas checked by the tests: format table of 'The GGML ecosystem, and where",
              "# synapse fits', section 5."]
     for name, (raw, f) in [("Q8_0", q8_0_block()), ("Q4_K", q4_k_block()),
-                           ("Q6_K", q6_k_block()), ("Q8_K", q8_k_block())]:
+                           ("Q6_K", q6_k_block()), ("Q8_K", q8_k_block()),
+                           ("Q4_0", q4_0_block()), ("Q5_0", q5_0_block())]:
         lines.append(f"[{name}]")
         for k, v in f.items():
             lines.append(f"{k} = {' '.join(map(str, v)) if isinstance(v, list) else v}")

@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 import oracle
-from oracle import Q8_0, Q4_K, Q6_K, Q8_K
+from oracle import Q8_0, Q4_K, Q6_K, Q8_K, Q4_0, Q5_0
 from conftest import GOLDEN, read_fixture
 from gguf_block_quantized_gb300 import synth, workloads
 
@@ -77,8 +77,10 @@ def test_fp16_to_fp32_exact_all_values():
 def test_block_sizes_match_format_table():
     # "The GGML ecosystem, and where synapse fits", section 5, format table.
     L = oracle.lib()
-    assert [L.orc_block_elems(t) for t in (Q8_0, Q4_K, Q6_K, Q8_K)] == [32, 256, 256, 256]
-    assert [L.orc_block_bytes(t) for t in (Q8_0, Q4_K, Q6_K, Q8_K)] == [34, 144, 210, 292]
+    assert [L.orc_block_elems(t) for t in (Q8_0, Q4_K, Q6_K, Q8_K, Q4_0, Q5_0)] == [32, 256, 256, 256, 32, 32]
+    assert [L.orc_block_bytes(t) for t in (Q8_0, Q4_K, Q6_K, Q8_K, Q4_0, Q5_0)] == [34, 144, 210, 292, 18, 22]
+    # Q4_0: fp16 d + 32 x 4 bits; Q5_0: fp16 d + 32-bit qh + 32 x 4 bits
+    assert 2 + 32 * 4 // 8 == 18 and 2 + 4 + 32 * 4 // 8 == 22
     # Q6_K: 256 x 4 bits + 256 x 2 bits + 16 int8 scales + fp16 d
     assert 256 * 4 // 8 + 256 * 2 // 8 + 16 + 2 == 210
 
@@ -88,6 +90,8 @@ def test_bits_per_weight():
     bpw = {t: 8 * oracle.BLOCK_BYTES[t] / oracle.BLOCK_ELEMS[t] for t in (Q8_0, Q4_K, Q6_K, Q8_K)}
     assert bpw[Q4_K] == 4.5 and bpw[Q8_0] == 8.5
     assert bpw[Q6_K] == 6.5625 and bpw[Q8_K] == 9.125
+    # the legacy 32-weight formats span "4.5 - 8.5" bpw ("llama.cpp and GGUF", format table)
+    assert 8 * 18 / 32 == 4.5 and 8 * 22 / 32 == 5.5
 
 
 def test_llama8b_q4_k_m_size_in_published_range():
@@ -161,6 +165,18 @@ def test_hand_q8_k_dequant_and_bsums():
     assert np.array_equal(got.astype(np.float64), d * q)
     bs = np.frombuffer(raw[260:292].tobytes(), dtype="<i2")
     assert list(bs) == list(_ints(f["bsums"])) == [int(q[16 * k:16 * k + 16].sum()) for k in range(16)]
+
+
+@pytest.mark.parametrize("t,off", [(Q4_0, 8), (Q5_0, 16)])
+def test_hand_qx_0_dequant_and_fields(t, off):
+    name = oracle.NAMES[t]
+    f = HB[name]
+    d, q = f16(int(f["d"])), _ints(f["q"])
+    raw = _raw(name)
+    gd, gq = oracle.unpack_qx_0(t, raw)
+    assert gd == int(f["d"]) and list(gq) == list(q)
+    got = oracle.dequantize(t, raw, 32)[0]
+    assert np.array_equal(got.astype(np.float64), d * (q - off))
 
 
 # ----------------------------------------------------------------------------------------
@@ -306,13 +322,43 @@ def test_q6_k_error_bound():
                 assert 0 <= int(sc[j]) <= 127
 
 
-@pytest.mark.parametrize("t", [Q8_0, Q8_K])
+@pytest.mark.parametrize("t,off", [(Q4_0, 8), (Q5_0, 16)])
+def test_qx_0_error_bound_and_extreme(t, off):
+    """w = d*(q - off) (format table): with d = m/-off for the block's largest-magnitude value
+    m, every weight is within D/2 of its input, except inputs above (off - 1/2)*|D| on the
+    side opposite to m, which clip to q = 2*off - 1 (within |D|); m itself is reproduced up
+    to the fp16 rounding of d."""
+    x = _test_inputs(512)
+    y = oracle.dequantize(t, oracle.quantize(t, x), 512)
+    b = oracle.quantize(t, x).reshape(x.shape[0], -1, oracle.BLOCK_BYTES[t])
+    for r in range(x.shape[0]):
+        for k in range(512 // 32):
+            xs, ys = x[r, 32 * k:32 * k + 32].astype(np.float64), y[r, 32 * k:32 * k + 32].astype(np.float64)
+            D = f16(int(b[r, k, 0]) | int(b[r, k, 1]) << 8)
+            i = int(np.argmax(np.abs(xs)))
+            m = xs[i]
+            if m == 0:
+                assert np.all(ys == 0)
+                continue
+            # fp16 rounding of d = m/-off: half an ulp, 2^-11 relative or 2^-25 absolute
+            # (subnormal); m is reproduced up to off times that
+            err_d = max(2 ** -11 * abs(m) / off, 2 ** -25)
+            slack = 1e-6 * np.abs(xs).max() + 1e-30
+            assert abs(ys[i] - m) <= off * err_d + slack
+            u = xs / D  # in [-off, off] up to the rounding of D
+            clip = u > off - 0.5
+            assert np.all(np.abs(xs - ys)[~clip] <= abs(D) / 2 + off * err_d + slack)
+            assert np.all(np.abs(xs - ys)[clip] <= abs(D) + off * err_d + slack)
+
+
+@pytest.mark.parametrize("t", [Q8_0, Q8_K, Q4_0, Q5_0])
 def test_requantize_is_a_fixed_point(t):
     """quantize(dequantize(quantize(x))) == quantize(x), byte for byte.
 
     Holds exactly for the symmetric 8-bit formats: the largest code is +-127, so the
-    re-derived scale is 127*D/127 = D and every code divides back exactly.  (The K-quant
-    encoders are not idempotent on outlier blocks, so they are pinned by their bounds.)"""
+    re-derived scale is 127*D/127 = D and every code divides back exactly; likewise for
+    Q4_0/Q5_0, whose largest-magnitude value dequantizes to -off*D.  (The K-quant encoders
+    are not idempotent on outlier blocks, so they are pinned by their bounds.)"""
     x = _test_inputs(512)
     b1 = oracle.quantize(t, x)
     b2 = oracle.quantize(t, oracle.dequantize(t, b1, 512))
@@ -320,7 +366,7 @@ def test_requantize_is_a_fixed_point(t):
 
 
 def test_range_errors():
-    for t in (Q8_0, Q4_K, Q6_K, Q8_K):
+    for t in (Q8_0, Q4_K, Q6_K, Q8_K, Q4_0, Q5_0):
         n = oracle.BLOCK_ELEMS[t]
         for bad in (np.nan, np.inf, -np.inf):
             x = np.zeros(n, np.float32); x[3] = bad
@@ -338,7 +384,7 @@ def test_range_errors():
 # integer block sums and the product: fp64 brute force on dequantized blocks
 # ----------------------------------------------------------------------------------------
 
-@pytest.mark.parametrize("t", [Q8_0, Q4_K, Q6_K])
+@pytest.mark.parametrize("t", [Q8_0, Q4_K, Q6_K, Q4_0, Q5_0])
 def test_block_sums_equal_dequantized_dot(t):
     """'Products: weights against quantized activations': the integer block dot scaled by
     the float block scales equals the fp64 dot of the two dequantized blocks."""
@@ -359,7 +405,7 @@ def test_block_sums_equal_dequantized_dot(t):
                 brute = float(np.dot(wd[o, k * be:(k + 1) * be], xd[tt, k * be:(k + 1) * be]))
                 wblk = W[o, k * wb:(k + 1) * wb]
                 xblk = Xq[tt, k * xb:(k + 1) * xb]
-                if t == Q8_0:
+                if t in (Q8_0, Q4_0, Q5_0):
                     v = f16(int(wblk[0]) | int(wblk[1]) << 8) * f16(int(xblk[0]) | int(xblk[1]) << 8) * int(S[tt, o, k, 0])
                 else:
                     dx = float(xblk[0:4].copy().view(np.float32)[0])
@@ -375,7 +421,7 @@ def test_block_sums_equal_dequantized_dot(t):
                 assert abs(v - brute) <= 2 ** -23 * mag + 1e-300, (tt, o, k)
 
 
-@pytest.mark.parametrize("t", [Q8_0, Q4_K, Q6_K])
+@pytest.mark.parametrize("t", [Q8_0, Q4_K, Q6_K, Q4_0, Q5_0])
 def test_mul_mat_equals_fp64_brute_force(t):
     n_out, n_in, n_tok = 7, 768, 4
     W = oracle.quantize(t, synth.normal(41, (n_out, n_in), 0.02))
@@ -401,7 +447,7 @@ def test_mul_mat_equals_fp64_brute_force(t):
     assert np.all(np.abs(Y - exact) <= bound * (1 + 1e-6) + 1e-6 * np.abs(exact))
 
 
-@pytest.mark.parametrize("t", [Q8_0, Q4_K, Q6_K])
+@pytest.mark.parametrize("t", [Q8_0, Q4_K, Q6_K, Q4_0, Q5_0])
 def test_mul_mat_orientation_example(t):
     """ggml_mul_mat(A, B^T) = C^T from the examples/simple page, with exact integers.
 
@@ -430,6 +476,18 @@ def test_mul_mat_orientation_example(t):
         W[:, 12:16] = 0x01                 # sc4..sc7 = 1
         W[:, 16] = A[:, 0].astype(np.uint8)  # element 0 of sub-block 0 (low nibble)
         W[:, 17] = A[:, 1].astype(np.uint8)  # element 1
+    elif t in (Q4_0, Q5_0):
+        off = 8 if t == Q4_0 else 16
+        W = np.zeros((4, oracle.BLOCK_BYTES[t]), np.uint8)
+        W[:, 0:2] = [0x00, 0xBC]                       # d = -1: w = off - q covers 8 in Q4_0
+        qs = 2 if t == Q4_0 else 6                     # first byte of the low-nibble codes
+        codes = np.full((4, 32), off, np.int64)        # q = off: weight 0 elsewhere
+        codes[:, :2] = off - A
+        for i in range(32):
+            l, hi = i % 16, i // 16
+            W[:, qs + l] |= ((codes[:, i] & 15) << (4 * hi)).astype(np.uint8)
+            if t == Q5_0:
+                W[:, 2 + i // 8] |= (((codes[:, i] >> 4) & 1) << (i % 8)).astype(np.uint8)
     else:
         W = np.zeros((4, 210), np.uint8)
         W[:, 0] = A[:, 0].astype(np.uint8)   # low 4 bits of weight 0 (low nibble of ql[0])
