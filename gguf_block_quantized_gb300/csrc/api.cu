@@ -13,6 +13,7 @@
 #include <mutex>
 #include <utility>
 
+#include "common.cuh"
 #include "kernels.h"
 #include "syn.h"
 
@@ -77,14 +78,15 @@ int device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-bool known_type(int t) {
-    return t == SYN_TYPE_Q8_0 || t == SYN_TYPE_Q4_K || t == SYN_TYPE_Q6_K || t == SYN_TYPE_Q8_K;
-}
+bool known_type(int t) { return t >= SYN_TYPE_Q8_0 && t <= SYN_TYPE_Q5_0; }
+// weight formats of mul_mat (Q8_K is an activation format only)
+bool is_weight(int t) { return known_type(t) && t != SYN_TYPE_Q8_K; }
+// the vec_dot_type the activations are converted to: Q8_0 for the 32-weight formats,
+// Q8_K for the K-quants ("Products: weights against quantized activations")
+int vec_dot(int t) { return (t == SYN_TYPE_Q4_K || t == SYN_TYPE_Q6_K) ? SYN_TYPE_Q8_K : SYN_TYPE_Q8_0; }
 
-int64_t elems(int t) { return t == SYN_TYPE_Q8_0 ? 32 : 256; }
-int64_t bytes_of(int t) {
-    return t == SYN_TYPE_Q8_0 ? 34 : t == SYN_TYPE_Q4_K ? 144 : t == SYN_TYPE_Q6_K ? 210 : 292;
-}
+int64_t elems(int t) { return syn::block_elems(t); }
+int64_t bytes_of(int t) { return syn::block_bytes(t); }
 
 int check_cuda(cudaError_t e) { return e == cudaSuccess ? SYN_OK : SYN_ERR_CUDA; }
 
@@ -200,8 +202,8 @@ int syn_dequantize(int type, const void* src, float* dst, int64_t n_rows, int64_
 
 int syn_quantize_activations(int wtype, const float* X, int64_t n_tok, int64_t n_in, int8_t* qs, float* d,
                              int16_t* bsums, syn_stream_t stream) {
-    if (wtype != SYN_TYPE_Q8_0 && wtype != SYN_TYPE_Q4_K && wtype != SYN_TYPE_Q6_K) return SYN_ERR_TYPE;
-    const int xt = wtype == SYN_TYPE_Q8_0 ? SYN_TYPE_Q8_0 : SYN_TYPE_Q8_K;
+    if (!is_weight(wtype)) return SYN_ERR_TYPE;
+    const int xt = vec_dot(wtype);
     if (n_tok < 0 || n_in <= 0 || n_in % elems(xt) || n_tok * n_in > kMaxElems) return SYN_ERR_SHAPE;
     if (n_tok == 0) return SYN_OK;
     if (!X || !qs || !d || (xt == SYN_TYPE_Q8_K && !bsums)) return SYN_ERR_NULL;
@@ -244,7 +246,7 @@ int syn_release(void) {
 
 int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in, const float* X, int64_t n_tok, float* Y,
                 syn_stream_t stream) {
-    if (type != SYN_TYPE_Q8_0 && type != SYN_TYPE_Q4_K && type != SYN_TYPE_Q6_K) return SYN_ERR_TYPE;
+    if (!is_weight(type)) return SYN_ERR_TYPE;
     if (n_out <= 0 || n_in <= 0 || n_tok < 0 || n_in % elems(type) || n_out * n_in > kMaxElems ||
         n_tok * n_in > kMaxElems || n_tok * n_out > kMaxElems || n_out > (int64_t(1) << 31))
         return SYN_ERR_SHAPE;
@@ -267,7 +269,7 @@ int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in, const floa
     void* ws;
     rc = workspace_for(s, prefill_ws_bytes(n_in, n_tok), &ws);
     if (rc) return rc;
-    const int xt = type == SYN_TYPE_Q8_0 ? SYN_TYPE_Q8_0 : SYN_TYPE_Q8_K;
+    const int xt = vec_dot(type);
     if (syn::gemm_needs_zero(n_out, n_in, n_tok, st->sms) &&
         cudaMemsetAsync(Y, 0, (size_t)n_tok * n_out * sizeof(float), s) != cudaSuccess)
         return SYN_ERR_CUDA;
@@ -285,7 +287,7 @@ int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_strea
     if (!descs) return SYN_ERR_NULL;
     for (int i = 0; i < n; i++) {
         const syn_mat_desc& d = descs[i];
-        if (d.type != SYN_TYPE_Q8_0 && d.type != SYN_TYPE_Q4_K && d.type != SYN_TYPE_Q6_K) return SYN_ERR_TYPE;
+        if (!is_weight(d.type)) return SYN_ERR_TYPE;
         if (d.n_out <= 0 || d.n_in <= 0 || n_tok < 0 || d.n_in % elems(d.type) || d.n_out * d.n_in > kMaxElems ||
             n_tok * d.n_in > kMaxElems || n_tok * d.n_out > kMaxElems || d.n_out > (int64_t(1) << 31))
             return SYN_ERR_SHAPE;
@@ -339,7 +341,7 @@ int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_strea
 
 int syn_block_sums(int type, const void* W, int64_t n_out, int64_t n_in, const void* Xq, int64_t n_tok, int32_t* S,
                    syn_stream_t stream) {
-    if (type != SYN_TYPE_Q8_0 && type != SYN_TYPE_Q4_K && type != SYN_TYPE_Q6_K) return SYN_ERR_TYPE;
+    if (!is_weight(type)) return SYN_ERR_TYPE;
     if (n_out <= 0 || n_in <= 0 || n_tok < 0 || n_in % elems(type) || n_out * n_in > kMaxElems ||
         n_tok * n_out * (n_in / elems(type)) > kMaxElems)
         return SYN_ERR_SHAPE;

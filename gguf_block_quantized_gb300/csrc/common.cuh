@@ -6,6 +6,8 @@
 //   Q4_K [d f16][dmin f16][scales 12 B][q nibbles 128 B]              144 B
 //   Q6_K [ql 128 B][qh 64 B][scales int8 x16][d f16]                   210 B
 //   Q8_K [d f32][q int8 x256][bsums int16 x16]                         292 B
+//   Q4_0 [d f16][qs 16 B: q[l] low nibble, q[l+16] high nibble]       18 B
+//   Q5_0 [d f16][qh u32: bit i = fifth bit of q[i]][qs 16 B as Q4_0]   22 B
 #pragma once
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -14,6 +16,8 @@
 #define SYN_Q4_K 2
 #define SYN_Q6_K 3
 #define SYN_Q8_K 4
+#define SYN_Q4_0 5
+#define SYN_Q5_0 6
 
 // Device-side error codes written into the library's per-device error word.
 #define SYN_DEVERR_TIMEOUT 1
@@ -30,10 +34,14 @@ template <> struct Fmt<SYN_Q8_0> { static constexpr int elems = 32, bytes = 34; 
 template <> struct Fmt<SYN_Q4_K> { static constexpr int elems = 256, bytes = 144; };
 template <> struct Fmt<SYN_Q6_K> { static constexpr int elems = 256, bytes = 210; };
 template <> struct Fmt<SYN_Q8_K> { static constexpr int elems = 256, bytes = 292; };
+template <> struct Fmt<SYN_Q4_0> { static constexpr int elems = 32, bytes = 18; };
+template <> struct Fmt<SYN_Q5_0> { static constexpr int elems = 32, bytes = 22; };
 
-__host__ __device__ inline int block_elems(int t) { return t == SYN_Q8_0 ? 32 : 256; }
+// 32-weight formats (vec_dot_type Q8_0)
+__host__ __device__ inline bool small_block(int t) { return t == SYN_Q8_0 || t == SYN_Q4_0 || t == SYN_Q5_0; }
+__host__ __device__ inline int block_elems(int t) { return small_block(t) ? 32 : 256; }
 __host__ __device__ inline int block_bytes(int t) {
-    return t == SYN_Q8_0 ? 34 : t == SYN_Q4_K ? 144 : t == SYN_Q6_K ? 210 : 292;
+    return t == SYN_Q8_0 ? 34 : t == SYN_Q4_K ? 144 : t == SYN_Q6_K ? 210 : t == SYN_Q8_K ? 292 : t == SYN_Q4_0 ? 18 : 22;
 }
 
 // ---------------------------------------------------------------------------------------

@@ -78,6 +78,12 @@ template <> struct GemmFmt<SYN_Q4_K> : GemmDepth<SYN_GEMM_Q4K_RAW, SYN_GEMM_Q4K_
 template <> struct GemmFmt<SYN_Q6_K> : GemmDepth<2, 3, 3> {
     static constexpr int BB = 210, SB_BYTES = 210, BOX = 240, ESIZE = 1, RAW_ROW = 240;
 };
+template <> struct GemmFmt<SYN_Q4_0> : GemmDepth<2, 3, 4> {
+    static constexpr int BB = 18, SB_BYTES = 144, BOX = 144, ESIZE = 1, RAW_ROW = 160;
+};
+template <> struct GemmFmt<SYN_Q5_0> : GemmDepth<2, 3, 3> {
+    static constexpr int BB = 22, SB_BYTES = 176, BOX = 176, ESIZE = 1, RAW_ROW = 192;
+};
 template <> struct GemmFmt<SYN_Q8_0> : GemmDepth<2, 3, 3> {
     static constexpr int BB = 34, SB_BYTES = 272, BOX = 272, ESIZE = 2, RAW_ROW = 288;
 };
@@ -313,6 +319,30 @@ __device__ __forceinline__ void deq32_q8_0(const uint8_t* blk, uint32_t out[16])
     }
 }
 
+// Q4_0 / Q5_0 (OFF = 8 / 16): one 18- / 22-byte block (32 k), codes q[l] / q[l + 16] in the
+// low / high nibble of byte l (Q5_0: fifth bits in a 32-bit word before them); w = D*(q - OFF)
+// with D stored in fp16: one rounding.
+template <int OFF>
+__device__ __forceinline__ void deq32_qx_0(const uint8_t* blk, uint32_t out[16]) {
+    const __half2 D = u32_as_h2(__byte_perm(*reinterpret_cast<const uint16_t*>(blk), 0, 0x1010));
+    const __half2 kOff = __float2half2_rn(1024.0f + OFF);
+    uint32_t w[5];
+    if (OFF == 8) lds_words_any<4>(blk + 2, w + 1);
+    else lds_words_any<5>(blk + 2, w);
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        uint32_t lo = w[1 + i] & 0x0F0F0F0Fu, hi = (w[1 + i] >> 4) & 0x0F0F0F0Fu;
+        if (OFF == 16) {
+            lo |= ((((w[0] >> (4 * i)) & 15u) * 0x00204081u) & 0x01010101u) << 4;
+            hi |= ((((w[0] >> (16 + 4 * i)) & 15u) * 0x00204081u) & 0x01010101u) << 4;
+        }
+        out[2 * i] = h2_as_u32(__hmul2(__hsub2(bytes01_h2(lo), kOff), D));
+        out[2 * i + 1] = h2_as_u32(__hmul2(__hsub2(bytes23_h2(lo), kOff), D));
+        out[8 + 2 * i] = h2_as_u32(__hmul2(__hsub2(bytes01_h2(hi), kOff), D));
+        out[8 + 2 * i + 1] = h2_as_u32(__hmul2(__hsub2(bytes23_h2(hi), kOff), D));
+    }
+}
+
 // ---------------------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------------------
@@ -424,7 +454,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     continue;
                 }
                 // raw weight slice of 128 rows: per row one window-aligned bulk copy
-                const int nblk_sb = (T == SYN_Q8_0) ? min(8, p.nb - ss * 8) : 1;
+                const int nblk_sb = small_block(T) ? min(8, p.nb - ss * 8) : 1;
                 const int64_t len = (int64_t)nblk_sb * F::BB;
                 uint32_t my_tx = 0;
                 int64_t a0[4];
@@ -575,7 +605,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     if (row_ok && kglob < p.n_in) {
                         if (T == SYN_Q4_K) deq32_q4_k(row, k4, h, p4, k4 >> 1, out);
                         else if (T == SYN_Q6_K) deq32_q6_k(row, k4, h, p6, k4 >> 1, out);
-                        else deq32_q8_0(row + (2 * k4 + h) * 34, out);
+                        else if (T == SYN_Q8_0) deq32_q8_0(row + (2 * k4 + h) * 34, out);
+                        else deq32_qx_0<T == SYN_Q4_0 ? 8 : 16>(row + (2 * k4 + h) * F::BB, out);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 16; i++) out[i] = 0u;
@@ -700,13 +731,16 @@ constexpr size_t gemm_smem_bytes() {
     return 1024 /* alignment slack */ + GemmSmem<T>::BARS + 256 /* barriers, TMEM slot, abort flag */;
 }
 static_assert(gemm_smem_bytes<SYN_Q4_K>() <= 232448 && gemm_smem_bytes<SYN_Q6_K>() <= 232448 &&
-                  gemm_smem_bytes<SYN_Q8_0>() <= 232448,
+                  gemm_smem_bytes<SYN_Q8_0>() <= 232448 && gemm_smem_bytes<SYN_Q4_0>() <= 232448 &&
+                  gemm_smem_bytes<SYN_Q5_0>() <= 232448,
               "shared memory per CTA exceeds 227 KB");
 template <int T>
 constexpr bool gemm_bars_fit() {
     return 8 * (2 * GemmFmt<T>::RAW_STAGES + 2 * GemmFmt<T>::A_STAGES + 2 * GemmFmt<T>::B_STAGES + 4) + 16 <= 256;
 }
-static_assert(gemm_bars_fit<SYN_Q4_K>() && gemm_bars_fit<SYN_Q6_K>() && gemm_bars_fit<SYN_Q8_0>(), "barrier area");
+static_assert(gemm_bars_fit<SYN_Q4_K>() && gemm_bars_fit<SYN_Q6_K>() && gemm_bars_fit<SYN_Q8_0>() &&
+                  gemm_bars_fit<SYN_Q4_0>() && gemm_bars_fit<SYN_Q5_0>(),
+              "barrier area");
 
 #ifndef SYN_GEMM_SPLIT_PENALTY
 #define SYN_GEMM_SPLIT_PENALTY 0.15
@@ -808,6 +842,8 @@ cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, co
     case SYN_Q4_K: box_bytes = GemmFmt<SYN_Q4_K>::BOX; esize = GemmFmt<SYN_Q4_K>::ESIZE; raw_row = GemmFmt<SYN_Q4_K>::RAW_ROW; break;
     case SYN_Q6_K: box_bytes = GemmFmt<SYN_Q6_K>::BOX; esize = GemmFmt<SYN_Q6_K>::ESIZE; raw_row = GemmFmt<SYN_Q6_K>::RAW_ROW; break;
     case SYN_Q8_0: box_bytes = GemmFmt<SYN_Q8_0>::BOX; esize = GemmFmt<SYN_Q8_0>::ESIZE; raw_row = GemmFmt<SYN_Q8_0>::RAW_ROW; break;
+    case SYN_Q4_0: box_bytes = GemmFmt<SYN_Q4_0>::BOX; esize = GemmFmt<SYN_Q4_0>::ESIZE; raw_row = GemmFmt<SYN_Q4_0>::RAW_ROW; break;
+    case SYN_Q5_0: box_bytes = GemmFmt<SYN_Q5_0>::BOX; esize = GemmFmt<SYN_Q5_0>::ESIZE; raw_row = GemmFmt<SYN_Q5_0>::RAW_ROW; break;
     default: return cudaErrorInvalidValue;
     }
     CUtensorMap wmap = map;  // placeholder when unused
@@ -842,6 +878,8 @@ cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, co
     case SYN_Q4_K: return run_gemm<SYN_Q4_K>(p, map, wmap, ymap, sms, s);
     case SYN_Q6_K: return run_gemm<SYN_Q6_K>(p, map, wmap, ymap, sms, s);
     case SYN_Q8_0: return run_gemm<SYN_Q8_0>(p, map, wmap, ymap, sms, s);
+    case SYN_Q4_0: return run_gemm<SYN_Q4_0>(p, map, wmap, ymap, sms, s);
+    case SYN_Q5_0: return run_gemm<SYN_Q5_0>(p, map, wmap, ymap, sms, s);
     default: return cudaErrorInvalidValue;
     }
 }

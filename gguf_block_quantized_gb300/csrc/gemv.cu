@@ -116,6 +116,14 @@ __device__ __forceinline__ float group_sum(float v, int lg) {
 __device__ __forceinline__ int k_chunk(int B, int c) { return 256 * B + 16 * (c ^ (B & 7) ^ ((c >> 3) << 2)); }
 __device__ __forceinline__ int q8_chunk(int B, int c) { return 32 * B + 16 * (c ^ ((B >> 2) & 1)); }
 
+// Activation sums per token, in int16 elements (the per-token stride): the 16-sums for the
+// K-quants (n_in/16 of them), one code sum per 32-block for Q4_0 / Q5_0 (their codes carry
+// an offset), padded to 8 so that every token's sums start on 16 bytes; none for Q8_0.
+__host__ __device__ __forceinline__ int64_t sum_stride(int type, int64_t n_in) {
+    return type == SYN_Q8_0 ? 0 : small_block(type) ? ((n_in / 32 + 7) & ~int64_t(7)) : n_in / 16;
+}
+__host__ __device__ __forceinline__ int64_t sum_bytes(int type, int64_t n_in) { return 2 * sum_stride(type, n_in); }
+
 // Convert every activation row of every matrix of the launch into the global workspace,
 // in the layout the decode kernel copies to shared memory: codes with swizzled 16-byte
 // chunks, block scales, 16-sums.  One warp per 256-block (K-quants) or per four 32-blocks
@@ -138,7 +146,7 @@ __global__ void __launch_bounds__(128) k_act_decode(const __grid_constant__ Gemv
         int8_t* aq = reinterpret_cast<int8_t*>(J.actg);
         float* ad = reinterpret_cast<float*>(J.actg + J.g_d);
         int16_t* as = reinterpret_cast<int16_t*>(J.actg + J.g_s);
-        if (J.type == SYN_Q8_0) {
+        if (small_block(J.type)) {
             const int t = r / J.units;
             const int blk = (r - t * J.units) * 4 + (lane >> 3), e = lane & 7;
             float v[4] = {0.f, 0.f, 0.f, 0.f};
@@ -149,9 +157,18 @@ __global__ void __launch_bounds__(128) k_act_decode(const __grid_constant__ Gemv
             uint16_t db;
             bool fin;
             const uint32_t q = q8_0_group(v, &db, &fin);
+            // Q4_0 / Q5_0 weights: the block's code sum, for the -8 / -16 offset of their codes
+            int qs = 0;
+            if (J.type != SYN_Q8_0) {
+                qs = __dp4a((int)q, 0x01010101, 0);
+                qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+                qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+                qs += __shfl_xor_sync(0xffffffffu, qs, 4);
+            }
             if (blk < J.nbx) {
                 *reinterpret_cast<uint32_t*>(aq + (int64_t)t * J.n_in + q8_chunk(blk, e >> 2) + 4 * (e & 3)) = q;
                 if (e == 0) ad[(int64_t)t * J.ds + blk] = h2f_bits(db);
+                if (e == 0 && J.type != SYN_Q8_0) as[(int64_t)t * sum_stride(J.type, J.n_in) + blk] = (int16_t)qs;
             }
         } else {
             const int t = r / J.nbx;
@@ -176,8 +193,9 @@ __global__ void __launch_bounds__(128) k_act_decode(const __grid_constant__ Gemv
 struct ActView {
     const int8_t* q;    // token 0 codes (swizzled chunks); token t at + t * n_in
     const float* d;     // token 0 scales; token t at + t * ds
-    const int16_t* s;   // token 0 16-sums; token t at + t * nbx * 16
-    int n_in, nbx, ds;
+    const int16_t* s;   // token 0 sums (K-quants: 16-sums, Q4_0/Q5_0: block code sums);
+                        // token t at + t * sst
+    int n_in, nbx, ds, sst;
 };
 
 // ---- Q4_K: half a block per lane (h = 0: sub-blocks 0..3, h = 1: sub-blocks 4..7) ----
@@ -305,17 +323,65 @@ __device__ __forceinline__ void lane_q8_0(const uint8_t* blk, int n, int B, cons
     }
 }
 
+// ---- Q4_0 / Q5_0 (OFF = 8 / 16): n (1 or 2) consecutive 18- / 22-byte blocks per lane;
+// blk 2-byte aligned.  I = sum q*x - OFF * (sum of the activation codes of the block). ----
+template <int NT, int OFF>
+__device__ __forceinline__ void lane_qx_0(const uint8_t* blk, int n, int B, const ActView& A, float acc[NT]) {
+    constexpr int BB = OFF == 8 ? 18 : 22;
+#pragma unroll
+    for (int e = 0; e < 2; e++) {
+        if (e >= n) break;
+        const uint8_t* p = blk + BB * e;
+        const float Dw = h2f_bits(*reinterpret_cast<const uint16_t*>(p));
+        uint32_t w[5];
+        if (OFF == 8) lds_words_any<4>(p + 2, w + 1);
+        else lds_words_any<5>(p + 2, w);  // w[0] = qh: bit k = fifth bit of code k
+        uint32_t lo[4], hi[4];  // codes 4i..4i+3 and 16+4i..16+4i+3, one per byte
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            lo[i] = w[1 + i] & 0x0F0F0F0Fu;
+            hi[i] = (w[1 + i] >> 4) & 0x0F0F0F0Fu;
+            if (OFF == 16) {  // spread 4 bits of qh into bit 4 of 4 bytes
+                lo[i] |= ((((w[0] >> (4 * i)) & 15u) * 0x00204081u) & 0x01010101u) << 4;
+                hi[i] |= ((((w[0] >> (16 + 4 * i)) & 15u) * 0x00204081u) & 0x01010101u) << 4;
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < NT; t++) {
+            const int8_t* xq = A.q + t * A.n_in;
+            const uint4 x0 = *reinterpret_cast<const uint4*>(xq + q8_chunk(B + e, 0));
+            const uint4 x1 = *reinterpret_cast<const uint4*>(xq + q8_chunk(B + e, 1));
+            int I = dp4a(lo[0], x0.x, 0);
+            I = dp4a(lo[1], x0.y, I);
+            I = dp4a(lo[2], x0.z, I);
+            I = dp4a(lo[3], x0.w, I);
+            I = dp4a(hi[0], x1.x, I);
+            I = dp4a(hi[1], x1.y, I);
+            I = dp4a(hi[2], x1.z, I);
+            I = dp4a(hi[3], x1.w, I);
+            I -= OFF * (int)A.s[t * A.sst + B + e];
+            acc[t] = fmaf(Dw * A.d[t * A.ds + B + e], (float)I, acc[t]);
+        }
+    }
+}
+
 // This lane's share of warp step `first` .. of a run of blocks: K-quants take half a block
-// per lane (block first + lane/2, part lane%2); Q8_0 takes two blocks per lane.
+// per lane (block first + lane/2, part lane%2); the 32-weight formats take two blocks per lane.
 // `avail` = blocks of the run from `first` on; the activation block of run block i is
 // (B0 + i) & bmask (bmask = nb - 1 when the run holds several whole rows).
 template <int NT>
 __device__ __forceinline__ void lane_step(int type, const uint8_t* base, int bb, int first, int avail, int B0,
                                           int bmask, const ActView& A, float acc[NT]) {
     const int lane = threadIdx.x & 31;
-    if (type == SYN_Q8_0) {
+    if (small_block(type)) {
         const int k = 2 * lane;
-        if (k < avail) lane_q8_0<NT>(base + (first + k) * bb, min(2, avail - k), (B0 + k) & bmask, A, acc);
+        if (k < avail) {
+            const uint8_t* p = base + (first + k) * bb;
+            const int n = min(2, avail - k), B = (B0 + k) & bmask;
+            if (type == SYN_Q8_0) lane_q8_0<NT>(p, n, B, A, acc);
+            else if (type == SYN_Q4_0) lane_qx_0<NT, 8>(p, n, B, A, acc);
+            else lane_qx_0<NT, 16>(p, n, B, A, acc);
+        }
     } else {
         const int k = lane >> 1;
         if (k < avail) {
@@ -381,7 +447,8 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
     const int b0 = split ? (u0 - (u0 / upr) * upr) * sblk : 0;
     const int64_t r1 = u1;  // unsplit matrices: units are rows
     const ActView A{reinterpret_cast<const int8_t*>(smem + Jp.act_q), reinterpret_cast<const float*>(smem + Jp.act_d),
-                    reinterpret_cast<const int16_t*>(smem + Jp.act_s), Jp.n_in, Jp.nbx, Jp.ds};
+                    reinterpret_cast<const int16_t*>(smem + Jp.act_s), Jp.n_in, Jp.nbx, Jp.ds,
+                    (int)sum_stride(type, Jp.n_in)};
 
     // stage extent at (row, bcol): blocks and whole rows (0 for a run inside one row)
     auto extent = [&](int64_t row, int bcol, int& nblk, int& nrows) {
@@ -451,7 +518,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
             uint32_t tx = 0;
             for (int j = ja; j <= jb; j++) {
                 const GemvJob& J = b.job[j];
-                tx += (uint32_t)(nt * J.n_in + nt * J.ds * 4 + (J.type == SYN_Q8_0 ? 0 : nt * (J.n_in / 8)));
+                tx += (uint32_t)(nt * J.n_in + nt * J.ds * 4 + nt * sum_bytes(J.type, J.n_in));
             }
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(act_bar, tx);
@@ -460,8 +527,8 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
                 bulk_g2s(smem_u32(smem + J.act_q), J.actg + t0 * J.n_in, (uint32_t)(nt * J.n_in), act_bar);
                 bulk_g2s(smem_u32(smem + J.act_d), J.actg + J.g_d + t0 * J.ds * 4, (uint32_t)(nt * J.ds * 4), act_bar);
                 if (J.type != SYN_Q8_0)
-                    bulk_g2s(smem_u32(smem + J.act_s), J.actg + J.g_s + t0 * (J.n_in / 8), (uint32_t)(nt * (J.n_in / 8)),
-                             act_bar);
+                    bulk_g2s(smem_u32(smem + J.act_s), J.actg + J.g_s + t0 * sum_bytes(J.type, J.n_in),
+                             (uint32_t)(nt * sum_bytes(J.type, J.n_in)), act_bar);
             }
         }
         if (!mbar_wait(act_bar, act_parity, b.err, abort_flag)) break;
@@ -506,10 +573,10 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
             if (lg >= 0) {
                 // rows of 2^lg <= bps blocks: bps >> lg rows per warp step; the lanes of a row
                 // form an aligned group of 2^lgl lanes
-                const int lgl = type == SYN_Q8_0 ? lg - 1 : lg + 1;
+                const int lgl = small_block(type) ? lg - 1 : lg + 1;
                 for (int s0 = 0; s0 < nblk; s0 += bps) {
                     lane_step<NT>(type, sbase, bb, s0, nblk - s0, s0, nb - 1, A, acc);
-                    const int mine = s0 + (type == SYN_Q8_0 ? 2 * lane : lane >> 1);  // first block of this lane
+                    const int mine = s0 + (small_block(type) ? 2 * lane : lane >> 1);  // first block of this lane
 #pragma unroll
                     for (int t = 0; t < NT; t++) {
                         const float v = group_sum(acc[t], lgl);
@@ -560,9 +627,8 @@ static_assert(GEMV_ACT_BUDGET >= 8 * 1024, "decode ring leaves too little shared
 int64_t gemv_act_limit() { return GEMV_ACT_BUDGET; }
 
 static int64_t act_bytes_per_token(int type, int64_t n_in) {
-    const int64_t nbx = n_in / (type == SYN_Q8_0 ? 32 : 256), ds = (nbx + 3) & ~int64_t(3);
-    if (type == SYN_Q8_0) return n_in + ds * 4;
-    return n_in + ds * 4 + (n_in / 16) * 2;
+    const int64_t nbx = n_in / block_elems(type), ds = (nbx + 3) & ~int64_t(3);
+    return n_in + ds * 4 + sum_bytes(type, n_in);
 }
 
 template <int NT>
@@ -576,7 +642,7 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
         J.act_d = (int)off;
         off = up16(off + (int64_t)NT * J.ds * 4);
         J.act_s = (int)off;
-        off = up16(off + (J.type == SYN_Q8_0 ? 0 : (int64_t)NT * (J.n_in / 16) * 2));
+        off = up16(off + (int64_t)NT * sum_bytes(J.type, J.n_in));
     }
     off = (off + 127) & ~int64_t(127);
     b.off_stage = (int)off;
@@ -644,7 +710,7 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
     int64_t units = 0;
     for (int j = 0; j < b.n_jobs; j++) {
         GemvJob& J = b.job[j];
-        J.units = J.type == SYN_Q8_0 ? (J.nbx + 3) / 4 : J.nbx;
+        J.units = small_block(J.type) ? (J.nbx + 3) / 4 : J.nbx;
         J.unit_begin = (int)units;
         units += b.n_tok * J.units;
     }
@@ -686,12 +752,12 @@ static void make_job(GemvJob& J, const GemvDesc& d, int64_t byte_begin) {
     J.row_bytes = (int64_t)J.nb * J.bb;
     J.total_floor16 = (d.n_out * J.row_bytes) & ~int64_t(15);
     J.byte_begin = byte_begin;
-    J.nbx = (int)(d.n_in / (d.type == SYN_Q8_0 ? 32 : 256));
+    J.nbx = (int)(d.n_in / block_elems(d.type));
     J.ds = (J.nbx + 3) & ~3;
-    J.bps = d.type == SYN_Q8_0 ? 64 : 16;
+    J.bps = small_block(d.type) ? 64 : 16;
     const int fit = GV_STAGE / J.bb;  // >= bps for every format (static_assert above)
     J.lg_nb = -1;
-    const bool packed = J.nb <= J.bps && (J.nb & (J.nb - 1)) == 0 && !(d.type == SYN_Q8_0 && J.nb < 2);
+    const bool packed = J.nb <= J.bps && (J.nb & (J.nb - 1)) == 0 && !(small_block(d.type) && J.nb < 2);
     if (packed) {
         int lg = 0;
         while ((1 << lg) < J.nb) lg++;
@@ -710,8 +776,8 @@ int64_t gemv_act_bytes(int type, int64_t n_in) { return act_bytes_per_token(type
 
 // Global workspace of one matrix's converted activations (all tokens).
 static int64_t act_global_bytes(int type, int64_t n_in, int64_t n_tok) {
-    const int64_t nbx = n_in / (type == SYN_Q8_0 ? 32 : 256), ds = (nbx + 3) & ~int64_t(3);
-    return up16(n_tok * n_in) + up16(n_tok * ds * 4) + (type == SYN_Q8_0 ? 0 : up16(n_tok * (n_in / 8))) + 256;
+    const int64_t nbx = n_in / block_elems(type), ds = (nbx + 3) & ~int64_t(3);
+    return up16(n_tok * n_in) + up16(n_tok * ds * 4) + up16(n_tok * sum_bytes(type, n_in)) + 256;
 }
 
 int64_t gemv_workspace_bytes(int n, const GemvDesc* d, int64_t n_tok) {

@@ -25,7 +25,46 @@ __global__ void __launch_bounds__(256) k_quantize(const float* __restrict__ src,
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     bool ok_all = true;
-    if (T == SYN_Q8_0) {
+    if (T == SYN_Q4_0 || T == SYN_Q5_0) {
+        // 4 blocks per warp step: lanes 8g..8g+7 own block 4*step+g, 4 values each
+        constexpr int OFF = T == SYN_Q4_0 ? 8 : 16, BB = T == SYN_Q4_0 ? 18 : 22, QS = T == SYN_Q4_0 ? 2 : 6;
+        for (int64_t base = warp * 4; base < n_blocks; base += n_warps * 4) {
+            int64_t b = base + (lane >> 3);
+            const int e = lane & 7;
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            if (b < n_blocks) {
+                float4 x = *reinterpret_cast<const float4*>(src + b * 32 + 4 * e);
+                v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+            }
+            uint16_t db;
+            bool fin;
+            const uint32_t q = qx_0_group<OFF>(v, &db, &fin);
+            // byte l of the codes: q[l] in the low nibble, q[l + 16] in the high one; lanes
+            // e < 4 hold q[4e..4e+3], lanes e + 4 hold q[16 + 4e ..]
+            const uint32_t up = __shfl_down_sync(0xffffffffu, q, 4);
+            uint32_t hb = 0;  // fifth bits of this lane's 4 codes at bits 4e..4e+3 (Q5_0)
+            if (T == SYN_Q5_0) {
+                const uint32_t t = (q >> 4) & 0x01010101u;
+                hb = ((t | (t >> 7) | (t >> 14) | (t >> 21)) & 15u) << (4 * e);
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) hb |= __shfl_xor_sync(0xffffffffu, hb, o);
+            }
+            if (b < n_blocks) {
+                uint8_t* p = dst + b * BB;
+                if (e == 0) st_u16(p, db);
+                if (T == SYN_Q5_0 && e == 0) {
+                    st_u16(p + 2, hb & 0xFFFF);
+                    st_u16(p + 4, hb >> 16);
+                }
+                if (e < 4) {
+                    const uint32_t packed = (q & 0x0F0F0F0Fu) | ((up & 0x0F0F0F0Fu) << 4);
+                    st_u16(p + QS + 4 * e, packed & 0xFFFF);
+                    st_u16(p + QS + 4 * e + 2, packed >> 16);
+                }
+                ok_all &= fin;
+            }
+        }
+    } else if (T == SYN_Q8_0) {
         // 4 blocks per warp step: lanes 8g..8g+7 own block 4*step+g
         for (int64_t base = warp * 4; base < n_blocks; base += n_warps * 4) {
             int64_t b = base + (lane >> 3);
@@ -150,6 +189,28 @@ __global__ void __launch_bounds__(256) k_dequantize(const uint8_t* __restrict__ 
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    if (T == SYN_Q4_0 || T == SYN_Q5_0) {
+        constexpr int OFF = T == SYN_Q4_0 ? 8 : 16, BB = T == SYN_Q4_0 ? 18 : 22, QS = T == SYN_Q4_0 ? 2 : 6;
+        for (int64_t base = warp * 4; base < n_blocks; base += n_warps * 4) {
+            int64_t b = base + (lane >> 3);
+            if (b >= n_blocks) continue;
+            const uint8_t* p = src + b * BB;
+            const float D = h2f_bits(ld_u16(p));
+            const int e = (lane & 7) * 4;  // values e .. e+3
+            const int l = e & 15, sh = e >= 16 ? 4 : 0;
+            uint32_t qh = 0;
+            if (T == SYN_Q5_0) qh = (uint32_t)ld_u16(p + 2) | ((uint32_t)ld_u16(p + 4) << 16);
+            float y[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                int q = (p[QS + l + i] >> sh) & 15;
+                if (T == SYN_Q5_0) q |= (int)((qh >> (e + i)) & 1) << 4;
+                y[i] = __fmul_rn(D, (float)(q - OFF));
+            }
+            *reinterpret_cast<float4*>(dst + b * 32 + e) = make_float4(y[0], y[1], y[2], y[3]);
+        }
+        return;
+    }
     if (T == SYN_Q8_0) {
         for (int64_t base = warp * 4; base < n_blocks; base += n_warps * 4) {
             int64_t b = base + (lane >> 3);
@@ -336,7 +397,19 @@ __global__ void k_block_sums(const uint8_t* __restrict__ W, int64_t n_out, int64
     int64_t o = (idx / nb) % n_out;
     int64_t t = idx / (nb * n_out);
     int32_t s0 = 0, s1 = 0;
-    if (T == SYN_Q8_0) {
+    if (T == SYN_Q4_0 || T == SYN_Q5_0) {
+        constexpr int OFF = T == SYN_Q4_0 ? 8 : 16, BB = T == SYN_Q4_0 ? 18 : 22, QS = T == SYN_Q4_0 ? 2 : 6;
+        const uint8_t* w = W + (o * nb + b) * BB;
+        const uint8_t* x = Xq + (t * nb + b) * 34;
+        const uint32_t qh = T == SYN_Q5_0 ? ((uint32_t)w[2] | ((uint32_t)w[3] << 8) | ((uint32_t)w[4] << 16) |
+                                             ((uint32_t)w[5] << 24))
+                                          : 0u;
+        for (int i = 0; i < 32; i++) {
+            int q = (w[QS + (i & 15)] >> (i >= 16 ? 4 : 0)) & 15;
+            if (T == SYN_Q5_0) q |= (int)((qh >> i) & 1) << 4;
+            s0 += (q - OFF) * (int32_t)(int8_t)x[2 + i];
+        }
+    } else if (T == SYN_Q8_0) {
         const uint8_t* w = W + (o * nb + b) * 34;
         const uint8_t* x = Xq + (t * nb + b) * 34;
         for (int i = 0; i < 32; i++) s0 += (int32_t)(int8_t)w[2 + i] * (int32_t)(int8_t)x[2 + i];
@@ -387,7 +460,7 @@ static int grid_for(int64_t warps_needed, int sms) {
 
 cudaError_t launch_quantize(int type, const float* src, void* dst, int64_t n_blocks, int* range_err,
                             int sms, cudaStream_t s) {
-    int64_t warps = (type == SYN_Q8_0) ? (n_blocks + 3) / 4 : n_blocks;
+    int64_t warps = small_block(type) ? (n_blocks + 3) / 4 : n_blocks;
     int g = grid_for(warps, sms);
     uint8_t* d = static_cast<uint8_t*>(dst);
     switch (type) {
@@ -395,6 +468,8 @@ cudaError_t launch_quantize(int type, const float* src, void* dst, int64_t n_blo
     case SYN_Q4_K: k_quantize<SYN_Q4_K><<<g, 256, 0, s>>>(src, d, n_blocks, range_err); break;
     case SYN_Q6_K: k_quantize<SYN_Q6_K><<<g, 256, 0, s>>>(src, d, n_blocks, range_err); break;
     case SYN_Q8_K: k_quantize<SYN_Q8_K><<<g, 256, 0, s>>>(src, d, n_blocks, range_err); break;
+    case SYN_Q4_0: k_quantize<SYN_Q4_0><<<g, 256, 0, s>>>(src, d, n_blocks, range_err); break;
+    case SYN_Q5_0: k_quantize<SYN_Q5_0><<<g, 256, 0, s>>>(src, d, n_blocks, range_err); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -402,7 +477,7 @@ cudaError_t launch_quantize(int type, const float* src, void* dst, int64_t n_blo
 
 cudaError_t launch_dequantize(int type, const void* src, float* dst, int64_t n_blocks, int sms,
                               cudaStream_t s) {
-    int64_t warps = (type == SYN_Q8_0) ? (n_blocks + 3) / 4 : n_blocks;
+    int64_t warps = small_block(type) ? (n_blocks + 3) / 4 : n_blocks;
     int g = grid_for(warps, sms);
     const uint8_t* p = static_cast<const uint8_t*>(src);
     switch (type) {
@@ -410,6 +485,8 @@ cudaError_t launch_dequantize(int type, const void* src, float* dst, int64_t n_b
     case SYN_Q4_K: k_dequantize<SYN_Q4_K><<<g, 256, 0, s>>>(p, dst, n_blocks); break;
     case SYN_Q6_K: k_dequantize<SYN_Q6_K><<<g, 256, 0, s>>>(p, dst, n_blocks); break;
     case SYN_Q8_K: k_dequantize<SYN_Q8_K><<<g, 256, 0, s>>>(p, dst, n_blocks); break;
+    case SYN_Q4_0: k_dequantize<SYN_Q4_0><<<g, 256, 0, s>>>(p, dst, n_blocks); break;
+    case SYN_Q5_0: k_dequantize<SYN_Q5_0><<<g, 256, 0, s>>>(p, dst, n_blocks); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -445,6 +522,8 @@ cudaError_t launch_block_sums(int type, const void* W, int64_t n_out, int64_t nb
     case SYN_Q8_0: k_block_sums<SYN_Q8_0><<<(unsigned)g, 256, 0, s>>>(w, n_out, nb, x, n_tok, S); break;
     case SYN_Q4_K: k_block_sums<SYN_Q4_K><<<(unsigned)g, 256, 0, s>>>(w, n_out, nb, x, n_tok, S); break;
     case SYN_Q6_K: k_block_sums<SYN_Q6_K><<<(unsigned)g, 256, 0, s>>>(w, n_out, nb, x, n_tok, S); break;
+    case SYN_Q4_0: k_block_sums<SYN_Q4_0><<<(unsigned)g, 256, 0, s>>>(w, n_out, nb, x, n_tok, S); break;
+    case SYN_Q5_0: k_block_sums<SYN_Q5_0><<<(unsigned)g, 256, 0, s>>>(w, n_out, nb, x, n_tok, S); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -60,6 +60,42 @@ __device__ __forceinline__ uint32_t q8_0_group(const float v[4], uint16_t* dbits
 }
 
 // ---------------------------------------------------------------------------------------
+// Q4_0 / Q5_0 (OFF = 8 / 16): groups of 8 lanes, 4 consecutive values per lane, one
+// 32-block per group.  m = the first value of largest magnitude (index order), d = m/-OFF,
+// q = clamp(round(x/D) + OFF, 0, 2*OFF - 1).  Returns the 4 codes as bytes of a word.
+// ---------------------------------------------------------------------------------------
+template <int OFF>
+__device__ __forceinline__ uint32_t qx_0_group(const float v[4], uint16_t* dbits, bool* finite) {
+    const int e = threadIdx.x & 7;
+    float a = 0.0f, m = 0.0f;
+    int idx = 4 * e;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const float ai = fabsf(v[i]);
+        if (ai > a) { a = ai; m = v[i]; idx = 4 * e + i; }
+    }
+    // (largest magnitude, lowest index) over the 8 lanes of the group
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        const float ao = __shfl_xor_sync(0xffffffffu, a, o);
+        const float mo = __shfl_xor_sync(0xffffffffu, m, o);
+        const int io = __shfl_xor_sync(0xffffffffu, idx, o);
+        if (ao > a || (ao == a && io < idx)) { a = ao; m = mo; idx = io; }
+    }
+    const float d = __fdiv_rn(m, -(float)OFF);
+    const __half hd = __float2half_rn(d);
+    const float D = __half2float(hd);
+    int q[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        q[i] = (D == 0.0f) ? OFF
+                           : (int)clampf(__fadd_rn(roundf(__fdiv_rn(v[i], D)), (float)OFF), 0.0f, (float)(2 * OFF - 1));
+    *dbits = __half_as_ushort(hd);
+    *finite = all_finite4(v) && !__hisinf(hd);
+    return pack4_s8(q[0], q[1], q[2], q[3]);
+}
+
+// ---------------------------------------------------------------------------------------
 // Q8_K: one warp per 256-block, 8 consecutive values per lane (lane L: 8L..8L+7).
 // Returns the codes as two words, the fp32 scale, and in *bsum the sum of the 16 codes
 // of sub-block L/2 (valid in every lane).

@@ -49,12 +49,20 @@ typedef struct CUstream_st* syn_stream_t; /* identical to cudaStream_t */
  *   Q6_K 256 weights, 210 B: 128 B low 4 bits, 64 B high 2 bits, 16 int8 scales, fp16 d;
  *                            16 sub-blocks of 16;                     w = d*sc*(q - 32)
  *   Q8_K 256 values,  292 B: fp32 d, 256 int8 q, 16 int16 sums of 16 q (activations only)
- * In-block byte order: the public GGUF layout (fields in the order listed above). */
+ *   Q4_0  32 weights,  18 B: fp16 d, 32 4-bit q;                      w = d*(q - 8)
+ *   Q5_0  32 weights,  22 B: fp16 d, 32-bit qh (each q's fifth bit), 32 4-bit low parts;
+ *                                                                     w = d*(q - 16)
+ * In-block byte order: the public GGUF layout (fields in the order listed above; Q4_0/Q5_0
+ * store q[l] in the low and q[l+16] in the high nibble of byte l).
+ * vec_dot_type (the activation format of the product): Q8_0 for Q8_0, Q4_0 and Q5_0; Q8_K
+ * for Q4_K and Q6_K. */
 enum {
     SYN_TYPE_Q8_0 = 1,
     SYN_TYPE_Q4_K = 2,
     SYN_TYPE_Q6_K = 3,
     SYN_TYPE_Q8_K = 4,
+    SYN_TYPE_Q4_0 = 5,
+    SYN_TYPE_Q5_0 = 6,
 };
 
 enum {
@@ -71,7 +79,7 @@ enum {
     SYN_ERR_TOO_LARGE = -10, /* the problem needs more than the fixed scratch array holds */
 };
 
-/* Elements per block: 32 (Q8_0) or 256 (Q4_K, Q6_K, Q8_K); -1 for an unknown type. */
+/* Elements per block: 32 (Q8_0, Q4_0, Q5_0) or 256 (Q4_K, Q6_K, Q8_K); -1 for an unknown type. */
 SYN_API int64_t syn_block_elems(int type);
 
 /* Bytes per block: 34, 144, 210, 292; -1 for an unknown type. */
@@ -82,7 +90,7 @@ SYN_API int64_t syn_block_bytes(int type);
 SYN_API int64_t syn_row_bytes(int type, int64_t n);
 
 /* Quantize n_rows rows of n_per_row fp32 values (src, row-major, contiguous) into blocks
- * (dst, n_rows * syn_row_bytes bytes).  type: Q8_0, Q4_K, Q6_K or Q8_K.
+ * (dst, n_rows * syn_row_bytes bytes).  type: Q8_0, Q4_K, Q6_K, Q8_K, Q4_0 or Q5_0.
  * Encoders (plain readings of the format table; bit-exact with the CPU oracle):
  *   Q8_0  d = fp16(amax/127); q = clamp(round(x / d_stored), -127, 127)
  *   Q8_K  d = amax/127 (fp32); q = clamp(round(x / d), -127, 127); bsums = sums of 16 q
@@ -91,7 +99,10 @@ SYN_API int64_t syn_row_bytes(int type, int64_t n);
  *         mn = min(63, round(m/dmin)), q = clamp(round((x + dmin*mn)/(d*sc)), 0, 15)
  *   Q6_K  per 16-sub-block: s = amax/31; d = fp16(max s / 127), sc = min(127, round(s/d)),
  *         q = clamp(round(x/(d*sc)), -32, 31) + 32
- * round = ties away from zero; a zero scale gives zero codes.
+ *   Q4_0  m = the block's value of largest magnitude (first one), d = fp16(m / -8),
+ *         q = clamp(round(x / d) + 8, 0, 15)
+ *   Q5_0  d = fp16(m / -16), q = clamp(round(x / d) + 16, 0, 31)
+ * round = ties away from zero; a zero scale gives zero codes (Q4_0/Q5_0: q = 8 / 16).
  * Returns SYN_ERR_RANGE if any input is NaN/Inf or a scale overflows fp16; to report
  * that, this call SYNCHRONIZES `stream` before returning (it is an offline operation).
  * Calls that overlap on the GPU share one status word and must not run concurrently.
@@ -101,22 +112,23 @@ SYN_API int syn_quantize(int type, const float* src, void* dst, int64_t n_rows, 
 
 /* Expand blocks back to fp32 ("dequantize_row_*", same page, section 5): dst gets
  * n_rows * n_per_row floats.  Q8_0: d*q; Q4_K: (d*sc)*q - (dmin*mn); Q6_K:
- * (d*sc)*(q-32); Q8_K: d*q — each product and difference one fp32 rounding, no FMA,
+ * (d*sc)*(q-32); Q8_K: d*q; Q4_0: d*(q-8); Q5_0: d*(q-16) — each product and difference
+ * one fp32 rounding, no FMA,
  * so the result is bit-exact with the CPU oracle.  Asynchronous.  Alignment: 16 B. */
 SYN_API int syn_dequantize(int type, const void* src, float* dst, int64_t n_rows, int64_t n_per_row,
                    syn_stream_t stream);
 
 /* The activation step of the product on its own (from_float to the vec_dot_type):
  * X (n_tok x n_in fp32) -> codes qs (n_tok x n_in int8), scales d (n_tok x n_in/Bx fp32,
- * Bx = 32 for Q8_0 weights, 256 for K-quant weights; for Q8_0 the value of the stored
- * fp16 scale) and, for K-quant weights only, bsums (n_tok x n_in/16 int16; may be NULL
- * for Q8_0).  wtype is the WEIGHT format (Q8_0, Q4_K or Q6_K).  This is the same device
+ * Bx = 32 for Q8_0/Q4_0/Q5_0 weights, 256 for K-quant weights; for Q8_0 the value of
+ * the stored fp16 scale) and, for K-quant weights only, bsums (n_tok x n_in/16 int16; may
+ * be NULL otherwise).  wtype is the WEIGHT format (Q8_0, Q4_K, Q6_K, Q4_0 or Q5_0).  This is the same device
  * code the product kernels run on their inputs.  Asynchronous.  Alignment: 16 B. */
 SYN_API int syn_quantize_activations(int wtype, const float* X, int64_t n_tok, int64_t n_in,
                              int8_t* qs, float* d, int16_t* bsums, syn_stream_t stream);
 
 /* Y = ggml_mul_mat(W, X) as described at the top of this file.
- * type: Q8_0, Q4_K or Q6_K (Q8_K is activation-only and rejected with SYN_ERR_TYPE).
+ * type: Q8_0, Q4_K, Q6_K, Q4_0 or Q5_0 (Q8_K is activation-only: SYN_ERR_TYPE).
  * n_tok <= the decode threshold (default 8, see syn_set_gemv_max_tok) runs the decode
  * kernel: one launch that quantizes X in shared memory and streams W once per group of
  * up to 8 tokens.  Larger n_tok runs the prefill path: one kernel quantizes X and writes
@@ -133,7 +145,7 @@ SYN_API int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in,
 
 /* One product of a group (see syn_mul_mat_batch). */
 typedef struct {
-    int type;          /* SYN_TYPE_Q8_0, SYN_TYPE_Q4_K or SYN_TYPE_Q6_K */
+    int type;          /* a weight format: Q8_0, Q4_K, Q6_K, Q4_0 or Q5_0 */
     const void* W;     /* n_out x n_in weights, 16-byte aligned */
     int64_t n_out;
     int64_t n_in;
@@ -159,10 +171,11 @@ SYN_API int syn_reserve(int64_t max_n_in, int64_t max_n_tok, syn_stream_t stream
 SYN_API int syn_release(void);
 
 /* Integer block sums for bit-exact checks (not on the hot path).  Xq holds n_tok rows of
- * packed vec_dot_type blocks (Q8_0 blocks for Q8_0 weights, Q8_K blocks otherwise).
+ * packed vec_dot_type blocks (Q8_0 blocks for Q8_0/Q4_0/Q5_0 weights, Q8_K otherwise).
  * S[((t*n_out + o)*n_blocks + b)*2 + {0,1}]:  Q8_0 {I, 0}: I = sum qw*qx;
  * Q4_K {A, Bm}: A = sum_j sc_j * sum_{i in j} q_i*qx_i, Bm = sum_j mn_j * (bsum_2j + bsum_2j+1);
- * Q6_K {C, 0}: C = sum_j sc_j * sum_{i in j} (q_i - 32)*qx_i.  Asynchronous. */
+ * Q6_K {C, 0}: C = sum_j sc_j * sum_{i in j} (q_i - 32)*qx_i;
+ * Q4_0 / Q5_0 {I, 0}: I = sum (qw - 8 / 16)*qx.  Asynchronous. */
 SYN_API int syn_block_sums(int type, const void* W, int64_t n_out, int64_t n_in,
                    const void* Xq, int64_t n_tok, int32_t* S, syn_stream_t stream);
 

@@ -65,7 +65,7 @@ def test_argument_checks_need_no_gpu(lib):
     assert L.syn_mul_mat(2, None, 4, 256, p, 1, p, None) == L.ERR_NULL
     assert L.syn_mul_mat(2, p + 4, 4, 256, p, 1, p, None) == L.ERR_ALIGN
     assert L.syn_quantize(2, p, p, 1, 255, None) == L.ERR_SHAPE
-    assert L.syn_quantize(5, p, p, 1, 256, None) == L.ERR_TYPE
+    assert L.syn_quantize(7, p, p, 1, 256, None) == L.ERR_TYPE  # unknown format
     assert L.syn_quantize(1, p, p, 0, 32, None) == L.OK
     assert L.syn_quantize(1, p + 8, p, 1, 32, None) == L.ERR_ALIGN
     assert L.syn_dequantize(3, None, p, 1, 256, None) == L.ERR_NULL

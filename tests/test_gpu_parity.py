@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 TOL = 1e-4
-TYPES_W = [oracle.Q8_0, oracle.Q4_K, oracle.Q6_K]
+TYPES_W = [oracle.Q8_0, oracle.Q4_K, oracle.Q6_K, oracle.Q4_0, oracle.Q5_0]
 TYPES_ALL = TYPES_W + [oracle.Q8_K]
 
 
@@ -88,7 +88,7 @@ def test_dequantize_bit_exact(syn, t):
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
 
 
-@pytest.mark.parametrize("t", [oracle.Q4_K, oracle.Q6_K, oracle.Q8_0])
+@pytest.mark.parametrize("t", [oracle.Q4_K, oracle.Q6_K, oracle.Q8_0, oracle.Q4_0, oracle.Q5_0])
 def test_dequantize_arbitrary_codes_bit_exact(syn, t):
     """Random block bytes (finite fp16 scales), including negative Q6_K scales."""
     n_rows, n = 19, 512
@@ -96,7 +96,7 @@ def test_dequantize_arbitrary_codes_bit_exact(syn, t):
     raw = synth.integers(3, (n_rows, rb), 0, 256).astype(np.uint8)
     nb, bb = n // oracle.BLOCK_ELEMS[t], oracle.BLOCK_BYTES[t]
     blocks = raw.reshape(n_rows, nb, bb)
-    offs = {oracle.Q8_0: [0], oracle.Q4_K: [0, 2], oracle.Q6_K: [208]}[t]
+    offs = {oracle.Q8_0: [0], oracle.Q4_K: [0, 2], oracle.Q6_K: [208], oracle.Q4_0: [0], oracle.Q5_0: [0]}[t]
     for o in offs:  # keep scales finite: clear the top exponent bit
         blocks[:, :, o + 1] &= 0xBF
     want = oracle.dequantize(t, raw, n)
@@ -114,7 +114,7 @@ def test_quantize_range_errors(syn):
         assert e.value.status == syn.ERR_RANGE
     x = np.zeros((1, 256), np.float32)
     x[0, 0] = 1e9
-    for t in (oracle.Q4_K, oracle.Q6_K):
+    for t in (oracle.Q4_K, oracle.Q6_K, oracle.Q4_0, oracle.Q5_0):
         with pytest.raises(syn.SynError):
             syn.quantize(t, dev(x))
     syn.quantize(oracle.Q8_K, dev(x))  # fp32 scale: fine
@@ -202,18 +202,20 @@ def test_mul_mat_gemm(syn, wt, shape):
     assert_close(Y, ref, bound, f"gemm {shape}")
 
 
-def test_mul_mat_q8_0_row_not_multiple_of_256(syn):
-    # Q8_0 rows need only 32-element blocks: 800 = 25 blocks (ragged last k-step)
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q5_0])
+def test_mul_mat_row_not_multiple_of_256(syn, wt):
+    # the 32-weight formats need only 32-element blocks: 800 = 25 blocks (ragged last k-step)
     for path in ("gemv", "gemm"):
-        Y, ref, bound = run_mul_mat(syn, oracle.Q8_0, 77, 800, 20, 77, path)
-        assert_close(Y, ref, bound, f"q8_0 n_in=800 {path}")
+        Y, ref, bound = run_mul_mat(syn, wt, 77, 800, 20, 77, path)
+        assert_close(Y, ref, bound, f"{oracle.NAMES[wt]} n_in=800 {path}")
 
 
 @pytest.mark.parametrize("n_tok", [1, 3, 8])
 def test_mul_mat_batch_mixed_group(syn, n_tok):
     """Grouped decode of matrices of all three formats and ragged shapes in one call."""
     shapes = [(oracle.Q4_K, 300, 2048), (oracle.Q6_K, 77, 1024), (oracle.Q8_0, 129, 800),
-              (oracle.Q4_K, 5, 256), (oracle.Q6_K, 1000, 512), (oracle.Q8_0, 64, 4096)]
+              (oracle.Q4_K, 5, 256), (oracle.Q6_K, 1000, 512), (oracle.Q8_0, 64, 4096),
+              (oracle.Q4_0, 200, 2048), (oracle.Q5_0, 99, 1024), (oracle.Q4_0, 17, 96)]
     items, refs = [], []
     for i, (wt, n_out, n_in) in enumerate(shapes):
         Wq = oracle.quantize(wt, synth.normal(300 + i, (n_out, n_in), 0.02))
