@@ -388,3 +388,15 @@ def test_full_llama8b_sweep_decode(syn, k):
 def test_full_llama8b_sweep_prefill(syn, k):
     i, m = LLAMA8B_DISTINCT[k]
     sampled_check(syn, m, 2048, 5, i, n_rows=32, n_toks=4, path="gemm")
+
+
+# Q4_0 / Q5_0 on the Llama-8B FFN up shape, as the benchmark runs them (decode inputs from
+# workload 6, prefill inputs from workload 7)
+@pytest.mark.parametrize("wt", [oracle.Q4_0, oracle.Q5_0])
+def test_full_qx_0_decode(syn, wt):
+    sampled_check(syn, workloads.Matrix("ffn_up", wt, 14336, 4096), 1, 6, 0, n_rows=256)
+
+
+@pytest.mark.parametrize("wt", [oracle.Q4_0, oracle.Q5_0])
+def test_full_qx_0_prefill(syn, wt):
+    sampled_check(syn, workloads.Matrix("ffn_up", wt, 14336, 4096), 512, 7, 0, n_rows=48, n_toks=6)
