@@ -15,6 +15,7 @@ Parity status per function (see the tests under tests/test_oracle_*.py for the p
   quantize Q4_K/Q6_K     pinned to error bounds, fixed point and hand blocks; the encoders
                          themselves are the plain readings of the format table
   quantize Q4_0/Q5_0     pinned to error bounds, the exact extreme, hand blocks
+  F16 weights            pinned (the fp16 conversion; the product against numpy float16 casts)
   dequantize             pinned (hand-written block bytes against the format formulas)
   block sums / mul_mat   pinned (fp64 brute force over dequantized blocks, the
                          ggml_mul_mat orientation example with exact integers)
@@ -30,11 +31,11 @@ import threading
 
 import numpy as np
 
-Q8_0, Q4_K, Q6_K, Q8_K, Q4_0, Q5_0 = 1, 2, 3, 4, 5, 6
-BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, Q8_K: 256, Q4_0: 32, Q5_0: 32}
-BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, Q8_K: 292, Q4_0: 18, Q5_0: 22}
-VEC_DOT_TYPE = {Q8_0: Q8_0, Q4_K: Q8_K, Q6_K: Q8_K, Q4_0: Q8_0, Q5_0: Q8_0}
-NAMES = {Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K", Q8_K: "Q8_K", Q4_0: "Q4_0", Q5_0: "Q5_0"}
+Q8_0, Q4_K, Q6_K, Q8_K, Q4_0, Q5_0, F16 = 1, 2, 3, 4, 5, 6, 7
+BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, Q8_K: 256, Q4_0: 32, Q5_0: 32, F16: 1}
+BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, Q8_K: 292, Q4_0: 18, Q5_0: 22, F16: 2}
+VEC_DOT_TYPE = {Q8_0: Q8_0, Q4_K: Q8_K, Q6_K: Q8_K, Q4_0: Q8_0, Q5_0: Q8_0, F16: F16}
+NAMES = {Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K", Q8_K: "Q8_K", Q4_0: "Q4_0", Q5_0: "Q5_0", F16: "F16"}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "syn_oracle.c")

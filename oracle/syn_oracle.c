@@ -33,6 +33,8 @@
  *  - Q4_0 / Q5_0 (same table: 32 weights, fp16 d, w = d*(q - 8) / d*(q - 16), q 4 / 5 bits):
  *    d = m / -8 (Q4_0) or m / -16 (Q5_0), m the block's value of largest magnitude with
  *    its sign, so that m itself maps to q = 0; q = clamp(round(x / D) + 8 (16), 0, 15 (31)).
+ *  - F16 weights: one fp16 value per weight (RNE from fp32); their vec_dot_type is F16
+ *    (the activations rounded to fp16 the same way); each product w*x is exact in fp64.
  *  - byte layout inside the blocks: the public GGUF on-disk layout (see the pack/unpack
  *    routines for the field order).
  *  - non-finite input, or a scale that overflows fp16, is rejected (status -5).
@@ -49,6 +51,7 @@
 #define ORC_Q8_K 4
 #define ORC_Q4_0 5
 #define ORC_Q5_0 6
+#define ORC_F16 7
 
 #define ORC_OK 0
 #define ORC_ERR_TYPE (-1)
@@ -127,6 +130,7 @@ int64_t orc_block_elems(int type) {
     switch (type) {
     case ORC_Q8_0: case ORC_Q4_0: case ORC_Q5_0: return 32;
     case ORC_Q4_K: case ORC_Q6_K: case ORC_Q8_K: return 256;
+    case ORC_F16: return 1;
     default: return -1;
     }
 }
@@ -142,6 +146,7 @@ int64_t orc_block_bytes(int type) {
     case ORC_Q8_K: return 4 + 256 + 2 * 16;
     case ORC_Q4_0: return 2 + 16;
     case ORC_Q5_0: return 2 + 4 + 16;
+    case ORC_F16: return 2;
     default: return -1;
     }
 }
@@ -476,6 +481,13 @@ int orc_quantize(int type, const float* src, uint8_t* dst, int64_t n_rows, int64
         case ORC_Q6_K: { q6_k_u b; if ((st = quant_q6_k(x, &b))) return st; pack_q6_k(&b, p); break; }
         case ORC_Q4_0: { qx_0_u b; if ((st = quant_qx_0(x, &b, 8))) return st; pack_q4_0(&b, p); break; }
         case ORC_Q5_0: { qx_0_u b; if ((st = quant_qx_0(x, &b, 16))) return st; pack_q5_0(&b, p); break; }
+        case ORC_F16: {
+            if (!isfinite(x[0])) return ORC_ERR_RANGE;
+            uint16_t h = orc_fp32_to_fp16(x[0]);
+            if ((h & 0x7C00u) == 0x7C00u) return ORC_ERR_RANGE;  /* overflow to infinity */
+            p[0] = (uint8_t)(h & 0xFF); p[1] = (uint8_t)(h >> 8);
+            break;
+        }
         }
     }
     return ORC_OK;
@@ -496,6 +508,7 @@ int orc_dequantize(int type, const uint8_t* src, float* dst, int64_t n_rows, int
         case ORC_Q6_K: { q6_k_u b; unpack_q6_k(p, &b); deq_q6_k(&b, y); break; }
         case ORC_Q4_0: { qx_0_u b; unpack_q4_0(p, &b); deq_qx_0(&b, 8, y); break; }
         case ORC_Q5_0: { qx_0_u b; unpack_q5_0(p, &b); deq_qx_0(&b, 16, y); break; }
+        case ORC_F16: y[0] = orc_fp16_to_fp32((uint16_t)(p[0] | (p[1] << 8))); break;
         }
     }
     return ORC_OK;
@@ -532,6 +545,7 @@ static int vec_dot_type(int wtype) {
     switch (wtype) {
     case ORC_Q8_0: case ORC_Q4_0: case ORC_Q5_0: return ORC_Q8_0;
     case ORC_Q4_K: case ORC_Q6_K: return ORC_Q8_K;
+    case ORC_F16: return ORC_F16;
     default: return -1;
     }
 }
@@ -605,7 +619,7 @@ static double block_value(int wtype, const uint8_t* wp, const uint8_t* xp, const
 int orc_block_sums(int wtype, const uint8_t* W, int64_t n_out, int64_t n_in,
                    const uint8_t* Xq, int64_t n_tok, int32_t* S) {
     int xt = vec_dot_type(wtype);
-    if (xt < 0) return ORC_ERR_TYPE;
+    if (xt < 0 || wtype == ORC_F16) return ORC_ERR_TYPE;  /* F16 products are not integer */
     int st = check_shape(wtype, n_out, n_in);
     if (st) return st;
     int64_t nb = n_in / orc_block_elems(wtype);
@@ -621,6 +635,14 @@ int orc_block_sums(int wtype, const uint8_t* W, int64_t n_out, int64_t n_in,
 /* y[t][o] for one (o, t) pair: fp64 sum over blocks, rounded once to fp32. */
 static float dot_row(int wtype, const uint8_t* Wrow, const uint8_t* Xrow, int64_t nb, int64_t wb, int64_t xb) {
     double acc = 0.0;
+    if (wtype == ORC_F16) {  /* exact fp16 x fp16 products, summed in fp64 */
+        for (int64_t i = 0; i < nb; i++) {
+            double w = orc_fp16_to_fp32((uint16_t)(Wrow[2 * i] | (Wrow[2 * i + 1] << 8)));
+            double x = orc_fp16_to_fp32((uint16_t)(Xrow[2 * i] | (Xrow[2 * i + 1] << 8)));
+            acc += w * x;
+        }
+        return (float)acc;
+    }
     for (int64_t b = 0; b < nb; b++) {
         int32_t s[2];
         block_sums(wtype, Wrow + b * wb, Xrow + b * xb, s);

@@ -509,3 +509,39 @@ def test_mul_mat_sampled_and_threads_agree():
     rows, toks = np.array([0, 36, 5, 17]), np.array([4, 0, 2])
     Ys = oracle.mul_mat_sampled(t, W, n_out, n_in, X, rows, toks)
     assert np.array_equal(Ys, Y1[toks][:, rows])
+
+
+# ----------------------------------------------------------------------------------------
+# F16 weights: vec_dot_type F16 ("The GGML ecosystem, and where synapse fits", section 5:
+# "F16 for F16"; "activations are rounded")
+# ----------------------------------------------------------------------------------------
+
+def test_f16_weights_are_ieee_half():
+    """The F16 'format' is the IEEE binary16 value of each weight, little endian; checked
+    against numpy's float16 cast (an independent RNE implementation)."""
+    x = np.concatenate([_test_inputs(64).ravel(), np.array([65504.0, -65504.0, 6.0e-8, 2.0 ** -24], np.float32)])
+    q = oracle.quantize(oracle.F16, x[None, :])
+    assert np.array_equal(q.view("<u2")[0], x.astype(np.float16).view(np.uint16))
+    back = oracle.dequantize(oracle.F16, q, x.size)[0]
+    assert np.array_equal(back, x.astype(np.float16).astype(np.float32))
+    # overflow to infinity and non-finite input are rejected
+    assert oracle.quantize_status(oracle.F16, np.array([[7.0e4]], np.float32)) == -5
+    assert oracle.quantize_status(oracle.F16, np.array([[np.inf]], np.float32)) == -5
+
+
+def test_f16_mul_mat_is_the_half_product_in_fp64():
+    """y = sum of fp16(w) * fp16(x) in exact arithmetic, rounded once to fp32."""
+    n_out, n_in, n_tok = 6, 333, 4
+    W = synth.normal(71, (n_out, n_in), 0.05)
+    X = synth.normal(72, (n_tok, n_in), 3.0)
+    Y = oracle.mul_mat(oracle.F16, oracle.quantize(oracle.F16, W), n_out, n_in, X)
+    w16 = W.astype(np.float16).astype(np.float64)
+    x16 = X.astype(np.float16).astype(np.float64)
+    # each product is exact in fp64 (11-bit significands); the fp64 sum carries at most
+    # n_in roundings of 2^-53 relative to the running magnitude
+    ref = x16 @ w16.T
+    mag = np.abs(x16) @ np.abs(w16).T
+    assert np.all(np.abs(Y.astype(np.float64) - ref) <= 2 ** -24 * np.abs(ref) + n_in * 2 ** -52 * mag)
+    with pytest.raises(oracle.OracleError):
+        oracle.block_sums(oracle.F16, oracle.quantize(oracle.F16, W), n_out, n_in,
+                          oracle.quantize(oracle.F16, X), n_tok)
