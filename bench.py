@@ -394,12 +394,14 @@ def other_configs(torch, syn, synth, workloads, stream, l2, hbm_peak, tc_peak, q
     gemv_cfg("q8_0_2048x2048_decode", workloads.Q8_0_SQUARE, 1, 1)
     gemv_cfg("q6_k_lm_head_decode_1tok", workloads.LM_HEAD_1B, 3, 1)
     gemv_cfg("q6_k_lm_head_decode_4tok", workloads.LM_HEAD_1B, 3, 4)
-    # the 32-weight formats Q4_0 / Q5_0 on the Llama-8B FFN up shape
-    for wt, nm in ((workloads.Q4_0, "q4_0"), (workloads.Q5_0, "q5_0")):
-        gemv_cfg(f"{nm}_14336x4096_decode", [workloads.Matrix("ffn_up", wt, 14336, 4096)], 6, 1)
+    # the 32-weight formats Q4_0 / Q5_0 and F16 weights on the Llama-8B FFN up shape
+    for wt, nm in ((workloads.Q4_0, "q4_0"), (workloads.Q5_0, "q5_0"), (workloads.F16, "f16")):
+        gemv_cfg(f"{nm}_14336x4096_decode", [workloads.Matrix("ffn_up", wt, 14336, 4096)],
+                 8 if wt == workloads.F16 else 6, 1)
         m = workloads.Matrix("ffn_up", wt, 14336, 4096)
-        Wp = syn.quantize(wt, torch.from_numpy(synth.weight(7, 0, m.n_out, m.n_in)).cuda())
-        Xp = torch.from_numpy(synth.activations(7, 0, 512, m.n_in)).cuda()
+        wl = 8 if wt == workloads.F16 else 7
+        Wp = syn.quantize(wt, torch.from_numpy(synth.weight(wl, 0, m.n_out, m.n_in)).cuda())
+        Xp = torch.from_numpy(synth.activations(wl, 0, 512, m.n_in)).cuda()
         Yp = torch.empty((512, m.n_out), device="cuda")
         syn.syn_reserve(m.n_in, 512, stream.cuda_stream)
         t = time_calls(torch, stream, lambda c: syn.mul_mat(wt, Wp, m.n_out, m.n_in, Xp, Y=Yp, stream=stream), 1, 4)

@@ -15,7 +15,7 @@ OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsyn.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["api.cu", "quant.cu", "gemv.cu", "gemm.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemv.cu", "gemv_f16.cu", "gemm.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "quant_dev.cuh", "kernels.h"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

@@ -78,15 +78,20 @@ int device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-bool known_type(int t) { return t >= SYN_TYPE_Q8_0 && t <= SYN_TYPE_Q5_0; }
+bool known_type(int t) { return t >= SYN_TYPE_Q8_0 && t <= SYN_TYPE_F16; }
 // weight formats of mul_mat (Q8_K is an activation format only)
 bool is_weight(int t) { return known_type(t) && t != SYN_TYPE_Q8_K; }
 // the vec_dot_type the activations are converted to: Q8_0 for the 32-weight formats,
-// Q8_K for the K-quants ("Products: weights against quantized activations")
-int vec_dot(int t) { return (t == SYN_TYPE_Q4_K || t == SYN_TYPE_Q6_K) ? SYN_TYPE_Q8_K : SYN_TYPE_Q8_0; }
+// Q8_K for the K-quants, F16 for F16 ("Products: weights against quantized activations")
+int vec_dot(int t) {
+    return (t == SYN_TYPE_Q4_K || t == SYN_TYPE_Q6_K) ? SYN_TYPE_Q8_K : t == SYN_TYPE_F16 ? SYN_TYPE_F16 : SYN_TYPE_Q8_0;
+}
+
 
 int64_t elems(int t) { return syn::block_elems(t); }
 int64_t bytes_of(int t) { return syn::block_bytes(t); }
+// F16 rows are read 8 values (16 bytes) at a time
+int64_t row_multiple(int t) { return t == SYN_TYPE_F16 ? 8 : elems(t); }
 
 int check_cuda(cudaError_t e) { return e == cudaSuccess ? SYN_OK : SYN_ERR_CUDA; }
 
@@ -202,7 +207,7 @@ int syn_dequantize(int type, const void* src, float* dst, int64_t n_rows, int64_
 
 int syn_quantize_activations(int wtype, const float* X, int64_t n_tok, int64_t n_in, int8_t* qs, float* d,
                              int16_t* bsums, syn_stream_t stream) {
-    if (!is_weight(wtype)) return SYN_ERR_TYPE;
+    if (!is_weight(wtype) || wtype == SYN_TYPE_F16) return SYN_ERR_TYPE;  // F16: syn_quantize(F16, X)
     const int xt = vec_dot(wtype);
     if (n_tok < 0 || n_in <= 0 || n_in % elems(xt) || n_tok * n_in > kMaxElems) return SYN_ERR_SHAPE;
     if (n_tok == 0) return SYN_OK;
@@ -247,7 +252,7 @@ int syn_release(void) {
 int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in, const float* X, int64_t n_tok, float* Y,
                 syn_stream_t stream) {
     if (!is_weight(type)) return SYN_ERR_TYPE;
-    if (n_out <= 0 || n_in <= 0 || n_tok < 0 || n_in % elems(type) || n_out * n_in > kMaxElems ||
+    if (n_out <= 0 || n_in <= 0 || n_tok < 0 || n_in % row_multiple(type) || n_out * n_in > kMaxElems ||
         n_tok * n_in > kMaxElems || n_tok * n_out > kMaxElems || n_out > (int64_t(1) << 31))
         return SYN_ERR_SHAPE;
     if (n_tok == 0) return SYN_OK;
@@ -257,6 +262,14 @@ int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in, const floa
     int rc = device_state(&st);
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (type == SYN_TYPE_F16 && n_tok <= g_gemv_max_tok.load()) {
+        void* ws;
+        rc = workspace_for(s, (size_t)(n_tok * n_in * 2 + 256), &ws);
+        if (rc) return rc;
+        rc = check_cuda(syn::launch_gemv_f16(W, n_out, n_in, X, n_tok, Y, ws, st->sms, s));
+        if (rc == SYN_OK) g_launches += 2;
+        return rc;
+    }
     if (n_tok <= g_gemv_max_tok.load() && syn::gemv_act_bytes(type, n_in) <= syn::gemv_act_limit()) {
         const syn::GemvDesc d{type, W, n_out, n_in, X, Y};
         void* ws;
@@ -288,7 +301,7 @@ int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_strea
     for (int i = 0; i < n; i++) {
         const syn_mat_desc& d = descs[i];
         if (!is_weight(d.type)) return SYN_ERR_TYPE;
-        if (d.n_out <= 0 || d.n_in <= 0 || n_tok < 0 || d.n_in % elems(d.type) || d.n_out * d.n_in > kMaxElems ||
+        if (d.n_out <= 0 || d.n_in <= 0 || n_tok < 0 || d.n_in % row_multiple(d.type) || d.n_out * d.n_in > kMaxElems ||
             n_tok * d.n_in > kMaxElems || n_tok * d.n_out > kMaxElems || d.n_out > (int64_t(1) << 31))
             return SYN_ERR_SHAPE;
         if (!d.W || !d.X || !d.Y) return SYN_ERR_NULL;
@@ -323,8 +336,8 @@ int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_strea
     };
     for (int i = 0; i < n; i++) {
         const syn_mat_desc& d = descs[i];
-        const int64_t a = syn::gemv_act_bytes(d.type, d.n_in);
-        if (a > syn::gemv_act_limit()) {  // too wide for the decode kernel: the prefill path
+        const int64_t a = d.type == SYN_TYPE_F16 ? 0 : syn::gemv_act_bytes(d.type, d.n_in);
+        if (d.type == SYN_TYPE_F16 || a > syn::gemv_act_limit()) {  // own launch (F16 decode, or too wide)
             rc = syn_mul_mat(d.type, d.W, d.n_out, d.n_in, d.X, n_tok, d.Y, stream);
             if (rc) return rc;
             continue;
@@ -341,7 +354,7 @@ int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_strea
 
 int syn_block_sums(int type, const void* W, int64_t n_out, int64_t n_in, const void* Xq, int64_t n_tok, int32_t* S,
                    syn_stream_t stream) {
-    if (!is_weight(type)) return SYN_ERR_TYPE;
+    if (!is_weight(type) || type == SYN_TYPE_F16) return SYN_ERR_TYPE;  // F16 products are not integer
     if (n_out <= 0 || n_in <= 0 || n_tok < 0 || n_in % elems(type) || n_out * n_in > kMaxElems ||
         n_tok * n_out * (n_in / elems(type)) > kMaxElems)
         return SYN_ERR_SHAPE;

@@ -8,6 +8,7 @@
 //   Q8_K [d f32][q int8 x256][bsums int16 x16]                         292 B
 //   Q4_0 [d f16][qs 16 B: q[l] low nibble, q[l+16] high nibble]       18 B
 //   Q5_0 [d f16][qh u32: bit i = fifth bit of q[i]][qs 16 B as Q4_0]   22 B
+//   F16  one IEEE half per weight                                     2 B
 #pragma once
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -18,6 +19,7 @@
 #define SYN_Q8_K 4
 #define SYN_Q4_0 5
 #define SYN_Q5_0 6
+#define SYN_F16 7
 
 // Device-side error codes written into the library's per-device error word.
 #define SYN_DEVERR_TIMEOUT 1
@@ -39,9 +41,10 @@ template <> struct Fmt<SYN_Q5_0> { static constexpr int elems = 32, bytes = 22; 
 
 // 32-weight formats (vec_dot_type Q8_0)
 __host__ __device__ inline bool small_block(int t) { return t == SYN_Q8_0 || t == SYN_Q4_0 || t == SYN_Q5_0; }
-__host__ __device__ inline int block_elems(int t) { return small_block(t) ? 32 : 256; }
+__host__ __device__ inline int block_elems(int t) { return t == SYN_F16 ? 1 : small_block(t) ? 32 : 256; }
 __host__ __device__ inline int block_bytes(int t) {
-    return t == SYN_Q8_0 ? 34 : t == SYN_Q4_K ? 144 : t == SYN_Q6_K ? 210 : t == SYN_Q8_K ? 292 : t == SYN_Q4_0 ? 18 : 22;
+    return t == SYN_Q8_0 ? 34 : t == SYN_Q4_K ? 144 : t == SYN_Q6_K ? 210 : t == SYN_Q8_K ? 292 : t == SYN_Q4_0 ? 18
+         : t == SYN_Q5_0 ? 22 : 2;
 }
 
 // ---------------------------------------------------------------------------------------

@@ -84,6 +84,11 @@ template <> struct GemmFmt<SYN_Q4_0> : GemmDepth<2, 3, 4> {
 template <> struct GemmFmt<SYN_Q5_0> : GemmDepth<2, 3, 3> {
     static constexpr int BB = 22, SB_BYTES = 176, BOX = 176, ESIZE = 1, RAW_ROW = 192;
 };
+// F16: no raw ring; the weight tile is loaded by TMA straight into the A ring (the same
+// 128-byte-swizzled K-major layout as the activation tiles)
+template <> struct GemmFmt<SYN_F16> : GemmDepth<1, 4, 4> {  // (one raw stage of 0 bytes: unused)
+    static constexpr int BB = 2, SB_BYTES = 512, BOX = 128, ESIZE = 2, RAW_ROW = 0;
+};
 template <> struct GemmFmt<SYN_Q8_0> : GemmDepth<2, 3, 3> {
     static constexpr int BB = 34, SB_BYTES = 272, BOX = 272, ESIZE = 2, RAW_ROW = 288;
 };
@@ -410,7 +415,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             mbar_init(smem_u32(&b_empty[i]), 1);
         }
         for (int i = 0; i < GEMM_A_STAGES; i++) {
-            mbar_init(smem_u32(&a_full[i]), 8);
+            mbar_init(smem_u32(&a_full[i]), T == SYN_F16 ? 1 : 8);
             mbar_init(smem_u32(&a_empty[i]), 1);
         }
         *abort_flag = 0;
@@ -430,7 +435,30 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         return (int)(st < 4 ? st : 4);
     };
 
-    if (warp == 0) {
+    if (warp == 0 && T == SYN_F16) {
+        // ------------------------------ F16 weight tiles ------------------------------
+        // 2-D TMA of 128 rows x 64 k of fp16 straight into the A ring (zero fill past
+        // n_out / n_in)
+        uint32_t kc = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            int m, n, ss0, ss1;
+            unit_coords(p, u, m, n, ss0, ss1);
+            for (int ss = ss0; ss < ss1 && ok; ss++) {
+                const int nst = steps_in(ss);
+                for (int k4 = 0; k4 < nst; k4++, kc++) {
+                    const int ka = kc % GEMM_A_STAGES;
+                    if (!mbar_wait(smem_u32(&a_empty[ka]), ((kc / GEMM_A_STAGES) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
+                    if (lane == 0) {
+                        const uint32_t af = smem_u32(&a_full[ka]);
+                        mbar_arrive_expect_tx(af, (uint32_t)GEMM_A_BYTES);
+                        tma_load_2d(smem_u32(sA + ka * GEMM_A_BYTES), &wmap, ss * GEMM_SUPER + k4 * GEMM_BK, m * GEMM_BM, af);
+                    }
+                    __syncwarp();
+                }
+            }
+        }
+    } else if (warp == 0) {
         // ------------------------------ raw weight producer ------------------------------
         uint32_t rc = 0;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
@@ -573,6 +601,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ac++;
         }
     } else if (warp < GEMM_EPI_WARP0) {
+      if (T != SYN_F16) {  // F16: no dequantization, the weights arrive as fp16
         // ------------------------------ dequantize ------------------------------
         const int dw = warp - GEMM_DEQ_WARP0;
         const int r = 32 * (dw & 3) + lane;   // row of the tile
@@ -629,6 +658,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 rc++;
             }
         }
+      }
     } else {
         // ------------------------------ epilogue ------------------------------
         // TMEM -> registers (32 columns per load); then either through a per-warp staging
@@ -732,14 +762,14 @@ constexpr size_t gemm_smem_bytes() {
 }
 static_assert(gemm_smem_bytes<SYN_Q4_K>() <= 232448 && gemm_smem_bytes<SYN_Q6_K>() <= 232448 &&
                   gemm_smem_bytes<SYN_Q8_0>() <= 232448 && gemm_smem_bytes<SYN_Q4_0>() <= 232448 &&
-                  gemm_smem_bytes<SYN_Q5_0>() <= 232448,
+                  gemm_smem_bytes<SYN_Q5_0>() <= 232448 && gemm_smem_bytes<SYN_F16>() <= 232448,
               "shared memory per CTA exceeds 227 KB");
 template <int T>
 constexpr bool gemm_bars_fit() {
     return 8 * (2 * GemmFmt<T>::RAW_STAGES + 2 * GemmFmt<T>::A_STAGES + 2 * GemmFmt<T>::B_STAGES + 4) + 16 <= 256;
 }
 static_assert(gemm_bars_fit<SYN_Q4_K>() && gemm_bars_fit<SYN_Q6_K>() && gemm_bars_fit<SYN_Q8_0>() &&
-                  gemm_bars_fit<SYN_Q4_0>() && gemm_bars_fit<SYN_Q5_0>(),
+                  gemm_bars_fit<SYN_Q4_0>() && gemm_bars_fit<SYN_Q5_0>() && gemm_bars_fit<SYN_F16>(),
               "barrier area");
 
 #ifndef SYN_GEMM_SPLIT_PENALTY
@@ -844,12 +874,22 @@ cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, co
     case SYN_Q8_0: box_bytes = GemmFmt<SYN_Q8_0>::BOX; esize = GemmFmt<SYN_Q8_0>::ESIZE; raw_row = GemmFmt<SYN_Q8_0>::RAW_ROW; break;
     case SYN_Q4_0: box_bytes = GemmFmt<SYN_Q4_0>::BOX; esize = GemmFmt<SYN_Q4_0>::ESIZE; raw_row = GemmFmt<SYN_Q4_0>::RAW_ROW; break;
     case SYN_Q5_0: box_bytes = GemmFmt<SYN_Q5_0>::BOX; esize = GemmFmt<SYN_Q5_0>::ESIZE; raw_row = GemmFmt<SYN_Q5_0>::RAW_ROW; break;
+    case SYN_F16: box_bytes = 0; esize = 2; raw_row = 0; break;
     default: return cudaErrorInvalidValue;
     }
     CUtensorMap wmap = map;  // placeholder when unused
     p.raw_tma = 0;
     p.raw_row = raw_row;
-    if (p.row_bytes % 16 == 0 && p.row_bytes < (int64_t(1) << 31)) {
+    if (type == SYN_F16) {
+        // fp16 rows (n_in % 8 == 0): 64-k x 128-row boxes, 128-byte swizzle, as the A tile
+        cuuint64_t wdims[2] = {(cuuint64_t)n_in, (cuuint64_t)n_out};
+        cuuint64_t wstrides[1] = {(cuuint64_t)n_in * 2};
+        cuuint32_t wbox[2] = {(cuuint32_t)GEMM_BK, (cuuint32_t)GEMM_BM};
+        cr = encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(W), wdims, wstrides, wbox, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    } else if (p.row_bytes % 16 == 0 && p.row_bytes < (int64_t(1) << 31)) {
         cuuint64_t wdims[2] = {(cuuint64_t)(p.row_bytes / esize), (cuuint64_t)n_out};
         cuuint64_t wstrides[1] = {(cuuint64_t)p.row_bytes};
         cuuint32_t wbox[2] = {(cuuint32_t)(box_bytes / esize), (cuuint32_t)GEMM_BM};
@@ -880,6 +920,7 @@ cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, co
     case SYN_Q8_0: return run_gemm<SYN_Q8_0>(p, map, wmap, ymap, sms, s);
     case SYN_Q4_0: return run_gemm<SYN_Q4_0>(p, map, wmap, ymap, sms, s);
     case SYN_Q5_0: return run_gemm<SYN_Q5_0>(p, map, wmap, ymap, sms, s);
+    case SYN_F16: return run_gemm<SYN_F16>(p, map, wmap, ymap, sms, s);
     default: return cudaErrorInvalidValue;
     }
 }

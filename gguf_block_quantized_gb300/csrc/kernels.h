@@ -47,6 +47,12 @@ cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, co
                         int64_t n_tok, float* Y, int* err, int sms, cudaStream_t s);
 bool gemm_needs_zero(int64_t n_out, int64_t n_in, int64_t n_tok, int sms);
 
+// F16 weights (n_in % 8 == 0): X -> fp16 (round to nearest even) into xh, and the decode
+// product reading W and the fp16 activations from ws (n_tok * n_in halves).
+cudaError_t launch_x_to_half(const float* X, int64_t n, void* xh, int sms, cudaStream_t s);
+cudaError_t launch_gemv_f16(const void* W, int64_t n_out, int64_t n_in, const float* X, int64_t n_tok, float* Y,
+                            void* ws, int sms, cudaStream_t s);
+
 // Adds n to the count syn_launch_count reports.
 void note_launches(int n);
 

@@ -65,7 +65,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 extern "C" int syn_mul_mat_prefill_static(int type, const void* W, int64_t n_out, int64_t n_in, const float* X,
                                           int64_t n_tok, float* Y, syn_stream_t stream) {
-    if (type < SYN_TYPE_Q8_0 || type > SYN_TYPE_Q5_0 || type == SYN_TYPE_Q8_K) return SYN_ERR_TYPE;
+    if (type < SYN_TYPE_Q8_0 || type > SYN_TYPE_F16 || type == SYN_TYPE_Q8_K) return SYN_ERR_TYPE;
     const int64_t be = syn::block_elems(type);
     if (n_out <= 0 || n_in <= 0 || n_tok < 0 || n_in % be || n_out > (int64_t(1) << 31) ||
         n_out * n_in > (int64_t(1) << 40) || n_tok * n_out > (int64_t(1) << 40))
@@ -82,7 +82,8 @@ extern "C" int syn_mul_mat_prefill_static(int type, const void* W, int64_t n_out
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int* err = reinterpret_cast<int*>(d->scratch);
     void* xh = d->scratch + kHeader;
-    const int xt = (type == SYN_TYPE_Q4_K || type == SYN_TYPE_Q6_K) ? SYN_TYPE_Q8_K : SYN_TYPE_Q8_0;
+    const int xt = (type == SYN_TYPE_Q4_K || type == SYN_TYPE_Q6_K) ? SYN_TYPE_Q8_K
+                 : type == SYN_TYPE_F16 ? SYN_TYPE_F16 : SYN_TYPE_Q8_0;
     if (syn::gemm_needs_zero(n_out, n_in, n_tok, d->sms) &&
         cudaMemsetAsync(Y, 0, (size_t)n_tok * n_out * sizeof(float), s) != cudaSuccess)
         return SYN_ERR_CUDA;

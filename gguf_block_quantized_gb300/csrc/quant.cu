@@ -448,6 +448,29 @@ __global__ void k_block_sums(const uint8_t* __restrict__ W, int64_t n_out, int64
 }
 
 // ---------------------------------------------------------------------------------------
+// F16 weights: the IEEE half of each value (round to nearest even); non-finite input or an
+// overflow to infinity sets the range flag
+// ---------------------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) k_quantize_f16(const float* __restrict__ src, __half* __restrict__ dst,
+                                                      int64_t n, int* __restrict__ range_err) {
+    bool ok = true;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float x = src[i];
+        const __half h = __float2half_rn(x);
+        ok &= isfinite(x) && !__hisinf(h);
+        dst[i] = h;
+    }
+    if (!__all_sync(0xffffffffu, ok) && (threadIdx.x & 31) == 0) atomicExch(range_err, 1);
+}
+
+__global__ void __launch_bounds__(256) k_dequantize_f16(const __half* __restrict__ src, float* __restrict__ dst,
+                                                        int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = __half2float(src[i]);
+}
+
+// ---------------------------------------------------------------------------------------
 // host launchers
 // ---------------------------------------------------------------------------------------
 
@@ -460,6 +483,11 @@ static int grid_for(int64_t warps_needed, int sms) {
 
 cudaError_t launch_quantize(int type, const float* src, void* dst, int64_t n_blocks, int* range_err,
                             int sms, cudaStream_t s) {
+    if (type == SYN_F16) {
+        k_quantize_f16<<<grid_for((n_blocks + 31) / 32, sms), 256, 0, s>>>(src, static_cast<__half*>(dst), n_blocks,
+                                                                          range_err);
+        return cudaGetLastError();
+    }
     int64_t warps = small_block(type) ? (n_blocks + 3) / 4 : n_blocks;
     int g = grid_for(warps, sms);
     uint8_t* d = static_cast<uint8_t*>(dst);
@@ -477,6 +505,11 @@ cudaError_t launch_quantize(int type, const float* src, void* dst, int64_t n_blo
 
 cudaError_t launch_dequantize(int type, const void* src, float* dst, int64_t n_blocks, int sms,
                               cudaStream_t s) {
+    if (type == SYN_F16) {
+        k_dequantize_f16<<<grid_for((n_blocks + 31) / 32, sms), 256, 0, s>>>(static_cast<const __half*>(src), dst,
+                                                                            n_blocks);
+        return cudaGetLastError();
+    }
     int64_t warps = small_block(type) ? (n_blocks + 3) / 4 : n_blocks;
     int g = grid_for(warps, sms);
     const uint8_t* p = static_cast<const uint8_t*>(src);
@@ -503,6 +536,7 @@ cudaError_t launch_quantize_act(int xtype, const float* X, int64_t n_blocks, int
 
 cudaError_t launch_act_half(int xtype, const float* X, int64_t n_blocks, void* xh, int sms,
                             cudaStream_t s) {
+    if (xtype == SYN_F16) return launch_x_to_half(X, n_blocks, xh, sms, s);  // F16: rounding only
     int64_t warps = (xtype == SYN_Q8_0) ? (n_blocks + 3) / 4 : n_blocks;
     int g = grid_for(warps, sms);
     __half* h = static_cast<__half*>(xh);

@@ -15,14 +15,14 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libsyn.so")
 
-Q8_0, Q4_K, Q6_K, Q8_K, Q4_0, Q5_0 = 1, 2, 3, 4, 5, 6
+Q8_0, Q4_K, Q6_K, Q8_K, Q4_0, Q5_0, F16 = 1, 2, 3, 4, 5, 6, 7
 OK, ERR_TYPE, ERR_SHAPE, ERR_NULL, ERR_ALIGN, ERR_RANGE, ERR_CUDA, ERR_TIMEOUT, ERR_NOMEM, ERR_DEVICE = \
     0, -1, -2, -3, -4, -5, -6, -7, -8, -9
 ERR_TOO_LARGE = -10
 STATIC_SCRATCH_BYTES = 32 << 20
-BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, Q8_K: 256, Q4_0: 32, Q5_0: 32}
-BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, Q8_K: 292, Q4_0: 18, Q5_0: 22}
-VEC_DOT_TYPE = {Q8_0: Q8_0, Q4_K: Q8_K, Q6_K: Q8_K, Q4_0: Q8_0, Q5_0: Q8_0}
+BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, Q8_K: 256, Q4_0: 32, Q5_0: 32, F16: 1}
+BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, Q8_K: 292, Q4_0: 18, Q5_0: 22, F16: 2}
+VEC_DOT_TYPE = {Q8_0: Q8_0, Q4_K: Q8_K, Q6_K: Q8_K, Q4_0: Q8_0, Q5_0: Q8_0, F16: F16}
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libsyn.so is not built ({LIB_PATH}); run "

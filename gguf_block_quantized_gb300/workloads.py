@@ -1,7 +1,7 @@
 """The benchmark and parity workloads: matrix shapes and weight formats.
 
 Format codes are the library's own (1 = Q8_0, 2 = Q4_K, 3 = Q6_K, 4 = Q8_K, 5 = Q4_0,
-6 = Q5_0).
+6 = Q5_0, 7 = F16).
 The Q4_K_M mix follows "The GGML ecosystem, and where synapse fits", section 3
 (llama-quantize): most matrices Q4_K; attn_v and ffn_down Q6_K in the first and last
 eighth of the layers and every third layer between them.
@@ -10,10 +10,10 @@ from __future__ import annotations
 
 from dataclasses import dataclass
 
-Q8_0, Q4_K, Q6_K, Q8_K, Q4_0, Q5_0 = 1, 2, 3, 4, 5, 6
-TYPE_NAMES = {Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K", Q8_K: "Q8_K", Q4_0: "Q4_0", Q5_0: "Q5_0"}
-BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, Q8_K: 256, Q4_0: 32, Q5_0: 32}
-BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, Q8_K: 292, Q4_0: 18, Q5_0: 22}
+Q8_0, Q4_K, Q6_K, Q8_K, Q4_0, Q5_0, F16 = 1, 2, 3, 4, 5, 6, 7
+TYPE_NAMES = {Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K", Q8_K: "Q8_K", Q4_0: "Q4_0", Q5_0: "Q5_0", F16: "F16"}
+BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, Q8_K: 256, Q4_0: 32, Q5_0: 32, F16: 1}
+BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, Q8_K: 292, Q4_0: 18, Q5_0: 22, F16: 2}
 
 
 @dataclass(frozen=True)

@@ -52,10 +52,12 @@ typedef struct CUstream_st* syn_stream_t; /* identical to cudaStream_t */
  *   Q4_0  32 weights,  18 B: fp16 d, 32 4-bit q;                      w = d*(q - 8)
  *   Q5_0  32 weights,  22 B: fp16 d, 32-bit qh (each q's fifth bit), 32 4-bit low parts;
  *                                                                     w = d*(q - 16)
+ *   F16   1 weight,     2 B: IEEE binary16 (round to nearest even from fp32)
  * In-block byte order: the public GGUF layout (fields in the order listed above; Q4_0/Q5_0
  * store q[l] in the low and q[l+16] in the high nibble of byte l).
  * vec_dot_type (the activation format of the product): Q8_0 for Q8_0, Q4_0 and Q5_0; Q8_K
- * for Q4_K and Q6_K. */
+ * for Q4_K and Q6_K; F16 for F16 (the activations rounded to fp16; products exact, fp32 sums;
+ * mul_mat needs n_in % 8 == 0 for F16 weights). */
 enum {
     SYN_TYPE_Q8_0 = 1,
     SYN_TYPE_Q4_K = 2,
@@ -63,6 +65,7 @@ enum {
     SYN_TYPE_Q8_K = 4,
     SYN_TYPE_Q4_0 = 5,
     SYN_TYPE_Q5_0 = 6,
+    SYN_TYPE_F16 = 7,
 };
 
 enum {
@@ -79,7 +82,7 @@ enum {
     SYN_ERR_TOO_LARGE = -10, /* the problem needs more than the fixed scratch array holds */
 };
 
-/* Elements per block: 32 (Q8_0, Q4_0, Q5_0) or 256 (Q4_K, Q6_K, Q8_K); -1 for an unknown type. */
+/* Elements per block: 32 (Q8_0, Q4_0, Q5_0), 256 (Q4_K, Q6_K, Q8_K) or 1 (F16); -1 for an unknown type. */
 SYN_API int64_t syn_block_elems(int type);
 
 /* Bytes per block: 34, 144, 210, 292; -1 for an unknown type. */
@@ -90,7 +93,7 @@ SYN_API int64_t syn_block_bytes(int type);
 SYN_API int64_t syn_row_bytes(int type, int64_t n);
 
 /* Quantize n_rows rows of n_per_row fp32 values (src, row-major, contiguous) into blocks
- * (dst, n_rows * syn_row_bytes bytes).  type: Q8_0, Q4_K, Q6_K, Q8_K, Q4_0 or Q5_0.
+ * (dst, n_rows * syn_row_bytes bytes).  type: Q8_0, Q4_K, Q6_K, Q8_K, Q4_0, Q5_0 or F16.
  * Encoders (plain readings of the format table; bit-exact with the CPU oracle):
  *   Q8_0  d = fp16(amax/127); q = clamp(round(x / d_stored), -127, 127)
  *   Q8_K  d = amax/127 (fp32); q = clamp(round(x / d), -127, 127); bsums = sums of 16 q
@@ -102,6 +105,7 @@ SYN_API int64_t syn_row_bytes(int type, int64_t n);
  *   Q4_0  m = the block's value of largest magnitude (first one), d = fp16(m / -8),
  *         q = clamp(round(x / d) + 8, 0, 15)
  *   Q5_0  d = fp16(m / -16), q = clamp(round(x / d) + 16, 0, 31)
+ *   F16   the IEEE half of x (an overflow to infinity is a range error)
  * round = ties away from zero; a zero scale gives zero codes (Q4_0/Q5_0: q = 8 / 16).
  * Returns SYN_ERR_RANGE if any input is NaN/Inf or a scale overflows fp16; to report
  * that, this call SYNCHRONIZES `stream` before returning (it is an offline operation).
@@ -112,7 +116,7 @@ SYN_API int syn_quantize(int type, const float* src, void* dst, int64_t n_rows, 
 
 /* Expand blocks back to fp32 ("dequantize_row_*", same page, section 5): dst gets
  * n_rows * n_per_row floats.  Q8_0: d*q; Q4_K: (d*sc)*q - (dmin*mn); Q6_K:
- * (d*sc)*(q-32); Q8_K: d*q; Q4_0: d*(q-8); Q5_0: d*(q-16) — each product and difference
+ * (d*sc)*(q-32); Q8_K: d*q; Q4_0: d*(q-8); Q5_0: d*(q-16); F16: the value — each product and difference
  * one fp32 rounding, no FMA,
  * so the result is bit-exact with the CPU oracle.  Asynchronous.  Alignment: 16 B. */
 SYN_API int syn_dequantize(int type, const void* src, float* dst, int64_t n_rows, int64_t n_per_row,
@@ -128,7 +132,7 @@ SYN_API int syn_quantize_activations(int wtype, const float* X, int64_t n_tok, i
                              int8_t* qs, float* d, int16_t* bsums, syn_stream_t stream);
 
 /* Y = ggml_mul_mat(W, X) as described at the top of this file.
- * type: Q8_0, Q4_K, Q6_K, Q4_0 or Q5_0 (Q8_K is activation-only: SYN_ERR_TYPE).
+ * type: Q8_0, Q4_K, Q6_K, Q4_0, Q5_0 or F16 (Q8_K is activation-only: SYN_ERR_TYPE).
  * n_tok <= the decode threshold (default 8, see syn_set_gemv_max_tok) runs the decode
  * kernel: one launch that quantizes X in shared memory and streams W once per group of
  * up to 8 tokens.  Larger n_tok runs the prefill path: one kernel quantizes X and writes

@@ -57,7 +57,7 @@ def test_argument_checks_need_no_gpu(lib):
     L = lib
     p = 1 << 20  # any aligned non-null value: the checks below reject before any use
     assert L.syn_mul_mat(4, p, 4, 256, p, 1, p, None) == L.ERR_TYPE      # Q8_K weights
-    assert L.syn_mul_mat(7, p, 4, 256, p, 1, p, None) == L.ERR_TYPE
+    assert L.syn_mul_mat(8, p, 4, 256, p, 1, p, None) == L.ERR_TYPE  # unknown format
     assert L.syn_mul_mat(2, p, 4, 100, p, 1, p, None) == L.ERR_SHAPE
     assert L.syn_mul_mat(2, p, 0, 256, p, 1, p, None) == L.ERR_SHAPE
     assert L.syn_mul_mat(2, p, 4, 256, p, -1, p, None) == L.ERR_SHAPE
@@ -65,7 +65,9 @@ def test_argument_checks_need_no_gpu(lib):
     assert L.syn_mul_mat(2, None, 4, 256, p, 1, p, None) == L.ERR_NULL
     assert L.syn_mul_mat(2, p + 4, 4, 256, p, 1, p, None) == L.ERR_ALIGN
     assert L.syn_quantize(2, p, p, 1, 255, None) == L.ERR_SHAPE
-    assert L.syn_quantize(7, p, p, 1, 256, None) == L.ERR_TYPE  # unknown format
+    assert L.syn_quantize(8, p, p, 1, 256, None) == L.ERR_TYPE  # unknown format
+    assert L.syn_mul_mat(7, p, 4, 100, p, 1, p, None) == L.ERR_SHAPE  # F16 rows: n_in % 8
+    assert L.syn_quantize_activations(7, p, 1, 256, p, p, p, None) == L.ERR_TYPE  # F16: no integer form
     assert L.syn_quantize(1, p, p, 0, 32, None) == L.OK
     assert L.syn_quantize(1, p + 8, p, 1, 32, None) == L.ERR_ALIGN
     assert L.syn_dequantize(3, None, p, 1, 256, None) == L.ERR_NULL

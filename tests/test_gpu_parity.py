@@ -400,3 +400,46 @@ def test_full_qx_0_decode(syn, wt):
 @pytest.mark.parametrize("wt", [oracle.Q4_0, oracle.Q5_0])
 def test_full_qx_0_prefill(syn, wt):
     sampled_check(syn, workloads.Matrix("ffn_up", wt, 14336, 4096), 512, 7, 0, n_rows=48, n_toks=6)
+
+
+# ----------------------------------------------------------------------------------------
+# F16 weights (vec_dot_type F16): conversion bit-exact, products against the oracle
+# ----------------------------------------------------------------------------------------
+
+def test_f16_quantize_dequantize_bit_exact(syn):
+    x = inputs_mixed(37, 520, 11)
+    want = oracle.quantize(oracle.F16, x)
+    got = host(syn.quantize(oracle.F16, dev(x)))
+    assert np.array_equal(got, want)
+    back = host(syn.dequantize(oracle.F16, dev(want), 520))
+    assert np.array_equal(back.view(np.uint32), oracle.dequantize(oracle.F16, want, 520).view(np.uint32))
+    with pytest.raises(syn.SynError):
+        syn.quantize(oracle.F16, dev(np.full((1, 8), 1e6, np.float32)))
+
+
+@pytest.mark.parametrize("shape", [(1, 8, 1), (77, 520, 1), (300, 2048, 3), (129, 4096, 8), (64, 1000, 40),
+                                   (257, 768, 300), (128, 256, 16)])
+@pytest.mark.parametrize("path", ["gemv", "gemm"])
+def test_f16_mul_mat(syn, shape, path):
+    n_out, n_in, n_tok = shape
+    Y, ref, bound = run_mul_mat(syn, oracle.F16, n_out, n_in, n_tok, 3000 + n_out, path)
+    assert_close(Y, ref, bound, f"f16 {shape} {path}")
+
+
+def test_f16_in_a_batch(syn):
+    items, refs = [], []
+    for i, (wt, n_out, n_in) in enumerate([(oracle.F16, 100, 1024), (oracle.Q4_K, 64, 512), (oracle.F16, 33, 72)]):
+        Wq = oracle.quantize(wt, synth.normal(700 + i, (n_out, n_in), 0.02))
+        X = synth.normal(800 + i, (2, n_in))
+        items.append((wt, dev(Wq), n_out, n_in, dev(X), torch.full((2, n_out), float("nan"), device="cuda")))
+        refs.append((oracle.mul_mat(wt, Wq, n_out, n_in, X), tolerance(wt, Wq, n_in, X)))
+    syn.mul_mat_batch(items, 2)
+    for (wt, _, n_out, n_in, _, Yd), (ref, bound) in zip(items, refs):
+        assert_close(host(Yd), ref, bound, f"batch {oracle.NAMES[wt]} {n_out}x{n_in}")
+    assert syn.device_status() == syn.OK
+
+
+@pytest.mark.parametrize("n_tok", [1, 512])
+def test_full_f16(syn, n_tok):
+    sampled_check(syn, workloads.Matrix("ffn_up", oracle.F16, 14336, 4096), n_tok, 8, 0, n_rows=96, n_toks=4,
+                  path="gemv" if n_tok == 1 else "gemm")
