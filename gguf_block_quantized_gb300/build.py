@@ -1,4 +1,5 @@
-"""Builds libsyn.so in-tree from csrc/*.cu for sm_103a (nvcc, one process per source file).
+"""Builds libsyn.so in-tree from csrc/*.cu (and the host-only gguf.cpp) for sm_103a (nvcc, one
+process per source file).
 
     python -m gguf_block_quantized_gb300.build [--force]
 """
@@ -15,7 +16,7 @@ OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsyn.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["api.cu", "quant.cu", "gemv.cu", "gemv_f16.cu", "gemm.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemv.cu", "gemv_f16.cu", "gemm.cu", "noalloc.cu", "gguf.cpp"]
 HEADERS = ["common.cuh", "quant_dev.cuh", "kernels.h"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
@@ -35,7 +36,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     procs, objs = [], []
     for src in SOURCES:
         sp = os.path.join(CSRC, src)
-        op = os.path.join(OBJ, src.replace(".cu", ".o"))
+        op = os.path.join(OBJ, os.path.splitext(src)[0] + ".o")
         objs.append(op)
         if force or _mtime(op) < max(_mtime(sp), newest_dep):
             cmd = [NVCC, *ARCH, *FLAGS, "-c", sp, "-o", op]

@@ -154,6 +154,9 @@ const char* syn_strerror(int status) {
     case SYN_ERR_NOMEM: return "out of device memory";
     case SYN_ERR_DEVICE: return "device is not sm_103 (GB300)";
     case SYN_ERR_TOO_LARGE: return "problem larger than the fixed scratch array";
+    case SYN_ERR_FORMAT: return "malformed GGUF file";
+    case SYN_ERR_IO: return "file could not be opened, mapped or written";
+    case SYN_ERR_NOTFOUND: return "no such GGUF key or tensor";
     default: return "unknown status";
     }
 }

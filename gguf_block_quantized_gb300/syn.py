@@ -19,6 +19,12 @@ Q8_0, Q4_K, Q6_K, Q8_K, Q4_0, Q5_0, F16 = 1, 2, 3, 4, 5, 6, 7
 OK, ERR_TYPE, ERR_SHAPE, ERR_NULL, ERR_ALIGN, ERR_RANGE, ERR_CUDA, ERR_TIMEOUT, ERR_NOMEM, ERR_DEVICE = \
     0, -1, -2, -3, -4, -5, -6, -7, -8, -9
 ERR_TOO_LARGE = -10
+ERR_FORMAT, ERR_IO, ERR_NOTFOUND = -11, -12, -13
+# GGUF metadata value types and ggml tensor element types (include/syn.h)
+GGUF_UINT8, GGUF_INT8, GGUF_UINT16, GGUF_INT16, GGUF_UINT32, GGUF_INT32, GGUF_FLOAT32, GGUF_BOOL, \
+    GGUF_STRING, GGUF_ARRAY, GGUF_UINT64, GGUF_INT64, GGUF_FLOAT64 = range(13)
+GGML_F32, GGML_F16, GGML_Q4_0, GGML_Q5_0, GGML_Q8_0, GGML_Q4_K, GGML_Q6_K, GGML_Q8_K, GGML_BF16 = \
+    0, 1, 2, 6, 8, 12, 14, 15, 30
 STATIC_SCRATCH_BYTES = 32 << 20
 BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, Q8_K: 256, Q4_0: 32, Q5_0: 32, F16: 1}
 BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, Q8_K: 292, Q4_0: 18, Q5_0: 22, F16: 2}
@@ -57,6 +63,38 @@ class MatDesc(ctypes.Structure):
 
 
 EXPORTS.append(("syn_mul_mat_batch", _i32, [_i32, ctypes.POINTER(MatDesc), _i64, _vp]))
+
+_u32, _u64, _cp = ctypes.c_uint32, ctypes.c_uint64, ctypes.c_char_p
+_P = ctypes.POINTER
+EXPORTS += [
+    ("syn_gguf_open", _vp, [_cp, _P(_i32)]),
+    ("syn_gguf_close", None, [_vp]),
+    ("syn_gguf_version", _i64, [_vp]),
+    ("syn_gguf_n_tensors", _i64, [_vp]),
+    ("syn_gguf_n_kv", _i64, [_vp]),
+    ("syn_gguf_alignment", _i64, [_vp]),
+    ("syn_gguf_data_start", _i64, [_vp]),
+    ("syn_gguf_find_tensor", _i64, [_vp, _cp]),
+    ("syn_gguf_tensor_info", _i32, [_vp, _i64, _P(_cp), _P(_u32), _P(_i32), _P(_i64), _P(_u64), _P(_vp),
+                                    _P(_i64)]),
+    ("syn_gguf_matrix", _i32, [_vp, _cp, _P(_i32), _P(_i64), _P(_i64), _P(_vp), _P(_i64)]),
+    ("syn_gguf_upload", _i32, [_vp, _i64, _vp, _i64, _vp]),
+    ("syn_gguf_kv_info", _i32, [_vp, _i64, _P(_cp), _P(_u32), _P(_u32), _P(_u64)]),
+    ("syn_gguf_get_int", _i32, [_vp, _cp, _P(_i64)]),
+    ("syn_gguf_get_float", _i32, [_vp, _cp, _P(ctypes.c_double)]),
+    ("syn_gguf_get_string", _i32, [_vp, _cp, _P(_vp), _P(_i64)]),
+    ("syn_gguf_get_array", _i32, [_vp, _cp, _P(_u32), _P(_u64), _P(_vp)]),
+    ("syn_gguf_get_array_string", _i32, [_vp, _cp, _u64, _P(_vp), _P(_i64)]),
+    ("syn_gguf_writer_begin", _vp, [_cp, _u32]),
+    ("syn_gguf_writer_kv_int", _i32, [_vp, _cp, _u32, _i64]),
+    ("syn_gguf_writer_kv_float", _i32, [_vp, _cp, _u32, ctypes.c_double]),
+    ("syn_gguf_writer_kv_string", _i32, [_vp, _cp, _cp, _i64]),
+    ("syn_gguf_writer_kv_array", _i32, [_vp, _cp, _u32, _u64, _vp]),
+    ("syn_gguf_writer_kv_string_array", _i32, [_vp, _cp, _u64, _P(_cp), _P(_i64)]),
+    ("syn_gguf_writer_add_tensor", _i32, [_vp, _cp, _u32, _i32, _P(_i64), _vp, _i64]),
+    ("syn_gguf_writer_finish", _i32, [_vp]),
+    ("syn_gguf_writer_abort", None, [_vp]),
+]
 
 for _name, _res, _args in EXPORTS:
     _f = getattr(_L, _name)
@@ -171,3 +209,153 @@ def device_status(clear: bool = True) -> int:
 
 def launch_count() -> int:
     return int(syn_launch_count())
+
+
+# ----------------------------------------------------------------------------------------
+# GGUF helpers (host side; the tensors come back as numpy views of the mapping)
+# ----------------------------------------------------------------------------------------
+
+class GGUFReader:
+    """An open GGUF file (syn_gguf_open); ``close()`` unmaps it and invalidates every view."""
+
+    def __init__(self, path: str):
+        st = ctypes.c_int(0)
+        self.h = syn_gguf_open(os.fsencode(path), ctypes.byref(st))
+        if not self.h:
+            raise SynError(st.value, f"syn_gguf_open({path})")
+
+    def close(self) -> None:
+        if self.h:
+            syn_gguf_close(self.h)
+            self.h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    version = property(lambda self: int(syn_gguf_version(self.h)))
+    alignment = property(lambda self: int(syn_gguf_alignment(self.h)))
+    data_start = property(lambda self: int(syn_gguf_data_start(self.h)))
+    n_tensors = property(lambda self: int(syn_gguf_n_tensors(self.h)))
+    n_kv = property(lambda self: int(syn_gguf_n_kv(self.h)))
+
+    def tensor(self, i: int) -> dict:
+        """name, ggml type, ne (n_dims values), offset, nbytes and a uint8 numpy view (or None)."""
+        import numpy as np
+        name, gt, nd = _cp(), _u32(), _i32()
+        ne, off, data, nb = (_i64 * 4)(), _u64(), _vp(), _i64()
+        check(syn_gguf_tensor_info(self.h, i, ctypes.byref(name), ctypes.byref(gt), ctypes.byref(nd), ne,
+                                   ctypes.byref(off), ctypes.byref(data), ctypes.byref(nb)), "syn_gguf_tensor_info")
+        view = None
+        if nb.value >= 0:
+            view = np.ctypeslib.as_array((ctypes.c_uint8 * nb.value).from_address(data.value)) if nb.value else \
+                np.zeros(0, np.uint8)
+        return {"name": name.value.decode(), "ggml_type": gt.value, "ne": list(ne[:nd.value]),
+                "offset": off.value, "nbytes": nb.value, "data": view}
+
+    def find(self, name: str) -> int:
+        return int(syn_gguf_find_tensor(self.h, name.encode()))
+
+    def matrix(self, name: str):
+        """(syn type, n_out, n_in, host address, nbytes) of a mul_mat weight."""
+        t, n_out, n_in, data, nb = _i32(), _i64(), _i64(), _vp(), _i64()
+        check(syn_gguf_matrix(self.h, name.encode(), ctypes.byref(t), ctypes.byref(n_out), ctypes.byref(n_in),
+                              ctypes.byref(data), ctypes.byref(nb)), f"syn_gguf_matrix({name})")
+        return t.value, n_out.value, n_in.value, data.value, nb.value
+
+    def upload(self, name: str, stream=None):
+        """The tensor's bytes copied into a new uint8 CUDA tensor (syn_gguf_upload)."""
+        torch = _torch()
+        i = self.find(name)
+        if i < 0:
+            raise SynError(ERR_NOTFOUND, f"syn_gguf_upload({name})")
+        nb = self.tensor(i)["nbytes"]
+        if nb < 0:
+            raise SynError(ERR_TYPE, f"syn_gguf_upload({name})")
+        dst = torch.empty(max(nb, 1), dtype=torch.uint8, device="cuda")
+        check(syn_gguf_upload(self.h, i, _ptr(dst), dst.numel(), _stream(stream)), f"syn_gguf_upload({name})")
+        return dst[:nb]
+
+    def kv_info(self, i: int):
+        key, vt, et, n = _cp(), _u32(), _u32(), _u64()
+        check(syn_gguf_kv_info(self.h, i, ctypes.byref(key), ctypes.byref(vt), ctypes.byref(et), ctypes.byref(n)),
+              "syn_gguf_kv_info")
+        return key.value.decode(), vt.value, et.value, n.value
+
+    def get_int(self, key: str) -> int:
+        v = _i64()
+        check(syn_gguf_get_int(self.h, key.encode(), ctypes.byref(v)), f"syn_gguf_get_int({key})")
+        return v.value
+
+    def get_float(self, key: str) -> float:
+        v = ctypes.c_double()
+        check(syn_gguf_get_float(self.h, key.encode(), ctypes.byref(v)), f"syn_gguf_get_float({key})")
+        return v.value
+
+    def get_string(self, key: str) -> bytes:
+        p, n = _vp(), _i64()
+        check(syn_gguf_get_string(self.h, key.encode(), ctypes.byref(p), ctypes.byref(n)), f"syn_gguf_get_string({key})")
+        return ctypes.string_at(p.value, n.value) if n.value else b""
+
+    def get_array(self, key: str):
+        """(element type, count, raw little-endian bytes) of a scalar array."""
+        et, n, p = _u32(), _u64(), _vp()
+        check(syn_gguf_get_array(self.h, key.encode(), ctypes.byref(et), ctypes.byref(n), ctypes.byref(p)),
+              f"syn_gguf_get_array({key})")
+        return et.value, n.value, p.value
+
+    def get_array_string(self, key: str, j: int) -> bytes:
+        p, n = _vp(), _i64()
+        check(syn_gguf_get_array_string(self.h, key.encode(), j, ctypes.byref(p), ctypes.byref(n)),
+              f"syn_gguf_get_array_string({key}, {j})")
+        return ctypes.string_at(p.value, n.value) if n.value else b""
+
+
+class GGUFWriter:
+    """syn_gguf_writer_*: entries are written in call order by ``finish()``."""
+
+    def __init__(self, path: str, alignment: int = 32):
+        self.h = syn_gguf_writer_begin(os.fsencode(path), alignment)
+        if not self.h:
+            raise SynError(ERR_SHAPE, f"syn_gguf_writer_begin({path}, {alignment})")
+
+    def kv_int(self, key: str, value_type: int, value: int) -> None:
+        check(syn_gguf_writer_kv_int(self.h, key.encode(), value_type, value), f"kv_int({key})")
+
+    def kv_float(self, key: str, value_type: int, value: float) -> None:
+        check(syn_gguf_writer_kv_float(self.h, key.encode(), value_type, value), f"kv_float({key})")
+
+    def kv_string(self, key: str, value: bytes) -> None:
+        check(syn_gguf_writer_kv_string(self.h, key.encode(), value, len(value)), f"kv_string({key})")
+
+    def kv_array(self, key: str, elem_type: int, values) -> None:
+        """values: a numpy array of the element type's width (its bytes are written as they are)."""
+        import numpy as np
+        a = np.ascontiguousarray(values)
+        check(syn_gguf_writer_kv_array(self.h, key.encode(), elem_type, a.size, a.ctypes.data if a.size else None),
+              f"kv_array({key})")
+
+    def kv_string_array(self, key: str, values) -> None:
+        n = len(values)
+        strs = (_cp * max(n, 1))(*values)
+        lens = (_i64 * max(n, 1))(*[len(v) for v in values])
+        check(syn_gguf_writer_kv_string_array(self.h, key.encode(), n, strs, lens), f"kv_string_array({key})")
+
+    def add_tensor(self, name: str, ggml_type: int, ne, data) -> None:
+        """data: a numpy array holding the tensor's bytes (any dtype, C-contiguous)."""
+        import numpy as np
+        a = np.ascontiguousarray(data)
+        arr = (_i64 * len(ne))(*ne)
+        check(syn_gguf_writer_add_tensor(self.h, name.encode(), ggml_type, len(ne), arr,
+                                         a.ctypes.data if a.nbytes else None, a.nbytes), f"add_tensor({name})")
+
+    def finish(self) -> None:
+        h, self.h = self.h, None
+        check(syn_gguf_writer_finish(h), "syn_gguf_writer_finish")
+
+    def abort(self) -> None:
+        if self.h:
+            syn_gguf_writer_abort(self.h)
+            self.h = None

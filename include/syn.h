@@ -80,6 +80,9 @@ enum {
     SYN_ERR_NOMEM = -8,   /* the workspace could not be allocated                       */
     SYN_ERR_DEVICE = -9,  /* the current device is not sm_103 / not usable              */
     SYN_ERR_TOO_LARGE = -10, /* the problem needs more than the fixed scratch array holds */
+    SYN_ERR_FORMAT = -11, /* a GGUF file is malformed or not a GGUF file               */
+    SYN_ERR_IO = -12,     /* a file could not be opened, mapped or written             */
+    SYN_ERR_NOTFOUND = -13, /* no GGUF key / tensor with that name or index              */
 };
 
 /* Elements per block: 32 (Q8_0, Q4_0, Q5_0), 256 (Q4_K, Q6_K, Q8_K) or 1 (F16); -1 for an unknown type. */
@@ -218,6 +221,132 @@ SYN_API int64_t syn_launch_count(void);
  * counted by syn_launch_count. */
 SYN_API int syn_mul_mat_prefill_static(int type, const void* W, int64_t n_out, int64_t n_in,
                                const float* X, int64_t n_tok, float* Y, syn_stream_t stream);
+
+/* ======================================================================================
+ * GGUF container (host code; only syn_gguf_upload touches the GPU)
+ *
+ * Layout ("The GGML ecosystem, and where synapse fits", section 2, the GGUF diagram; "ggml
+ * Documentation", GGUF specification, "File Structure" and the general.alignment key;
+ * "llama.cpp and GGUF", "Tensor info, alignment, and mmap"), little-endian:
+ *   header       "GGUF", version u32 (3), n_tensors u64, n_kv u64
+ *   metadata     n_kv x { key string, value type u32, value }
+ *   tensor info  n_tensors x { name string, n_dims u32, ne u64[n_dims], type u32, offset u64 }
+ *   padding      zeros to a multiple of general.alignment (u32; 32 when absent; a multiple of 8)
+ *   data         tensor i at data_start + offset_i (offset_i a multiple of the alignment)
+ * A string is a u64 byte count followed by the bytes (no terminator); an array value is an
+ * element type u32, a count u64 and the packed elements.  ne lists the innermost dimension
+ * first: a weight matrix with n_in inputs and n_out outputs has ne = [n_in, n_out], rows
+ * contiguous, exactly the W layout of syn_mul_mat.  Tensor offsets are relative to the
+ * start of the data section.  The numeric codes below (value types, ggml tensor types)
+ * follow the public GGUF specification; the pages name the types without their codes.
+ * ====================================================================================== */
+
+/* metadata value types */
+enum {
+    SYN_GGUF_UINT8 = 0, SYN_GGUF_INT8 = 1, SYN_GGUF_UINT16 = 2, SYN_GGUF_INT16 = 3,
+    SYN_GGUF_UINT32 = 4, SYN_GGUF_INT32 = 5, SYN_GGUF_FLOAT32 = 6, SYN_GGUF_BOOL = 7,
+    SYN_GGUF_STRING = 8, SYN_GGUF_ARRAY = 9, SYN_GGUF_UINT64 = 10, SYN_GGUF_INT64 = 11,
+    SYN_GGUF_FLOAT64 = 12,
+};
+
+/* ggml tensor element types the reader can size (others are listed with nbytes = -1) */
+enum {
+    SYN_GGML_F32 = 0, SYN_GGML_F16 = 1, SYN_GGML_Q4_0 = 2, SYN_GGML_Q5_0 = 6,
+    SYN_GGML_Q8_0 = 8, SYN_GGML_Q4_K = 12, SYN_GGML_Q6_K = 14, SYN_GGML_Q8_K = 15,
+    SYN_GGML_BF16 = 30,
+};
+
+typedef struct syn_gguf syn_gguf;               /* an open, memory-mapped GGUF file */
+typedef struct syn_gguf_writer syn_gguf_writer; /* a GGUF file being assembled       */
+
+/* Opens and memory-maps a GGUF (version 2 or 3) file read-only and checks its structure:
+ * magic and version, every string, array and tensor-info record inside the file, unique
+ * keys and tensor names, general.alignment (u32, a non-zero multiple of 8), 1..4
+ * dimensions each >= 1, rows of whole blocks, every offset a multiple of the alignment and
+ * every sized tensor inside the file.  Returns NULL on failure with *status (if non-NULL)
+ * set to SYN_ERR_NULL (path NULL), SYN_ERR_IO (open/stat/mmap failed) or SYN_ERR_FORMAT;
+ * else *status = SYN_OK.  Pointers returned by the accessors below point into the mapping
+ * and stay valid until syn_gguf_close.  Tensor data are at least alignment-aligned within
+ * the (page-aligned) mapping.  A handle may be read from several threads at once. */
+SYN_API syn_gguf* syn_gguf_open(const char* path, int* status);
+SYN_API void syn_gguf_close(syn_gguf* g); /* unmaps; NULL is a no-op */
+
+/* Header facts; -1 for a NULL handle.  data_start is the file offset of the data section. */
+SYN_API int64_t syn_gguf_version(const syn_gguf* g);
+SYN_API int64_t syn_gguf_n_tensors(const syn_gguf* g);
+SYN_API int64_t syn_gguf_n_kv(const syn_gguf* g);
+SYN_API int64_t syn_gguf_alignment(const syn_gguf* g);
+SYN_API int64_t syn_gguf_data_start(const syn_gguf* g);
+
+/* Index of the tensor called name (exact bytes), or -1. */
+SYN_API int64_t syn_gguf_find_tensor(const syn_gguf* g, const char* name);
+
+/* Tensor i's info; every output pointer may be NULL.  ne receives 4 values (unused
+ * dimensions = 1).  *data is a HOST pointer into the mapping and *nbytes its size, or NULL
+ * and -1 for an element type the reader cannot size.  SYN_ERR_NULL (g NULL) or
+ * SYN_ERR_NOTFOUND (i out of range). */
+SYN_API int syn_gguf_tensor_info(const syn_gguf* g, int64_t i, const char** name, uint32_t* ggml_type,
+                                 int* n_dims, int64_t* ne, uint64_t* offset, const void** data,
+                                 int64_t* nbytes);
+
+/* The tensor called name as syn_mul_mat's weight operand: *type the library's format code
+ * (SYN_TYPE_*), n_in = ne[0], n_out = ne[1]*ne[2]*ne[3], *data the HOST pointer into the
+ * mapping and *nbytes = n_out * syn_row_bytes(type, n_in).  Output pointers may be NULL.
+ * SYN_ERR_NULL, SYN_ERR_NOTFOUND, or SYN_ERR_TYPE when the element type is not one of
+ * Q8_0, Q4_K, Q6_K, Q4_0, Q5_0, F16. */
+SYN_API int syn_gguf_matrix(const syn_gguf* g, const char* name, int* type, int64_t* n_out, int64_t* n_in,
+                            const void** data, int64_t* nbytes);
+
+/* Copies tensor i's bytes from the mapping into the DEVICE buffer dst (dst_bytes long) with
+ * one cudaMemcpyAsync on stream (pageable source: the copy has finished reading the
+ * mapping when the call returns).  SYN_ERR_NULL, SYN_ERR_NOTFOUND, SYN_ERR_TYPE (tensor not
+ * sized), SYN_ERR_SHAPE (dst_bytes too small) or SYN_ERR_CUDA. */
+SYN_API int syn_gguf_upload(const syn_gguf* g, int64_t i, void* dst, int64_t dst_bytes, syn_stream_t stream);
+
+/* Metadata entry i: key, value type, and for arrays the element type and count (0 for
+ * other values).  Output pointers may be NULL.  SYN_ERR_NULL or SYN_ERR_NOTFOUND. */
+SYN_API int syn_gguf_kv_info(const syn_gguf* g, int64_t i, const char** key, uint32_t* value_type,
+                             uint32_t* elem_type, uint64_t* n_elems);
+
+/* Typed getters by key.  SYN_ERR_NULL (any pointer NULL), SYN_ERR_NOTFOUND (no such key),
+ * SYN_ERR_TYPE (the value has another type).  get_int takes every integer type and bool
+ * (SYN_ERR_RANGE for a UINT64 above INT64_MAX); get_float takes FLOAT32 and FLOAT64;
+ * get_string gives the bytes (not terminated) and their count; get_array gives the element
+ * type, count and a pointer to the packed little-endian elements (for string arrays use
+ * get_array_string, which returns element j or SYN_ERR_NOTFOUND past the end). */
+SYN_API int syn_gguf_get_int(const syn_gguf* g, const char* key, int64_t* out);
+SYN_API int syn_gguf_get_float(const syn_gguf* g, const char* key, double* out);
+SYN_API int syn_gguf_get_string(const syn_gguf* g, const char* key, const char** bytes, int64_t* len);
+SYN_API int syn_gguf_get_array(const syn_gguf* g, const char* key, uint32_t* elem_type, uint64_t* n,
+                               const void** data);
+SYN_API int syn_gguf_get_array_string(const syn_gguf* g, const char* key, uint64_t j, const char** bytes,
+                                      int64_t* len);
+
+/* Writer.  begin records the path and the alignment (a non-zero multiple of 8; when it is
+ * not 32 the first metadata entry is general.alignment = alignment, u32) and returns NULL
+ * for a NULL path or a bad alignment.  The kv_* calls append metadata entries in call order
+ * (SYN_ERR_SHAPE for a repeated key or for general.alignment; SYN_ERR_TYPE for a value
+ * type the call does not write: kv_int writes the integer types and BOOL, keeping the low
+ * bytes of value; kv_float FLOAT32 (rounded from value) or FLOAT64; kv_array any scalar
+ * element type, n elements of its size packed at data).  add_tensor appends a tensor (ne
+ * innermost first, 1..4 dims; nbytes must equal the size its type and shape give; names
+ * unique: SYN_ERR_SHAPE otherwise; SYN_ERR_TYPE for a type the reader cannot size); the
+ * bytes are copied, each tensor placed at the next multiple of the alignment.  finish
+ * writes the version-3 file (header, metadata, tensor info, zero padding, data) and frees
+ * the writer whatever it returns (SYN_OK or SYN_ERR_IO); abort frees it without writing.
+ * Everything is held in host memory until finish. */
+SYN_API syn_gguf_writer* syn_gguf_writer_begin(const char* path, uint32_t alignment);
+SYN_API int syn_gguf_writer_kv_int(syn_gguf_writer* w, const char* key, uint32_t value_type, int64_t value);
+SYN_API int syn_gguf_writer_kv_float(syn_gguf_writer* w, const char* key, uint32_t value_type, double value);
+SYN_API int syn_gguf_writer_kv_string(syn_gguf_writer* w, const char* key, const char* bytes, int64_t len);
+SYN_API int syn_gguf_writer_kv_array(syn_gguf_writer* w, const char* key, uint32_t elem_type, uint64_t n,
+                                     const void* data);
+SYN_API int syn_gguf_writer_kv_string_array(syn_gguf_writer* w, const char* key, uint64_t n,
+                                            const char* const* strs, const int64_t* lens);
+SYN_API int syn_gguf_writer_add_tensor(syn_gguf_writer* w, const char* name, uint32_t ggml_type, int n_dims,
+                                       const int64_t* ne, const void* data, int64_t nbytes);
+SYN_API int syn_gguf_writer_finish(syn_gguf_writer* w);
+SYN_API void syn_gguf_writer_abort(syn_gguf_writer* w);
 
 /* Static text for a status code. */
 SYN_API const char* syn_strerror(int status);
