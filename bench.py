@@ -5,8 +5,10 @@
 
 A step is one decode pass over the seven projections of one Llama-1B-shaped layer
 (q, k, v, o, gate, up: Q4_K; down: Q6_K; d = 2048, ffn = 8192, one token) through one
-syn_mul_mat_batch call: one decode launch converts the seven activations and streams every
-weight once (the same step as seven syn_mul_mat calls is reported too).  Weights are
+syn_mul_mat_batch call: one launch converts the seven activations, one decode launch streams
+every weight once (the same step as seven syn_mul_mat calls is reported too).  The timed steps
+are captured 16 to a CUDA graph, as a model's decode captures its layers in one graph; the
+same step with one graph per step is reported as graph_per_step_value.  Weights are
 ~N(0, 0.02) quantized with syn_quantize, activations ~N(0, 1), both synthetic.  Steps
 rotate over enough weight copies (>= 4x the L2 size) that every step reads its weights
 from HBM.  The printed value is weight GB/s: algorithmic bytes (weights + fp32 inputs +
@@ -34,6 +36,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "quantized mul_mat weight GB/s (decode GEMV) and TFLOP/s (prefill), % roofline"
 WORKLOAD = "llama1b_layer_decode_q4_k_m"
+STEPS_PER_GRAPH = 16
 
 
 def load_peaks():
@@ -135,12 +138,15 @@ def recorded_traffic(summary: str, source: str):
     return int(m.group(1))
 
 
-def time_graphs(torch, graphs, steps, stream):
+def time_graphs(torch, graphs, steps, stream, tail=None):
+    """Seconds for `steps` replays (cycling over graphs), plus one replay of `tail`."""
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     start.record(stream)
     for i in range(steps):
         graphs[i % len(graphs)].replay()
+    if tail is not None:
+        tail.replay()
     end.record(stream)
     end.synchronize()
     return start.elapsed_time(end) / 1e3
@@ -183,32 +189,55 @@ def gpu_arm(args, rank, world, dist):
         step(c)
         step_single(c)
     torch.cuda.synchronize()
+    # the timed steps: STEPS_PER_GRAPH consecutive steps per CUDA graph (as a model's decode
+    # captures its layers in one graph), each step reading another weight copy
     l0 = syn.launch_count()
     graphs = []
+    for c0 in range(n_copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(STEPS_PER_GRAPH):
+                step((c0 * STEPS_PER_GRAPH + r) % n_copies)
+        graphs.append(g)
+    launches_per_step = (syn.launch_count() - l0) // (n_copies * STEPS_PER_GRAPH)
+    rem = args.steps % STEPS_PER_GRAPH
+    rem_graph = None
+    if rem:
+        rem_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(rem_graph, stream=stream):
+            for r in range(rem):
+                step(r % n_copies)
+    per_step = []  # one graph per step (the launch of each graph not hidden)
     for c in range(n_copies):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             step(c)
-        graphs.append(g)
-    launches_per_step = (syn.launch_count() - l0) // n_copies
+        per_step.append(g)
     singles = []
     for c in range(n_copies):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             step_single(c)
         singles.append(g)
-    for i in range(args.warmup):
-        graphs[i % n_copies].replay()
+    for i in range(args.warmup):  # W warm-up steps (whole graphs, at least W steps)
+        if i % STEPS_PER_GRAPH == 0:
+            graphs[(i // STEPS_PER_GRAPH) % n_copies].replay()
+    for g in per_step:
+        g.replay()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+
+    def timed_steps():  # exactly args.steps steps
+        return time_graphs(torch, graphs, args.steps // STEPS_PER_GRAPH, stream, tail=rem_graph)
+
     with ClockSampler(dev) as clk:
-        t = time_graphs(torch, graphs, args.steps, stream)
+        t = timed_steps()
         # keep the sampler alive for a few samples even when the region is short
         extra = 0
         while len(clk.lines) < 5 and extra < 40:
-            time_graphs(torch, graphs, args.steps, stream)
+            timed_steps()
             extra += 1
     if dist:
         tt = torch.tensor([t], device="cuda")
@@ -216,6 +245,9 @@ def gpu_arm(args, rank, world, dist):
         t = float(tt.item())
     value = alg_bytes * args.steps * world / t / 1e9
     ms_per_step = t / args.steps * 1e3
+    n_ps = max(100, args.steps // 4)
+    t_ps = time_graphs(torch, per_step, n_ps, stream) / n_ps
+    per_step_value = alg_bytes / t_ps / 1e9
     for i in range(3):
         singles[i % n_copies].replay()
     t_single = time_graphs(torch, singles, max(100, args.steps // 4), stream) / max(100, args.steps // 4)
@@ -320,9 +352,10 @@ def gpu_arm(args, rank, world, dist):
                                                        for m in mats],
                    "n_tok": n_tok, "parallelism": f"replicas x{world}",
                    "l2": f"rotating {n_copies} weight copies ({n_copies * set_bytes / 1e6:.0f} MB >= 4x L2 "
-                         f"{l2 / 1e6:.0f} MB)", "cuda_graphs": True, "api": "syn_mul_mat_batch (one decode launch per step)"},
-        "roofline": {"bound": "hbm", "kernel": "k_gemv<1>: one grouped decode launch of the 7 matrices "
-                                               "(activation conversion fused)",
+                         f"{l2 / 1e6:.0f} MB)", "cuda_graphs": f"{STEPS_PER_GRAPH} steps per graph",
+                   "api": "syn_mul_mat_batch (one conversion + one decode launch per step)"},
+        "roofline": {"bound": "hbm", "kernel": "k_act_decode + k_gemv<1>: the conversion launch and the "
+                                               "grouped decode launch of the 7 matrices",
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
                      "traffic": recorded_traffic("k_gemv_llama1b_layer.md", "gguf_block_quantized_gb300/csrc/gemv.cu"),
@@ -330,6 +363,8 @@ def gpu_arm(args, rank, world, dist):
                                      "achieved/launch_us cover the conversion + decode launch pair",
                      "launch_us": round(k_time * 1e6, 3),
                      "single_launch_us": {m.name: round(tm * 1e6, 3) for m, tm in per_mat}},
+        "graph_per_step_value": {"value": round(per_step_value, 2), "unit": "GB/s",
+                                 "note": "the same step, one CUDA graph launch per step"},
         "single_call_value": {"value": round(single_value, 2), "unit": "GB/s",
                               "note": "same step as 7 separate syn_mul_mat calls (7 launches)"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -8,15 +8,20 @@
 // weight once per token group, so the kernel is bound by HBM bandwidth ("llama.cpp and
 // GGUF", CPU and Edge Inference: tokens/s <= bandwidth / model size).
 //
-// One CTA per SM.  The warps of the grid are dealt to the matrices of the launch in
+// Two launches per product group, chained by programmatic dependent launch:
+//   0. k_act_decode converts the activation rows of every matrix of the launch (the encoder
+//      of syn_quantize_activations) into a global workspace, in a swizzled layout: the
+//      16-byte chunks of consecutive blocks land in different bank groups.
+// k_gemv: one CTA per SM.  The warps of the grid are dealt to the matrices of the launch in
 // proportion to their bytes; each warp streams a contiguous range of rows of one matrix.
 //   1. Each warp starts its 1-D bulk copies (cp.async.bulk, completion on an mbarrier)
-//      into its own 3-deep ring of shared-memory stages: a stage is a run of whole blocks,
+//      into its own 2-deep ring of shared-memory stages: a stage is a run of whole blocks,
 //      copied through a window widened to 16-byte boundaries (so 34- and 210-byte blocks
 //      need no alignment); bytes past the last 16-byte boundary of W come by plain loads.
-//   2. Meanwhile the CTA converts the activation rows of the matrices its warps touch into
-//      shared memory, with the same encoder as syn_quantize_activations, in a swizzled
-//      layout: the 16-byte chunks of consecutive blocks land in different bank groups.
+//      It does so before waiting for the conversion launch, then releases the next launch
+//      on the stream (whose own weight copies then overlap this launch's tail).
+//   2. One thread bulk-copies the converted activations of the CTA's matrices into shared
+//      memory.
 //   3. Each lane decodes whole blocks (one per warp step): unpacks 4/6/8-bit codes in
 //      registers, forms the integer sub-block dots with dp4a, applies the integer sub-block
 //      scales and then the fp32 block scales.  Rows of at most 32 blocks are spread over
@@ -124,17 +129,66 @@ __host__ __device__ __forceinline__ int64_t sum_stride(int type, int64_t n_in) {
 }
 __host__ __device__ __forceinline__ int64_t sum_bytes(int type, int64_t n_in) { return 2 * sum_stride(type, n_in); }
 
+// Conversion unit r of matrix J (token r / units, then a 256-block, or four 32-blocks of the
+// Q8_0 family) into the decode layout: codes with swizzled 16-byte chunks, block scales,
+// 16-sums (K-quants) or block code sums (Q4_0 / Q5_0).  One warp.
+__device__ __forceinline__ void convert_unit(const GemvJob& J, int r, int8_t* aq, float* ad, int16_t* as, int lane) {
+    if (small_block(J.type)) {
+        const int t = r / J.units;
+        const int blk = (r - t * J.units) * 4 + (lane >> 3), e = lane & 7;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (blk < J.nbx) {
+            const float4 x = *reinterpret_cast<const float4*>(J.X + (int64_t)t * J.n_in + blk * 32 + 4 * e);
+            v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+        }
+        uint16_t db;
+        bool fin;
+        const uint32_t q = q8_0_group(v, &db, &fin);
+        // Q4_0 / Q5_0 weights: the block's code sum, for the -8 / -16 offset of their codes
+        int qs = 0;
+        if (J.type != SYN_Q8_0) {
+            qs = __dp4a((int)q, 0x01010101, 0);
+            qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+            qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+            qs += __shfl_xor_sync(0xffffffffu, qs, 4);
+        }
+        if (blk < J.nbx) {
+            *reinterpret_cast<uint32_t*>(aq + (int64_t)t * J.n_in + q8_chunk(blk, e >> 2) + 4 * (e & 3)) = q;
+            if (e == 0) ad[(int64_t)t * J.ds + blk] = h2f_bits(db);
+            if (e == 0 && J.type != SYN_Q8_0) as[(int64_t)t * sum_stride(J.type, J.n_in) + blk] = (int16_t)qs;
+        }
+    } else {
+        const int t = r / J.nbx;
+        const int blk = r - t * J.nbx;
+        const float* x = J.X + (int64_t)t * J.n_in + blk * 256 + lane * 8;
+        const float4 x0 = *reinterpret_cast<const float4*>(x);
+        const float4 x1 = *reinterpret_cast<const float4*>(x + 4);
+        const float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        uint32_t w0, w1;
+        float dd;
+        int bs;
+        bool fin;
+        q8_k_warp(v, &w0, &w1, &dd, &bs, &fin);
+        *reinterpret_cast<uint2*>(aq + (int64_t)t * J.n_in + k_chunk(blk, lane >> 1) + 8 * (lane & 1)) =
+            make_uint2(w0, w1);
+        if (lane == 0) ad[(int64_t)t * J.ds + blk] = dd;
+        if ((lane & 1) == 0) as[((int64_t)t * J.nbx + blk) * 16 + (lane >> 1)] = (int16_t)bs;
+    }
+}
+
 // Convert every activation row of every matrix of the launch into the global workspace,
-// in the layout the decode kernel copies to shared memory: codes with swizzled 16-byte
-// chunks, block scales, 16-sums.  One warp per 256-block (K-quants) or per four 32-blocks
-// (Q8_0).  Lets the dependent decode launch start (programmatic dependent launch) at once.
+// in the layout the decode kernel copies to shared memory.  One row of CTAs per matrix.
+// Lets the dependent decode launch start (programmatic dependent launch) at once.  It is
+// itself launched as a programmatic dependent of whatever precedes it on the stream, so it
+// waits for that work (which may produce X, or still read the workspace and Y this kernel
+// writes) before touching memory.
 __global__ void __launch_bounds__(128) k_act_decode(const __grid_constant__ GemvBatch b) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int GW = (int)((gridDim.x * blockDim.x) >> 5);
-    // one row of CTAs per matrix (blockIdx.y); 32-bit index arithmetic only (64-bit
-    // division runs on the slow fp64 pipe)
+    // 32-bit index arithmetic only (64-bit division runs on the slow fp64 pipe)
     const int j = blockIdx.y;
     const GemvJob& J = b.job[j];
     if (J.upr > 1) {  // runs of this matrix's rows are added into Y by different warps
@@ -142,52 +196,9 @@ __global__ void __launch_bounds__(128) k_act_decode(const __grid_constant__ Gemv
         for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ny; i += gridDim.x * blockDim.x) J.Y[i] = 0.f;
     }
     const int n_units = (int)b.n_tok * J.units;
-    for (int r = gw; r < n_units; r += GW) {
-        int8_t* aq = reinterpret_cast<int8_t*>(J.actg);
-        float* ad = reinterpret_cast<float*>(J.actg + J.g_d);
-        int16_t* as = reinterpret_cast<int16_t*>(J.actg + J.g_s);
-        if (small_block(J.type)) {
-            const int t = r / J.units;
-            const int blk = (r - t * J.units) * 4 + (lane >> 3), e = lane & 7;
-            float v[4] = {0.f, 0.f, 0.f, 0.f};
-            if (blk < J.nbx) {
-                const float4 x = *reinterpret_cast<const float4*>(J.X + (int64_t)t * J.n_in + blk * 32 + 4 * e);
-                v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-            }
-            uint16_t db;
-            bool fin;
-            const uint32_t q = q8_0_group(v, &db, &fin);
-            // Q4_0 / Q5_0 weights: the block's code sum, for the -8 / -16 offset of their codes
-            int qs = 0;
-            if (J.type != SYN_Q8_0) {
-                qs = __dp4a((int)q, 0x01010101, 0);
-                qs += __shfl_xor_sync(0xffffffffu, qs, 1);
-                qs += __shfl_xor_sync(0xffffffffu, qs, 2);
-                qs += __shfl_xor_sync(0xffffffffu, qs, 4);
-            }
-            if (blk < J.nbx) {
-                *reinterpret_cast<uint32_t*>(aq + (int64_t)t * J.n_in + q8_chunk(blk, e >> 2) + 4 * (e & 3)) = q;
-                if (e == 0) ad[(int64_t)t * J.ds + blk] = h2f_bits(db);
-                if (e == 0 && J.type != SYN_Q8_0) as[(int64_t)t * sum_stride(J.type, J.n_in) + blk] = (int16_t)qs;
-            }
-        } else {
-            const int t = r / J.nbx;
-            const int blk = r - t * J.nbx;
-            const float* x = J.X + (int64_t)t * J.n_in + blk * 256 + lane * 8;
-            const float4 x0 = *reinterpret_cast<const float4*>(x);
-            const float4 x1 = *reinterpret_cast<const float4*>(x + 4);
-            const float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            uint32_t w0, w1;
-            float dd;
-            int bs;
-            bool fin;
-            q8_k_warp(v, &w0, &w1, &dd, &bs, &fin);
-            *reinterpret_cast<uint2*>(aq + (int64_t)t * J.n_in + k_chunk(blk, lane >> 1) + 8 * (lane & 1)) =
-                make_uint2(w0, w1);
-            if (lane == 0) ad[(int64_t)t * J.ds + blk] = dd;
-            if ((lane & 1) == 0) as[((int64_t)t * J.nbx + blk) * 16 + (lane >> 1)] = (int16_t)bs;
-        }
-    }
+    for (int r = gw; r < n_units; r += GW)
+        convert_unit(J, r, reinterpret_cast<int8_t*>(J.actg), reinterpret_cast<float*>(J.actg + J.g_d),
+                     reinterpret_cast<int16_t*>(J.actg + J.g_s), lane);
 }
 
 struct ActView {
@@ -410,7 +421,6 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
     extern __shared__ __align__(1024) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gw = blockIdx.x * GV_WARPS + warp;
-    const int GW = gridDim.x * GV_WARPS;
     uint8_t* ring = smem + b.off_stage + (size_t)warp * GV_NS * GV_SLOT;
     const uint32_t ring_addr = smem_u32(ring);
     const uint32_t bar0 = smem_u32(smem + b.off_bar) + warp * GV_NS * 8;
@@ -508,6 +518,10 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
             advance(irow, ibcol, nblk, nrows);
             iu++;
         }
+        // the next launch on the stream may start now (a following conversion kernel waits
+        // for this launch to finish before it touches memory; its own decode launch then
+        // streams weights while this one drains)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         // the converted activations of tokens t0.. of the CTA's matrices: written by the
         // conversion kernel this launch depends on, so wait for it first
         asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -674,14 +688,41 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
         const int64_t per = std::max<int64_t>(1, T / unit_bytes(J));
         return (J.n_units + per - 1) / per;
     };
-    int64_t lo = 1, hi = 1;
-    for (int j = 0; j < b.n_jobs; j++) hi = std::max<int64_t>(hi, (int64_t)b.job[j].n_units * unit_bytes(b.job[j]));
-    while (lo < hi) {
-        const int64_t T = lo + (hi - lo) / 2;
-        int64_t need = 0;
-        for (int j = 0; j < b.n_jobs; j++) need += warps_for(b.job[j], T);
-        if (need <= GW) hi = T;
-        else lo = T + 1;
+    auto bisect = [&]() {
+        int64_t lo = 1, hi = 1;
+        for (int j = 0; j < b.n_jobs; j++) hi = std::max<int64_t>(hi, (int64_t)b.job[j].n_units * unit_bytes(b.job[j]));
+        while (lo < hi) {
+            const int64_t T = lo + (hi - lo) / 2;
+            int64_t need = 0;
+            for (int j = 0; j < b.n_jobs; j++) need += warps_for(b.job[j], T);
+            if (need <= GW) hi = T;
+            else lo = T + 1;
+        }
+        return lo;
+    };
+    int64_t lo = bisect();
+    // Rows of two stages are split into two runs only where that lowers the bound by more
+    // than 5 %: whole rows need no zeroed Y and no atomic additions.
+    bool any_split = false;
+    for (int j = 0; j < b.n_jobs; j++) any_split |= b.job[j].upr > 1;
+    if (any_split) {
+        int upr_was[GEMV_MAX_JOBS];
+        for (int j = 0; j < b.n_jobs; j++) {
+            GemvJob& J = b.job[j];
+            upr_was[j] = J.upr;
+            J.upr = 1;
+            J.n_units = (int)J.n_out;
+        }
+        const int64_t whole = bisect();
+        if (whole * 100 > lo * 105) {
+            for (int j = 0; j < b.n_jobs; j++) {
+                GemvJob& J = b.job[j];
+                J.upr = upr_was[j];
+                J.n_units = (int)(J.n_out * J.upr);
+            }
+        } else {
+            lo = whole;
+        }
     }
     int64_t nw[GEMV_MAX_JOBS], used = 0;
     for (int j = 0; j < b.n_jobs; j++) {
@@ -706,7 +747,9 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
     }
     for (int k = w; k < GW; k++) b.warp_job[k] = (uint8_t)(b.n_jobs - 1);  // idle: share of the last
     if (w < GW) b.job[b.n_jobs - 1].warp_end = GW;
-    // the conversion kernel: a plain launch, ordered after everything before it
+    // the conversion kernel: a programmatic dependent of the preceding work on the stream
+    // (it waits for that work to finish before touching memory); a previous decode launch
+    // releases it early, so its launch latency overlaps that launch's tail
     int64_t units = 0;
     for (int j = 0; j < b.n_jobs; j++) {
         GemvJob& J = b.job[j];
@@ -719,8 +762,16 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
     int64_t max_units = 1;
     for (int j = 0; j < b.n_jobs; j++) max_units = std::max<int64_t>(max_units, b.n_tok * b.job[j].units);
     const int64_t act_x = std::min<int64_t>((max_units + 3) / 4, std::max<int64_t>(1, (int64_t)sms * 4 / b.n_jobs));
-    k_act_decode<<<dim3((unsigned)act_x, (unsigned)b.n_jobs), 128, 0, s>>>(b);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t acfg = {};
+    acfg.gridDim = dim3((unsigned)act_x, (unsigned)b.n_jobs);
+    acfg.blockDim = dim3(128);
+    acfg.stream = s;
+    acfg.attrs = attr;
+    acfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&acfg, k_act_decode, b);
     if (e != cudaSuccess) return e;
     // the decode kernel, launched as its programmatic dependent: it streams weights (which the
     // conversion kernel does not touch) before waiting for the converted activations
@@ -729,9 +780,6 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
     cfg.blockDim = dim3(GV_WARPS * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, b);

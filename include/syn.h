@@ -21,7 +21,12 @@
  *     asynchronous unless stated otherwise;
  *   - the return value is SYN_OK (0) or a negative SYN_ERR_* code; on an error nothing
  *     has been enqueued, except for SYN_ERR_CUDA (a launch failed) and SYN_ERR_TIMEOUT;
- *   - nothing throws, nothing prints.
+ *   - nothing throws, nothing prints;
+ *   - the decode launches of syn_mul_mat / syn_mul_mat_batch release programmatic dependents
+ *     (CUDA programmatic dependent launch) before they finish: a kernel of the caller's that
+ *     is launched right after them with programmatic stream serialization allowed must call
+ *     cudaGridDependencySynchronize() (griddepcontrol.wait) before it reads their outputs.
+ *     Kernels launched without that attribute, and copies, are ordered as usual.
  */
 #ifndef SYN_H
 #define SYN_H

@@ -290,6 +290,71 @@ def test_gemv_split_rows_deterministic(syn):
     assert syn.device_status() == syn.OK
 
 
+@pytest.mark.parametrize("n_tok", [1, 3])
+def test_decode_chain_back_to_back(syn, n_tok):
+    """Dependent decode steps enqueued back to back: step i+1 reads step i's output as its
+    input, every step reuses the library's workspace, and a split-row product adds into the
+    same Y every step.  The conversion launch of step i+1 starts while step i's decode launch
+    drains (programmatic dependent launch) and must wait for it: the results, eager and
+    replayed from one CUDA graph, are bit-identical to the same calls with a device
+    synchronisation between them, and the first step matches the oracle."""
+    L, d = 5, 2048
+    Wa = [oracle.quantize(oracle.Q4_K, synth.normal(700 + i, (d, d), 0.02)) for i in range(L)]
+    Wb = [oracle.quantize(oracle.Q6_K, synth.normal(720 + i, (1024, d), 0.02)) for i in range(L)]
+    Ws = oracle.quantize(oracle.Q6_K, synth.normal(740, (600, 8192), 0.02))  # rows split in two runs
+    Wa_d, Wb_d, Ws_d = [dev(w) for w in Wa], [dev(w) for w in Wb], dev(Ws)
+    X0 = synth.normal(741, (n_tok, d))
+    X0_d = dev(X0)
+    X8 = dev(synth.normal(742, (n_tok, 8192)))
+    stream = torch.cuda.Stream()
+
+    def buffers():
+        nan = float("nan")
+        return ([torch.full((n_tok, d), nan, device="cuda") for _ in range(L)],
+                [torch.full((n_tok, 1024), nan, device="cuda") for _ in range(L)],
+                torch.full((n_tok, 600), nan, device="cuda"))
+
+    def run(bufs, sync):
+        Ya, Yb, Ys = bufs
+        x = X0_d
+        for i in range(L):
+            syn.mul_mat_batch([(oracle.Q4_K, Wa_d[i], d, d, x, Ya[i]), (oracle.Q6_K, Wb_d[i], 1024, d, x, Yb[i]),
+                               (oracle.Q6_K, Ws_d, 600, 8192, X8, Ys)], n_tok, stream=stream)
+            if sync:
+                torch.cuda.synchronize()
+            x = Ya[i]
+
+    def fetch(bufs):
+        torch.cuda.synchronize()
+        Ya, Yb, Ys = bufs
+        return [host(y).copy() for y in Ya + Yb + [Ys]]
+
+    with torch.cuda.stream(stream):
+        ref_bufs = buffers()
+        run(ref_bufs, True)
+        ref = fetch(ref_bufs)
+        eager = buffers()
+        run(eager, False)
+        got = [fetch(eager)]
+    graph_bufs = buffers()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run(graph_bufs, False)
+    for _ in range(2):
+        for y in graph_bufs[0] + graph_bufs[1] + [graph_bufs[2]]:
+            y.fill_(float("nan"))
+        g.replay()
+        got.append(fetch(graph_bufs))
+    for out in got:
+        for k, (a, b) in enumerate(zip(out, ref)):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), f"output {k} differs"
+    assert_close(ref[0], oracle.mul_mat(oracle.Q4_K, Wa[0], d, d, X0), tolerance(oracle.Q4_K, Wa[0], d, X0), "step 0")
+    X8h = host(X8)
+    assert_close(ref[-1], oracle.mul_mat(oracle.Q6_K, Ws, 600, 8192, X8h), tolerance(oracle.Q6_K, Ws, 8192, X8h),
+                 "split rows")
+    assert syn.device_status() == syn.OK
+
+
 def test_mul_mat_zero_and_degenerate(syn):
     wt, n_out, n_in = oracle.Q4_K, 40, 512
     Wq = oracle.quantize(wt, inputs_mixed(n_out, n_in, 3))
