@@ -32,6 +32,9 @@ std::atomic<int> g_gemv_max_tok{[] {
     return 8;
 }()};
 
+std::atomic<int> g_det{0};       // deterministic mode (syn_set_deterministic)
+std::atomic<int> g_sm_limit{0};  // 0: every SM
+
 struct DeviceState {
     bool init = false;
     int sms = 0;
@@ -75,6 +78,20 @@ int device_state(DeviceState** out) {
     *out = &st;
     return SYN_OK;
 }
+
+// SMs the launches of this call may use.
+int sms_of(const DeviceState* st) {
+    const int lim = g_sm_limit.load();
+    return lim > 0 && lim < st->sms ? lim : st->sms;
+}
+
+}  // namespace
+
+namespace syn {
+int sm_limit() { return g_sm_limit.load(); }
+}  // namespace syn
+
+namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
@@ -168,6 +185,13 @@ int syn_set_gemv_max_tok(int n) {
     return g_gemv_max_tok.exchange(n);
 }
 
+int syn_set_deterministic(int on) { return g_det.exchange(on ? 1 : 0); }
+
+int syn_set_sm_limit(int n) {
+    if (n < 0) return -1;
+    return g_sm_limit.exchange(n);
+}
+
 int syn_quantize(int type, const float* src, void* dst, int64_t n_rows, int64_t n_per_row, syn_stream_t stream) {
     if (!known_type(type)) return SYN_ERR_TYPE;
     if (n_rows < 0 || n_per_row <= 0 || n_per_row % elems(type) || n_rows * n_per_row > kMaxElems)
@@ -182,7 +206,7 @@ int syn_quantize(int type, const float* src, void* dst, int64_t n_rows, int64_t 
     int* range = st->words + 1;
     if (cudaMemsetAsync(range, 0, sizeof(int), s) != cudaSuccess) return SYN_ERR_CUDA;
     const int64_t nblocks = n_rows * (n_per_row / elems(type));
-    if (syn::launch_quantize(type, src, dst, nblocks, range, st->sms, s) != cudaSuccess) return SYN_ERR_CUDA;
+    if (syn::launch_quantize(type, src, dst, nblocks, range, sms_of(st), s) != cudaSuccess) return SYN_ERR_CUDA;
     g_launches++;
     int flag = 0;
     if (cudaMemcpyAsync(&flag, range, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return SYN_ERR_CUDA;
@@ -201,7 +225,7 @@ int syn_dequantize(int type, const void* src, float* dst, int64_t n_rows, int64_
     int rc = device_state(&st);
     if (rc) return rc;
     const int64_t nblocks = n_rows * (n_per_row / elems(type));
-    if (syn::launch_dequantize(type, src, dst, nblocks, st->sms, reinterpret_cast<cudaStream_t>(stream)) !=
+    if (syn::launch_dequantize(type, src, dst, nblocks, sms_of(st), reinterpret_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return SYN_ERR_CUDA;
     g_launches++;
@@ -220,7 +244,7 @@ int syn_quantize_activations(int wtype, const float* X, int64_t n_tok, int64_t n
     int rc = device_state(&st);
     if (rc) return rc;
     const int64_t nblocks = n_tok * (n_in / elems(xt));
-    if (syn::launch_quantize_act(xt, X, nblocks, qs, d, xt == SYN_TYPE_Q8_K ? bsums : nullptr, st->sms,
+    if (syn::launch_quantize_act(xt, X, nblocks, qs, d, xt == SYN_TYPE_Q8_K ? bsums : nullptr, sms_of(st),
                                  reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SYN_ERR_CUDA;
     g_launches++;
@@ -265,20 +289,23 @@ int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in, const floa
     int rc = device_state(&st);
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (type == SYN_TYPE_F16 && n_tok <= g_gemv_max_tok.load()) {
+    const bool det = g_det.load() != 0;
+    if (type == SYN_TYPE_F16 && (det || n_tok <= g_gemv_max_tok.load())) {
         void* ws;
         rc = workspace_for(s, (size_t)(n_tok * n_in * 2 + 256), &ws);
         if (rc) return rc;
-        rc = check_cuda(syn::launch_gemv_f16(W, n_out, n_in, X, n_tok, Y, ws, st->sms, s));
+        rc = check_cuda(syn::launch_gemv_f16(W, n_out, n_in, X, n_tok, Y, ws, sms_of(st), s));
         if (rc == SYN_OK) g_launches += 2;
         return rc;
     }
-    if (n_tok <= g_gemv_max_tok.load() && syn::gemv_act_bytes(type, n_in) <= syn::gemv_act_limit()) {
+    const bool fits = syn::gemv_act_bytes(type, n_in) <= syn::gemv_act_limit();
+    if (det && !fits) return SYN_ERR_SHAPE;
+    if (det || (n_tok <= g_gemv_max_tok.load() && fits)) {
         const syn::GemvDesc d{type, W, n_out, n_in, X, Y};
         void* ws;
         rc = workspace_for(s, (size_t)syn::gemv_workspace_bytes(1, &d, n_tok), &ws);
         if (rc) return rc;
-        rc = check_cuda(syn::launch_gemv_batch(1, &d, n_tok, ws, st->words, st->sms, s));
+        rc = check_cuda(syn::launch_gemv_batch(1, &d, n_tok, ws, st->words, sms_of(st), det, s));
         if (rc == SYN_OK) g_launches += 2;
         return rc;
     }
@@ -286,12 +313,12 @@ int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in, const floa
     rc = workspace_for(s, prefill_ws_bytes(n_in, n_tok), &ws);
     if (rc) return rc;
     const int xt = vec_dot(type);
-    if (syn::gemm_needs_zero(n_out, n_in, n_tok, st->sms) &&
+    if (syn::gemm_needs_zero(n_out, n_in, n_tok, sms_of(st)) &&
         cudaMemsetAsync(Y, 0, (size_t)n_tok * n_out * sizeof(float), s) != cudaSuccess)
         return SYN_ERR_CUDA;
-    if (launch_act_half(xt, X, n_tok * (n_in / elems(xt)), ws, st->sms, s) != cudaSuccess) return SYN_ERR_CUDA;
+    if (launch_act_half(xt, X, n_tok * (n_in / elems(xt)), ws, sms_of(st), s) != cudaSuccess) return SYN_ERR_CUDA;
     g_launches++;
-    if (syn::launch_gemm(type, W, n_out, n_in, ws, n_tok, Y, st->words, st->sms, s) != cudaSuccess)
+    if (syn::launch_gemm(type, W, n_out, n_in, ws, n_tok, Y, st->words, sms_of(st), s) != cudaSuccess)
         return SYN_ERR_CUDA;
     g_launches++;
     return SYN_OK;
@@ -314,6 +341,7 @@ int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_strea
     int rc = device_state(&st);
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool det = g_det.load() != 0;
     if (n_tok > g_gemv_max_tok.load()) {
         for (int i = 0; i < n; i++) {
             rc = syn_mul_mat(descs[i].type, descs[i].W, descs[i].n_out, descs[i].n_in, descs[i].X, n_tok, descs[i].Y,
@@ -331,7 +359,7 @@ int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_strea
         void* ws;
         int r = workspace_for(s, (size_t)syn::gemv_workspace_bytes(ng, group, n_tok), &ws);
         if (r) return r;
-        r = check_cuda(syn::launch_gemv_batch(ng, group, n_tok, ws, st->words, st->sms, s));
+        r = check_cuda(syn::launch_gemv_batch(ng, group, n_tok, ws, st->words, sms_of(st), det, s));
         if (r == SYN_OK) g_launches += 2;
         ng = 0;
         act = 0;

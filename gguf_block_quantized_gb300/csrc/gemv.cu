@@ -834,7 +834,8 @@ int64_t gemv_workspace_bytes(int n, const GemvDesc* d, int64_t n_tok) {
     return bytes + 256;
 }
 
-cudaError_t launch_gemv_batch(int n, const GemvDesc* d, int64_t n_tok, void* ws, int* err, int sms, cudaStream_t s) {
+cudaError_t launch_gemv_batch(int n, const GemvDesc* d, int64_t n_tok, void* ws, int* err, int sms, bool no_split,
+                              cudaStream_t s) {
     if (n < 1 || n > GEMV_MAX_JOBS) return cudaErrorInvalidValue;
     GemvBatch b{};
     b.n_jobs = n;
@@ -845,6 +846,10 @@ cudaError_t launch_gemv_batch(int n, const GemvDesc* d, int64_t n_tok, void* ws,
     for (int j = 0; j < n; j++) {
         make_job(b.job[j], d[j], bytes);
         GemvJob& J = b.job[j];
+        if (no_split) {
+            J.upr = 1;
+            J.n_units = (int)J.n_out;
+        }
         J.actg = g;
         J.g_d = up16(n_tok * J.n_in);
         J.g_s = J.g_d + up16(n_tok * J.ds * 4);
@@ -864,10 +869,5 @@ cudaError_t launch_gemv_batch(int n, const GemvDesc* d, int64_t n_tok, void* ws,
     }
 }
 
-cudaError_t launch_gemv(int type, const void* W, int64_t n_out, int64_t n_in, const float* X, int64_t n_tok,
-                        float* Y, void* ws, int* err, int sms, cudaStream_t s) {
-    const GemvDesc d{type, W, n_out, n_in, X, Y};
-    return launch_gemv_batch(1, &d, n_tok, ws, err, sms, s);
-}
 
 }  // namespace syn

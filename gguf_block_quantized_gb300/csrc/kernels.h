@@ -16,12 +16,6 @@ cudaError_t launch_act_half(int xtype, const float* X, int64_t n_blocks, void* x
 cudaError_t launch_block_sums(int type, const void* W, int64_t n_out, int64_t nb, const void* Xq,
                               int64_t n_tok, int32_t* S, cudaStream_t s);
 
-// Decode product: Y = W * Xq for small n_tok.  Two launches: the activation conversion into
-// the workspace ws (gemv_workspace_bytes), then the decode kernel as its programmatic
-// dependent (it streams weights before waiting for the conversion).
-cudaError_t launch_gemv(int type, const void* W, int64_t n_out, int64_t n_in, const float* X,
-                        int64_t n_tok, float* Y, void* ws, int* err, int sms, cudaStream_t s);
-
 // Decode products of up to GEMV_MAX_JOBS independent matrices in one launch.
 constexpr int GEMV_MAX_JOBS = 16;
 struct GemvDesc {
@@ -31,13 +25,21 @@ struct GemvDesc {
     const float* X;
     float* Y;
 };
-cudaError_t launch_gemv_batch(int n, const GemvDesc* d, int64_t n_tok, void* ws, int* err, int sms, cudaStream_t s);
+// Decode products: Y = W * Xq for few tokens.  Two launches: the activation conversion into
+// the workspace ws (gemv_workspace_bytes), then the decode kernel as its programmatic
+// dependent (it streams weights before waiting for the conversion).  no_split: every output
+// row is computed by one warp (the deterministic mode), else long rows may be split.
+cudaError_t launch_gemv_batch(int n, const GemvDesc* d, int64_t n_tok, void* ws, int* err, int sms, bool no_split,
+                              cudaStream_t s);
 int64_t gemv_workspace_bytes(int n, const GemvDesc* d, int64_t n_tok);
 
 // Shared memory one token of a matrix's converted activations takes in the decode kernel;
 // a launch holds at most gemv_act_limit() bytes of them (all matrices, one token).
 int64_t gemv_act_bytes(int type, int64_t n_in);
 int64_t gemv_act_limit();
+
+// The SM limit set by syn_set_sm_limit (0: none).
+int sm_limit();
 
 // Prefill product on the tensor cores.  xh: n_tok x n_in fp16 activations, written by
 // launch_act_half immediately before on the same stream (the product kernel is its

@@ -80,16 +80,18 @@ extern "C" int syn_mul_mat_prefill_static(int type, const void* W, int64_t n_out
     int rc = setup(dev, &d);
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int lim = syn::sm_limit();
+    const int sms = lim > 0 && lim < d->sms ? lim : d->sms;
     int* err = reinterpret_cast<int*>(d->scratch);
     void* xh = d->scratch + kHeader;
     const int xt = (type == SYN_TYPE_Q4_K || type == SYN_TYPE_Q6_K) ? SYN_TYPE_Q8_K
                  : type == SYN_TYPE_F16 ? SYN_TYPE_F16 : SYN_TYPE_Q8_0;
-    if (syn::gemm_needs_zero(n_out, n_in, n_tok, d->sms) &&
+    if (syn::gemm_needs_zero(n_out, n_in, n_tok, sms) &&
         cudaMemsetAsync(Y, 0, (size_t)n_tok * n_out * sizeof(float), s) != cudaSuccess)
         return SYN_ERR_CUDA;
-    if (syn::launch_act_half(xt, X, n_tok * (n_in / be), xh, d->sms, s) != cudaSuccess) return SYN_ERR_CUDA;
+    if (syn::launch_act_half(xt, X, n_tok * (n_in / be), xh, sms, s) != cudaSuccess) return SYN_ERR_CUDA;
     syn::note_launches(1);
-    if (syn::launch_gemm(type, W, n_out, n_in, xh, n_tok, Y, err, d->sms, s) != cudaSuccess) return SYN_ERR_CUDA;
+    if (syn::launch_gemm(type, W, n_out, n_in, xh, n_tok, Y, err, sms, s) != cudaSuccess) return SYN_ERR_CUDA;
     syn::note_launches(1);
     return SYN_OK;
 }

@@ -54,6 +54,8 @@ EXPORTS = [
     ("syn_launch_count", _i64, []),
     ("syn_strerror", ctypes.c_char_p, [_i32]),
     ("syn_mul_mat_prefill_static", _i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
+    ("syn_set_deterministic", _i32, [_i32]),
+    ("syn_set_sm_limit", _i32, [_i32]),
 ]
 
 class MatDesc(ctypes.Structure):
@@ -201,6 +203,16 @@ def block_sums(t: int, W, n_out: int, n_in: int, Xq, n_tok: int, stream=None):
 
 def set_gemv_max_tok(n: int) -> int:
     return int(syn_set_gemv_max_tok(n))
+
+
+def set_deterministic(on: bool) -> bool:
+    """Deterministic mode on/off; returns the previous setting."""
+    return bool(syn_set_deterministic(1 if on else 0))
+
+
+def set_sm_limit(n: int) -> int:
+    """At most n SMs for the library's launches (0: all); returns the previous limit."""
+    return int(syn_set_sm_limit(n))
 
 
 def device_status(clear: bool = True) -> int:

@@ -197,6 +197,30 @@ SYN_API int syn_block_sums(int type, const void* W, int64_t n_out, int64_t n_in,
  * SYN_GEMV_MAX_TOK when the library is loaded. */
 SYN_API int syn_set_gemv_max_tok(int n);
 
+/* Deterministic mode (on != 0; process-wide, default off; returns the previous setting).
+ * The invariants follow synapse's ("The GGML ecosystem, and where synapse fits", section 7,
+ * the table of what differs by design: each gemm row is bit-identical to gemv (G1); results
+ * are bit-identical for any thread count (D1)).  In this mode every syn_mul_mat /
+ * syn_mul_mat_batch product, whatever n_tok, runs on the decode kernels (token groups of up
+ * to 8, weights re-read per group) and no output row is split between warps, so that each
+ * Y element is computed by one fixed sequence of operations that depends only on the
+ * format, n_in and the inputs.  Hence, bit for bit:
+ *   - a token's row of Y is the same whatever the other tokens of the call (prefill rows
+ *     equal decode rows: G1);
+ *   - Y is the same for any SM limit (syn_set_sm_limit), grouping of products into
+ *     syn_mul_mat_batch calls, or split of the tokens into calls (the counterpart of D1).
+ * Accuracy is that of the decode path (the tolerance of syn_mul_mat).  Prefill is far
+ * slower in this mode (no tensor cores).  Products whose converted activation row does not
+ * fit the decode kernel's shared memory (n_in above about 60,000 for the 8-bit activation
+ * formats) return SYN_ERR_SHAPE in this mode.  syn_mul_mat_prefill_static is not affected
+ * (it always runs the tensor-core prefill). */
+SYN_API int syn_set_deterministic(int on);
+
+/* At most n SMs for the library's launches (n >= 1; 0 = all of them, the default).
+ * Process-wide; returns the previous value, or -1 (and changes nothing) for n < 0.  Lets a
+ * caller leave SMs to concurrent work; the grid of every kernel is sized to the limit. */
+SYN_API int syn_set_sm_limit(int n);
+
 /* Read (and with clear != 0, reset) the device-side error word of the current device:
  * SYN_OK, or SYN_ERR_TIMEOUT if a kernel gave up a bounded wait.  Synchronizes the
  * device. */

@@ -51,6 +51,9 @@ def test_host_functions(lib):
     old = lib.syn_set_gemv_max_tok(5)
     assert lib.syn_set_gemv_max_tok(old) == 5
     assert lib.syn_set_gemv_max_tok(-1) == -1
+    assert lib.syn_set_deterministic(7) == 0 and lib.syn_set_deterministic(0) == 1
+    assert lib.syn_set_sm_limit(-1) == -1
+    assert lib.syn_set_sm_limit(5) == 0 and lib.syn_set_sm_limit(0) == 5
 
 
 def test_argument_checks_need_no_gpu(lib):

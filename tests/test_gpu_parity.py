@@ -355,6 +355,82 @@ def test_decode_chain_back_to_back(syn, n_tok):
     assert syn.device_status() == syn.OK
 
 
+DET_SHAPES = [(300, 1024, 37), (600, 8192, 11), (77, 2304, 9)]  # (n_out, n_in, n_tok); 8192: rows split by default
+
+
+@pytest.mark.parametrize("wt", TYPES_W + [oracle.F16])
+@pytest.mark.parametrize("shape", DET_SHAPES)
+def test_deterministic_mode_invariants(syn, wt, shape):
+    """Deterministic mode (G1, D1 of synapse): a token's output row is bit-identical whatever
+    the other tokens of the call (prefill rows equal decode rows), whatever the SM limit,
+    the grouping of products into one batch call or the split of the tokens into calls;
+    and it is within the product's tolerance of the oracle."""
+    n_out, n_in, n_tok = shape
+    Wq = oracle.quantize(wt, synth.normal(800 + n_in, (n_out, n_in), 0.02))
+    X = synth.normal(801 + n_in, (n_tok, n_in))
+    W, Xd = dev(Wq), dev(X)
+    old = syn.set_deterministic(True)
+    try:
+        ref = host(syn.mul_mat(wt, W, n_out, n_in, Xd))
+        outs = {"one token per call": np.concatenate([host(syn.mul_mat(wt, W, n_out, n_in, Xd[t:t + 1]))
+                                                      for t in range(n_tok)]),
+                "calls of 5 tokens": np.concatenate([host(syn.mul_mat(wt, W, n_out, n_in, Xd[t:t + 5]))
+                                                     for t in range(0, n_tok, 5)])}
+        for lim in (1, 13, 100):
+            prev = syn.set_sm_limit(lim)
+            try:
+                outs[f"{lim} SMs"] = host(syn.mul_mat(wt, W, n_out, n_in, Xd))
+            finally:
+                syn.set_sm_limit(prev)
+        # grouped with two other products in one batch call (decode-sized token count)
+        if wt != oracle.F16:
+            Wo = dev(oracle.quantize(oracle.Q6_K, synth.normal(802, (129, 8192), 0.02)))
+            Xo = dev(synth.normal(803, (n_tok, 8192)))
+            Yb = torch.full((n_tok, n_out), float("nan"), device="cuda")
+            Yo = [torch.empty((n_tok, 129), device="cuda") for _ in range(2)]
+            syn.mul_mat_batch([(oracle.Q6_K, Wo, 129, 8192, Xo, Yo[0]), (wt, W, n_out, n_in, Xd, Yb),
+                               (oracle.Q6_K, Wo, 129, 8192, Xo, Yo[1])], n_tok)
+            outs["batched"] = host(Yb)
+        for what, Y in outs.items():
+            assert np.array_equal(Y.view(np.uint32), ref.view(np.uint32)), what
+    finally:
+        syn.set_deterministic(old)
+    assert_close(ref, oracle.mul_mat(wt, Wq, n_out, n_in, X), tolerance(wt, Wq, n_in, X), "deterministic vs oracle")
+    assert syn.device_status() == syn.OK
+
+
+def test_deterministic_mode_rejects_too_wide_rows(syn):
+    """A row whose converted activations do not fit the decode kernel's shared memory is
+    rejected in deterministic mode (the tensor-core prefill takes it otherwise)."""
+    wt, n_out, n_in = oracle.Q4_K, 3, 98304
+    Wq = oracle.quantize(wt, synth.normal(810, (n_out, n_in), 0.02))
+    X = synth.normal(811, (1, n_in))
+    W, Xd = dev(Wq), dev(X)
+    Y = torch.empty((1, n_out), device="cuda")
+    old = syn.set_deterministic(True)
+    try:
+        assert syn.syn_mul_mat(wt, syn._ptr(W), n_out, n_in, syn._ptr(Xd), 1, syn._ptr(Y), None) == syn.ERR_SHAPE
+    finally:
+        syn.set_deterministic(old)
+    Y = host(syn.mul_mat(wt, W, n_out, n_in, Xd))
+    assert_close(Y, oracle.mul_mat(wt, Wq, n_out, n_in, X), tolerance(wt, Wq, n_in, X), "wide row, default mode")
+
+
+@pytest.mark.parametrize("lim", [1, 7, 64])
+def test_sm_limit_parity(syn, lim):
+    """Products on a limited number of SMs (decode, grouped decode and tensor-core prefill)
+    stay within tolerance of the oracle."""
+    prev = syn.set_sm_limit(lim)
+    try:
+        for wt, n_out, n_in, n_tok in [(oracle.Q4_K, 300, 2048, 1), (oracle.Q6_K, 129, 8192, 3),
+                                      (oracle.Q8_0, 257, 1024, 40), (oracle.Q4_K, 200, 768, 130)]:
+            Y, ref, bound = run_mul_mat(syn, wt, n_out, n_in, n_tok, 820 + lim, "gemv" if n_tok <= 8 else "gemm")
+            assert_close(Y, ref, bound, f"{oracle.NAMES[wt]} {n_out}x{n_in} tok={n_tok} on {lim} SMs")
+    finally:
+        syn.set_sm_limit(prev)
+    assert syn.device_status() == syn.OK
+
+
 def test_mul_mat_zero_and_degenerate(syn):
     wt, n_out, n_in = oracle.Q4_K, 40, 512
     Wq = oracle.quantize(wt, inputs_mixed(n_out, n_in, 3))
