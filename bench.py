@@ -445,6 +445,69 @@ def other_configs(torch, syn, synth, workloads, stream, l2, hbm_peak, tc_peak, q
                                                   "frac": round(fl / t / 1e12 / tc_peak, 4), "us": round(t * 1e6, 2)}
         del Wp, Xp, Yp
     torch.cuda.empty_cache()
+
+    # deterministic mode (every product on the decode kernels, no split rows): the layer step
+    # and a 512-token prefill of the Llama-8B FFN up shape (Q4_K)
+    mats = workloads.LLAMA1B_LAYER
+    n_cop = max(2, -(-4 * l2 // sum(m.weight_bytes for m in mats)))
+    W = build_weights(torch, syn, workloads, synth, mats, 2, n_cop)
+    X = [torch.from_numpy(synth.activations(2, i, 1, m.n_in)).cuda() for i, m in enumerate(mats)]
+    Y = [torch.empty((1, m.n_out), device="cuda") for m in mats]
+    m8 = workloads.Matrix("ffn_up", workloads.Q4_K, 14336, 4096)
+    Wp = syn.quantize(m8.wtype, torch.from_numpy(synth.weight(4, 0, m8.n_out, m8.n_in)).cuda())
+    Xp = torch.from_numpy(synth.activations(4, 0, 512, m8.n_in)).cuda()
+    Yp = torch.empty((512, m8.n_out), device="cuda")
+    prev = syn.set_deterministic(True)
+    try:
+        t = time_calls(torch, stream, lambda c: syn.mul_mat_batch(
+            [(m.wtype, W[c][i], m.n_out, m.n_in, X[i], Y[i]) for i, m in enumerate(mats)], 1, stream=stream), n_cop, 16)
+        alg = sum(workloads.gemv_bytes(m, 1) for m in mats)
+        out["deterministic_llama1b_layer_decode"] = {"value": round(alg / t / 1e9, 1), "unit": "GB/s",
+                                                     "frac": round(alg / t / 1e9 / hbm_peak, 4),
+                                                     "us": round(t * 1e6, 3)}
+        t = time_calls(torch, stream, lambda c: syn.mul_mat(m8.wtype, Wp, m8.n_out, m8.n_in, Xp, Y=Yp, stream=stream),
+                       1, 2, trials=3)
+        fl = workloads.gemm_flops(m8, 512)
+        out["deterministic_q4_k_14336x4096_prefill_512tok"] = {
+            "value": round(fl / t / 1e12, 1), "unit": "TFLOP/s", "frac": round(fl / t / 1e12 / tc_peak, 4),
+            "us": round(t * 1e6, 2), "note": "decode kernels, 64 groups of 8 tokens: weights read 64 times"}
+    finally:
+        syn.set_deterministic(prev)
+    del W, X, Y, Wp, Xp, Yp
+    torch.cuda.empty_cache()
+
+    # GGUF: the layer's seven weight tensors written to a synthetic file, opened (mmap and
+    # structure checks) and copied to the device with syn_gguf_upload (page cache warm)
+    import tempfile
+    mats = workloads.LLAMA1B_LAYER
+    code = {workloads.Q4_K: syn.GGML_Q4_K, workloads.Q6_K: syn.GGML_Q6_K}
+    with tempfile.TemporaryDirectory() as td:
+        path = os.path.join(td, "layer.gguf")
+        w = syn.GGUFWriter(path)
+        w.kv_string("general.architecture", b"llama")
+        for i, m in enumerate(mats):
+            q = syn.quantize(m.wtype, torch.from_numpy(synth.weight(2, i, m.n_out, m.n_in)).cuda()).cpu().numpy()
+            w.add_tensor(f"blk.0.{m.name}.weight", code[m.wtype], [m.n_in, m.n_out], q)
+        w.finish()
+        dst = [torch.empty(m.weight_bytes, dtype=torch.uint8, device="cuda") for m in mats]
+        times = []
+        for _ in range(4):
+            t0 = time.perf_counter()
+            r = syn.GGUFReader(path)
+            t1 = time.perf_counter()
+            for i, m in enumerate(mats):
+                syn.check(syn.syn_gguf_upload(r.h, i, dst[i].data_ptr(), m.weight_bytes, stream.cuda_stream))
+            stream.synchronize()
+            t2 = time.perf_counter()
+            r.close()
+            times.append((t1 - t0, t2 - t1))
+        o = sorted(t[0] for t in times[1:])[1]
+        u = sorted(t[1] for t in times[1:])[1]
+        wsum = sum(m.weight_bytes for m in mats)
+        out["gguf_llama1b_layer_open_upload"] = {"value": round(wsum / u / 1e9, 2), "unit": "GB/s",
+                                                 "open_us": round(o * 1e6, 1), "upload_ms": round(u * 1e3, 3),
+                                                 "bytes": wsum, "note": "host mmap -> device, one copy per tensor"}
+        del dst
     if quick:
         return out
 
