@@ -114,6 +114,81 @@ __device__ __forceinline__ float group_sum(float v, int lg) {
     return v;
 }
 
+// Window of packed warp steps whose row sums are reduced together: 8 / NT steps.
+template <int NT>
+struct Win {
+    static constexpr int N = NT >= 8 ? 1 : 8 / NT;
+};
+
+// Rows of at most 32 blocks: every warp step leaves, in each aligned group of 2^lgl lanes,
+// the partial sums of one row.  The partials of the last Win steps are kept (part[i] is step
+// i of the window; a window of n < N steps sits in part[N - n ..]) and reduced at once: a
+// transposed butterfly over the group (offsets 2^(lgl-1) .. 1) that, while a lane holds more
+// than one value, sends half of them to its partner and keeps the other half; then plain
+// butterfly steps.  Each row's partials are added in the same tree whatever the window, so
+// the result does not depend on where a row falls.  The one lane per group and value that
+// holds a total writes it: rows row0 + step * rstep + (lane >> lgl), rows below row_end.
+template <int NT>
+__device__ __forceinline__ void win_flush(float (&part)[Win<NT>::N][NT], int n, int lgl, int lane, int64_t row0,
+                                          int rstep, int64_t row_end, float* Y, int64_t n_out, int64_t t0,
+                                          int64_t n_tok) {
+    constexpr int N = Win<NT>::N;
+    if (N > 1 && n == 1) {  // one step: the plain butterfly on it alone (same tree per row)
+        const int64_t row = row0 + (lane >> lgl);
+#pragma unroll
+        for (int t = 0; t < NT; t++) {
+            float v = part[N - 1][t];
+            for (int k = 0; k < lgl; k++) v += __shfl_xor_sync(0xffffffffu, v, 1 << (lgl - 1 - k));
+            if ((lane & ((1 << lgl) - 1)) == 0 && row < row_end && t0 + t < n_tok) Y[(t0 + t) * n_out + row] = v;
+            part[N - 1][t] = 0.f;
+        }
+        return;
+    }
+    int vbase = 0, k_done = 0;
+#pragma unroll
+    for (int k = 0; (N >> k) > 1; k++) {
+        if (k < lgl) {
+            const int o = 1 << (lgl - 1 - k);
+            const bool up = (lane & o) != 0;
+            const int half = N >> (k + 1);
+#pragma unroll
+            for (int i = 0; i < (N >> (k + 1)); i++) {
+#pragma unroll
+                for (int t = 0; t < NT; t++) {
+                    const float send = up ? part[i][t] : part[i + half][t];
+                    const float keep = up ? part[i + half][t] : part[i][t];
+                    part[i][t] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+            if (up) vbase += half;
+            k_done = k + 1;
+        }
+    }
+    for (int k = k_done; k < lgl; k++) {
+        const int o = 1 << (lgl - 1 - k);
+#pragma unroll
+        for (int t = 0; t < NT; t++) part[0][t] += __shfl_xor_sync(0xffffffffu, part[0][t], o);
+    }
+    const int left = N >> k_done;  // values this lane holds
+    const bool writer = (lane & ((1 << (lgl - k_done)) - 1)) == 0;
+#pragma unroll
+    for (int i = 0; i < N; i++) {
+        if (i < left && writer) {
+            const int step = vbase + i - (N - n);
+            const int64_t row = row0 + (int64_t)step * rstep + (lane >> lgl);
+            if (step >= 0 && row < row_end) {
+#pragma unroll
+                for (int t = 0; t < NT; t++)
+                    if (t0 + t < n_tok) Y[(t0 + t) * n_out + row] = part[i][t];
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < N; i++)
+#pragma unroll
+        for (int t = 0; t < NT; t++) part[i][t] = 0.f;
+}
+
 // Swizzled activation chunks: byte offset of chunk c (16 bytes) of block B.  The two lanes
 // of a K-quant block read chunks c and c + 8 of it, and the four blocks of a quarter-warp
 // are consecutive: chunk c of block B goes to 16-byte bank group (c ^ B ^ 4*(c >= 8)) % 8,
@@ -550,6 +625,17 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
         float acc[NT];
 #pragma unroll
         for (int t = 0; t < NT; t++) acc[t] = 0.f;
+        // packed rows: the window of steps whose row sums are reduced together
+        constexpr int PW = Win<NT>::N;
+        float part[PW][NT];
+#pragma unroll
+        for (int i = 0; i < PW; i++)
+#pragma unroll
+            for (int t = 0; t < NT; t++) part[i][t] = 0.f;
+        int pw = 0;
+        int64_t prow = r0;
+        const int lgl = lg < 0 ? 0 : small_block(type) ? lg - 1 : lg + 1;  // log2 lanes per packed row
+        const int rstep = lg < 0 ? 0 : bps >> lg;                          // packed rows per warp step
         int64_t crow = r0;
         int cbcol = b0;
         int cu = u0;
@@ -585,18 +671,24 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
             }
             const uint8_t* sbase = ring + s * GV_SLOT + (int)(((crow * nb + cbcol) * (int64_t)bb) & 15);
             if (lg >= 0) {
-                // rows of 2^lg <= bps blocks: bps >> lg rows per warp step; the lanes of a row
-                // form an aligned group of 2^lgl lanes
-                const int lgl = small_block(type) ? lg - 1 : lg + 1;
+                // rows of 2^lg <= bps blocks: rstep rows per warp step; the lanes of a row form
+                // an aligned group of 2^lgl lanes.  Stages hold a multiple of rstep rows, so the
+                // warp's steps cover its rows in order, rstep at a time.
                 for (int s0 = 0; s0 < nblk; s0 += bps) {
                     lane_step<NT>(type, sbase, bb, s0, nblk - s0, s0, nb - 1, A, acc);
-                    const int mine = s0 + (small_block(type) ? 2 * lane : lane >> 1);  // first block of this lane
+#pragma unroll
+                    for (int i = 0; i + 1 < PW; i++)
+#pragma unroll
+                        for (int t = 0; t < NT; t++) part[i][t] = part[i + 1][t];
 #pragma unroll
                     for (int t = 0; t < NT; t++) {
-                        const float v = group_sum(acc[t], lgl);
-                        if ((lane & ((1 << lgl) - 1)) == 0 && mine < nblk && t0 + t < b.n_tok)
-                            Y[(t0 + t) * n_out + crow + (mine >> lg)] = v;
+                        part[PW - 1][t] = acc[t];
                         acc[t] = 0.f;
+                    }
+                    if (++pw == PW) {
+                        win_flush<NT>(part, PW, lgl, lane, prow, rstep, r1, Y, n_out, t0, b.n_tok);
+                        prow += (int64_t)PW * rstep;
+                        pw = 0;
                     }
                 }
             } else {
@@ -625,6 +717,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
             advance(crow, cbcol, nblk, nrows);
             cu++;
         }
+        if (!failed && pw > 0) win_flush<NT>(part, pw, lgl, lane, prow, rstep, r1, Y, n_out, t0, b.n_tok);
         seq = qi;
     }
 }
