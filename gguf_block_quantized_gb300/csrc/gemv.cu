@@ -94,6 +94,8 @@ struct GemvBatch {
     int64_t total_bytes;
     int64_t n_tok;
     int* err;
+    int fused;              // 1: each CTA converts its own activations (no conversion launch)
+    int off_x;              // fused: shared-memory staging of the CTA's fp32 activation rows
     int off_stage, off_bar, off_flag;
     // matrix of each decode warp of the grid: one parameter-space load instead of a
     // dependent walk over the job table
@@ -204,20 +206,38 @@ __host__ __device__ __forceinline__ int64_t sum_stride(int type, int64_t n_in) {
 }
 __host__ __device__ __forceinline__ int64_t sum_bytes(int type, int64_t n_in) { return 2 * sum_stride(type, n_in); }
 
-// Conversion unit r of matrix J (token r / units, then a 256-block, or four 32-blocks of the
-// Q8_0 family) into the decode layout: codes with swizzled 16-byte chunks, block scales,
-// 16-sums (K-quants) or block code sums (Q4_0 / Q5_0).  One warp.
-__device__ __forceinline__ void convert_unit(const GemvJob& J, int r, int8_t* aq, float* ad, int16_t* as, int lane) {
+// Conversion unit r of matrix J: token r / units, then a 256-block (K-quants, 8 values per
+// lane) or four 32-blocks (the Q8_0 family, 4 values per lane; blocks past the row are 0).
+// Token r / units is row r / units of X (n_in floats each).  unit_load reads the lane's
+// values, unit_store encodes them into the decode layout (codes with swizzled 16-byte chunks,
+// block scales, 16-sums (K-quants) or block code sums (Q4_0 / Q5_0)) at slot r / units.
+// One warp.
+__device__ __forceinline__ void unit_load(const GemvJob& J, const float* X, int r, int lane, float v[8]) {
     if (small_block(J.type)) {
         const int t = r / J.units;
         const int blk = (r - t * J.units) * 4 + (lane >> 3), e = lane & 7;
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (blk < J.nbx) {
-            const float4 x = *reinterpret_cast<const float4*>(J.X + (int64_t)t * J.n_in + blk * 32 + 4 * e);
-            v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-        }
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (blk < J.nbx) x = *reinterpret_cast<const float4*>(X + (int64_t)t * J.n_in + blk * 32 + 4 * e);
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+        v[4] = v[5] = v[6] = v[7] = 0.f;
+    } else {
+        const int t = r / J.nbx;
+        const int blk = r - t * J.nbx;
+        const float* x = X + (int64_t)t * J.n_in + blk * 256 + lane * 8;
+        const float4 x0 = *reinterpret_cast<const float4*>(x);
+        const float4 x1 = *reinterpret_cast<const float4*>(x + 4);
+        v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
+        v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+    }
+}
+
+__device__ __forceinline__ void unit_store(const GemvJob& J, int r, const float v[8], int8_t* aq, float* ad, int16_t* as,
+                                           int lane) {
+    bool fin;
+    if (small_block(J.type)) {
+        const int t = r / J.units;
+        const int blk = (r - t * J.units) * 4 + (lane >> 3), e = lane & 7;
         uint16_t db;
-        bool fin;
         const uint32_t q = q8_0_group(v, &db, &fin);
         // Q4_0 / Q5_0 weights: the block's code sum, for the -8 / -16 offset of their codes
         int qs = 0;
@@ -235,14 +255,9 @@ __device__ __forceinline__ void convert_unit(const GemvJob& J, int r, int8_t* aq
     } else {
         const int t = r / J.nbx;
         const int blk = r - t * J.nbx;
-        const float* x = J.X + (int64_t)t * J.n_in + blk * 256 + lane * 8;
-        const float4 x0 = *reinterpret_cast<const float4*>(x);
-        const float4 x1 = *reinterpret_cast<const float4*>(x + 4);
-        const float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
         uint32_t w0, w1;
         float dd;
         int bs;
-        bool fin;
         q8_k_warp(v, &w0, &w1, &dd, &bs, &fin);
         *reinterpret_cast<uint2*>(aq + (int64_t)t * J.n_in + k_chunk(blk, lane >> 1) + 8 * (lane & 1)) =
             make_uint2(w0, w1);
@@ -272,8 +287,12 @@ __global__ void __launch_bounds__(128) k_act_decode(const __grid_constant__ Gemv
     }
     const int n_units = (int)b.n_tok * J.units;
     for (int r = gw; r < n_units; r += GW)
-        convert_unit(J, r, reinterpret_cast<int8_t*>(J.actg), reinterpret_cast<float*>(J.actg + J.g_d),
-                     reinterpret_cast<int16_t*>(J.actg + J.g_s), lane);
+    {
+        float v[8];
+        unit_load(J, J.X, r, lane, v);
+        unit_store(J, r, v, reinterpret_cast<int8_t*>(J.actg), reinterpret_cast<float*>(J.actg + J.g_d),
+                   reinterpret_cast<int16_t*>(J.actg + J.g_s), lane);
+    }
 }
 
 struct ActView {
@@ -491,7 +510,9 @@ __device__ __forceinline__ void warp_share(const GemvBatch& b, int gw, int& j, i
     u1 = q * (i + 1) + (rem * (i + 1)) / nw;
 }
 
-template <int NT>
+// FUSED: the CTA converts its activations itself (b.fused); a separate instantiation, so that
+// the other path compiles as if it did not exist.
+template <int NT, bool FUSED>
 __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant__ GemvBatch b) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -602,6 +623,43 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
         asm volatile("griddepcontrol.wait;" ::: "memory");
         __syncthreads();  // every warp is done with the previous token group's activations
         const uint32_t act_parity = (uint32_t)((t0 / NT) & 1);
+        if (FUSED) {
+            // the fp32 rows of tokens t0.. of the CTA's matrices by bulk copy into the staging
+            // area, then converted by the CTA's warps (units dealt round-robin over matrices
+            // ja..jb) into the activation layout
+            const int nt = (int)min((int64_t)NT, b.n_tok - t0);
+            if (threadIdx.x == 0) {
+                uint32_t tx = 0;
+                for (int j = ja; j <= jb; j++) tx += (uint32_t)(nt * b.job[j].n_in * 4);
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(act_bar, tx);
+                uint32_t xo = 0;
+                for (int j = ja; j <= jb; j++) {
+                    const GemvJob& J = b.job[j];
+                    const uint32_t by = (uint32_t)(nt * J.n_in * 4);
+                    bulk_g2s(smem_u32(smem + b.off_x + xo), J.X + t0 * J.n_in, by, act_bar);
+                    xo += by;
+                }
+            }
+            if (!mbar_wait(act_bar, act_parity, b.err, abort_flag)) break;
+            uint32_t xo = 0;
+            int ubase = 0;
+            for (int j = ja; j <= jb; j++) {
+                const GemvJob& J = b.job[j];
+                const float* xs = reinterpret_cast<const float*>(smem + b.off_x + xo);
+                const int n_u = nt * J.units;
+                for (int r = ((warp - ubase) % GV_WARPS + GV_WARPS) % GV_WARPS; r < n_u; r += GV_WARPS) {
+                    float v[8];
+                    unit_load(J, xs, r, lane, v);
+                    unit_store(J, r, v, reinterpret_cast<int8_t*>(smem + J.act_q),
+                               reinterpret_cast<float*>(smem + J.act_d), reinterpret_cast<int16_t*>(smem + J.act_s),
+                               lane);
+                }
+                ubase += n_u;
+                xo += (uint32_t)(nt * J.n_in * 4);
+            }
+            __syncthreads();
+        } else {
         if (threadIdx.x == 0) {
             const int64_t nt = min((int64_t)NT, b.n_tok - t0);
             uint32_t tx = 0;
@@ -621,6 +679,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
             }
         }
         if (!mbar_wait(act_bar, act_parity, b.err, abort_flag)) break;
+        }
 
         float acc[NT];
 #pragma unroll
@@ -758,13 +817,14 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
     off += GV_WARPS * GV_NS * 8;
     b.off_flag = (int)off;
     off += 16;  // abort flag, activation barrier
-    const size_t smem = (size_t)off;
-    if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
-    auto kern = k_gemv<NT>;
+    if (off > 227 * 1024) return cudaErrorInvalidConfiguration;
+    b.off_x = (int)up16(off);
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        attr_err = cudaFuncSetAttribute(k_gemv<NT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(k_gemv<NT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
     if (attr_err != cudaSuccess) return attr_err;
     // Warps per matrix: the smallest per-warp byte bound T for which ceil(units / units per
@@ -851,23 +911,51 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
         units += b.n_tok * J.units;
     }
     b.total_units = (int)units;
+    // Each CTA converts the activations of its own matrices (staged in shared memory) when
+    // that is at most one conversion unit per warp and the rows fit next to the rings: no
+    // conversion launch and no workspace round trip.  More units per CTA cost more than the
+    // launch they save (every CTA would repeat the divisions of the encoder).
+    const int64_t nt = std::min<int64_t>(NT, b.n_tok);
+    int64_t x_need = 0, u_need = 0;
+    for (int c = 0; c < sms; c++) {
+        int64_t xb = 0, ub = 0;
+        for (int j = b.warp_job[c * GV_WARPS]; j <= b.warp_job[c * GV_WARPS + GV_WARPS - 1]; j++) {
+            xb += nt * b.job[j].n_in * 4;
+            ub += nt * b.job[j].units;
+        }
+        x_need = std::max(x_need, xb);
+        u_need = std::max(u_need, ub);
+    }
+    b.fused = u_need <= GV_WARPS && b.off_x + x_need <= 227 * 1024 ? 1 : 0;
+    const size_t smem = b.fused ? (size_t)(b.off_x + x_need) : (size_t)b.off_x;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (b.fused) {
+        // rows split between two warps are added into Y: zero it first
+        for (int j = 0; j < b.n_jobs; j++) {
+            const GemvJob& J = b.job[j];
+            if (J.upr > 1) {
+                const cudaError_t ez = cudaMemsetAsync(J.Y, 0, (size_t)(b.n_tok * J.n_out) * sizeof(float), s);
+                if (ez != cudaSuccess) return ez;
+            }
+        }
+    } else {
     // one row of 4-warp CTAs per matrix, a warp per unit (up to four SMs' worth of CTAs)
     int64_t max_units = 1;
     for (int j = 0; j < b.n_jobs; j++) max_units = std::max<int64_t>(max_units, b.n_tok * b.job[j].units);
     const int64_t act_x = std::min<int64_t>((max_units + 3) / 4, std::max<int64_t>(1, (int64_t)sms * 4 / b.n_jobs));
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t acfg = {};
     acfg.gridDim = dim3((unsigned)act_x, (unsigned)b.n_jobs);
     acfg.blockDim = dim3(128);
     acfg.stream = s;
     acfg.attrs = attr;
     acfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&acfg, k_act_decode, b);
+    const cudaError_t e = cudaLaunchKernelEx(&acfg, k_act_decode, b);
     if (e != cudaSuccess) return e;
-    // the decode kernel, launched as its programmatic dependent: it streams weights (which the
-    // conversion kernel does not touch) before waiting for the converted activations
+    }
+    // the decode kernel, a programmatic dependent of the conversion launch (or, fused, of the
+    // preceding work): it streams weights (which nothing before it writes) before it waits
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sms);
     cfg.blockDim = dim3(GV_WARPS * 32);
@@ -875,7 +963,7 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, b);
+    return b.fused ? cudaLaunchKernelEx(&cfg, k_gemv<NT, true>, b) : cudaLaunchKernelEx(&cfg, k_gemv<NT, false>, b);
 }
 
 // One matrix of a launch.  Rows of a power-of-two number of blocks up to 32 are packed
