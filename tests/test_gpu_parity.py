@@ -148,6 +148,44 @@ def test_quantize_activations_bit_exact(syn, wt):
     assert np.array_equal(d.view(np.uint32), want_d.view(np.uint32))
 
 
+def tie_rows(xt, n_in):
+    """Activation rows whose quotients x / d sit exactly on, or within 2^-24 .. 2^-10 of, the
+    half-integers where rounding turns (d exactly representable: amax = 127 * d)."""
+    rng = np.random.default_rng(77)
+    be = oracle.BLOCK_ELEMS[xt]
+    rows = []
+    for d in (1.0, 0.5, 3.0, 0.375, 2.0 ** -10, 6.103515625e-05):  # the last: fp16-subnormal edge
+        x = np.empty(n_in, np.float64)
+        for b0 in range(0, n_in, be):
+            k = rng.integers(-126, 126, be).astype(np.float64)
+            delta = rng.choice([0.0, 0.0, 2.0 ** -24, -2.0 ** -24, 2.0 ** -16, -2.0 ** -16, 2.0 ** -13, -2.0 ** -13,
+                                2.0 ** -10], be)
+            x[b0:b0 + be] = (k + 0.5 + delta) * d
+            x[b0] = 127.0 * d  # the block maximum: d = amax / 127 exactly
+        rows.append(x.astype(np.float32))
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_K])
+def test_quantize_activations_ties_bit_exact(syn, wt):
+    """Values on and next to rounding ties of x / d: the encoders' multiply-by-reciprocal
+    fast path must fall back to the division exactly where it could round differently."""
+    xt = oracle.VEC_DOT_TYPE[wt]
+    n_in = 1024
+    X = tie_rows(xt, n_in)
+    n_tok = X.shape[0]
+    packed = oracle.quantize(xt, X)
+    qs, d, bs = syn.quantize_activations(wt, dev(X))
+    be, bb = oracle.BLOCK_ELEMS[xt], oracle.BLOCK_BYTES[xt]
+    blocks = packed.reshape(n_tok, n_in // be, bb)
+    off = 2 if xt == oracle.Q8_0 else 4
+    want_q = blocks[:, :, off:off + be].view(np.int8).reshape(n_tok, n_in)
+    assert np.array_equal(host(qs), want_q)
+    # the same rows through syn_quantize (weights path of the same encoders)
+    got = host(syn.quantize(xt, dev(X)))
+    assert np.array_equal(got.reshape(-1), packed.reshape(-1))
+
+
 @pytest.mark.parametrize("wt", TYPES_W)
 def test_block_sums_bit_exact(syn, wt):
     n_out, n_in, n_tok = 9, 1024, 3
