@@ -283,20 +283,31 @@ def gpu_arm(args, rank, world, dist):
         per_mat.append((m, tm))
 
     # ---------------- e2e through the public API, host buffers ----------------
-    xh = [torch.from_numpy(synth.activations(2, i, n_tok, m.n_in)).pin_memory() for i, m in enumerate(mats)]
-    yh = [torch.empty((n_tok, m.n_out)).pin_memory() for m in mats]
-    xd = [torch.empty_like(x, device="cuda") for x in xh]
+    # the layer's seven inputs packed in one pinned host buffer (and the outputs in another):
+    # one host-to-device copy, the grouped call, one device-to-host copy, a synchronize
+    x_off = [0]
+    for m in mats:
+        x_off.append(x_off[-1] + n_tok * m.n_in)
+    y_off = [0]
+    for m in mats:
+        y_off.append(y_off[-1] + n_tok * m.n_out)
+    xh = torch.empty(x_off[-1]).pin_memory()
+    for i, m in enumerate(mats):
+        xh[x_off[i]:x_off[i + 1]] = torch.from_numpy(synth.activations(2, i, n_tok, m.n_in)).reshape(-1)
+    yh = torch.empty(y_off[-1]).pin_memory()
+    xd_all = torch.empty_like(xh, device="cuda")
+    yd_all = torch.empty(y_off[-1], device="cuda")
+    xd = [xd_all[x_off[i]:x_off[i + 1]].view(n_tok, m.n_in) for i, m in enumerate(mats)]
+    yd = [yd_all[y_off[i]:y_off[i + 1]].view(n_tok, m.n_out) for i, m in enumerate(mats)]
     e2e_steps = max(50, min(args.steps, 2000))
-    h2d = sum(x.numel() * 4 for x in xh)
-    d2h = sum(y.numel() * 4 for y in yh)
+    h2d = xh.numel() * 4
+    d2h = yh.numel() * 4
 
     def e2e_step(c):
-        for i in range(len(mats)):
-            xd[i].copy_(xh[i], non_blocking=True)
-        syn.mul_mat_batch([(m.wtype, W[c][i], m.n_out, m.n_in, xd[i], Y[i]) for i, m in enumerate(mats)], n_tok,
+        xd_all.copy_(xh, non_blocking=True)
+        syn.mul_mat_batch([(m.wtype, W[c][i], m.n_out, m.n_in, xd[i], yd[i]) for i, m in enumerate(mats)], n_tok,
                           stream=stream)
-        for i in range(len(mats)):
-            yh[i].copy_(Y[i], non_blocking=True)
+        yh.copy_(yd_all, non_blocking=True)
         stream.synchronize()
 
     for c in range(3):
@@ -368,7 +379,7 @@ def gpu_arm(args, rank, world, dist):
         "single_call_value": {"value": round(single_value, 2), "unit": "GB/s",
                               "note": "same step as 7 separate syn_mul_mat calls (7 launches)"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps},
+                "steps": e2e_steps, "note": "one host-to-device copy of the 7 packed inputs, syn_mul_mat_batch, one device-to-host copy of the packed outputs, a stream synchronize, per step"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "prefill": {"workload": "llama8b_ffn_q4_k_prefill_512", "value": round(pre_tflops, 1), "unit": "TFLOP/s",
