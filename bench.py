@@ -317,6 +317,25 @@ def gpu_arm(args, rank, world, dist):
         e2e_step(k % n_copies)
     e2e_t = time.perf_counter() - s0
     e2e_value = alg_bytes * e2e_steps * world / e2e_t / 1e9
+    # the same step captured in a CUDA graph (copies and launches), one replay + a synchronize
+    # per step, as a decode loop would run it
+    e2e_graphs = []
+    for c in range(n_copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            xd_all.copy_(xh, non_blocking=True)
+            syn.mul_mat_batch([(m.wtype, W[c][i], m.n_out, m.n_in, xd[i], yd[i]) for i, m in enumerate(mats)],
+                              n_tok, stream=stream)
+            yh.copy_(yd_all, non_blocking=True)
+        e2e_graphs.append(g)
+    for c in range(3):
+        e2e_graphs[c % n_copies].replay()
+        stream.synchronize()
+    s0 = time.perf_counter()
+    for k in range(e2e_steps):
+        e2e_graphs[k % n_copies].replay()
+        stream.synchronize()
+    e2e_graph_value = alg_bytes * e2e_steps * world / (time.perf_counter() - s0) / 1e9
 
     # ---------------- prefill: Llama-8B FFN up/down, Q4_K, 512 tokens ----------------
     pre = workloads.LLAMA8B_FFN
@@ -380,6 +399,9 @@ def gpu_arm(args, rank, world, dist):
                               "note": "same step as 7 separate syn_mul_mat calls (7 launches)"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "note": "one host-to-device copy of the 7 packed inputs, syn_mul_mat_batch, one device-to-host copy of the packed outputs, a stream synchronize, per step"},
+        "e2e_cuda_graph": {"value": round(e2e_graph_value, 2), "unit": "GB/s",
+                           "note": "the e2e step (copy in, grouped call, copy out) captured in a CUDA graph; "
+                                   "one replay and a stream synchronize per step"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "prefill": {"workload": "llama8b_ffn_q4_k_prefill_512", "value": round(pre_tflops, 1), "unit": "TFLOP/s",
