@@ -411,3 +411,58 @@ def test_mul_mat_on_weights_from_a_gguf_file(syn, tmp_path, n_tok):
             deq = oracle.dequantize(t, qs[name], n_in).astype(np.float64)
             bound = 1e-4 * np.linalg.norm(deq, axis=1)[None, :] * np.linalg.norm(X.astype(np.float64), axis=1)[:, None]
             assert np.all(np.abs(Y - ref) <= bound), name
+
+
+def test_reader_survives_fuzzed_files(syn, tmp_path):
+    """Random corruptions of valid files (byte flips, overwritten length and count fields,
+    truncations, appended garbage): the reader returns either a handle or SYN_ERR_FORMAT,
+    never reads outside the mapping (a crash would end the test process), and every tensor of
+    a file it accepts lies inside the file."""
+    import ctypes
+    rng = np.random.default_rng(4242)
+    kv, tensors = random_content(rng)
+    base = G.serialize(kv, tensors, alignment=64)
+    golden = golden_files()
+    seeds = [base, golden["file_a"], golden["file_b"]]
+    path = str(tmp_path / "fuzz.gguf")
+    opened = 0
+    for it in range(1500):
+        data = bytearray(seeds[it % len(seeds)])
+        kind = it % 5
+        if kind == 0:  # flip a few random bytes
+            for _ in range(int(rng.integers(1, 8))):
+                data[int(rng.integers(0, len(data)))] ^= int(rng.integers(1, 256))
+        elif kind == 1:  # overwrite a u64 at a random 8-aligned header/metadata position
+            at = int(rng.integers(0, min(len(data) - 8, 512)))
+            vals = [0, 1, 2**31, 2**32, 2**40, 2**63, 2**64 - 1]
+            data[at:at + 8] = struct.pack("<Q", vals[int(rng.integers(0, len(vals)))])
+        elif kind == 2:  # truncate
+            del data[int(rng.integers(0, len(data))):]
+        elif kind == 3:  # append garbage
+            data += bytes(rng.integers(0, 256, int(rng.integers(1, 200))).astype(np.uint8))
+        else:  # overwrite a u32 (types, dimension counts, alignment)
+            at = int(rng.integers(0, min(len(data) - 4, 512)))
+            vals = [0, 1, 4, 5, 9, 13, 99, 2**31]
+            data[at:at + 4] = struct.pack("<I", vals[int(rng.integers(0, len(vals)))])
+        with open(path, "wb") as f:
+            f.write(bytes(data))
+        st = ctypes.c_int(0)
+        h = syn.syn_gguf_open(path.encode(), ctypes.byref(st))
+        if not h:
+            assert st.value == syn.ERR_FORMAT, (it, st.value)
+            continue
+        opened += 1
+        try:
+            n = syn.syn_gguf_n_tensors(h)
+            ds = syn.syn_gguf_data_start(h)
+            for i in range(n):
+                nb, off = ctypes.c_int64(), ctypes.c_uint64()
+                assert syn.syn_gguf_tensor_info(h, i, None, None, None, None, ctypes.byref(off), None,
+                                                ctypes.byref(nb)) == syn.OK
+                if nb.value >= 0:
+                    assert ds + off.value + nb.value <= len(data)
+            for i in range(syn.syn_gguf_n_kv(h)):
+                assert syn.syn_gguf_kv_info(h, i, None, None, None, None) == syn.OK
+        finally:
+            syn.syn_gguf_close(h)
+    assert opened > 0
