@@ -175,12 +175,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 
 // Signed 4-way byte dot product.  The 4- and 6-bit weight codes (0..63) are below 128,
 // so they read the same as signed bytes.
-// Prefetch [src, src + bytes) into L2 (no completion tracking).  src 16-byte aligned,
-// bytes a multiple of 16.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
     return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
 }

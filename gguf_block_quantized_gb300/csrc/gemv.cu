@@ -74,7 +74,6 @@ struct GemvJob {
     int lg_nb;              // log2(nb) when rows are packed several per warp step, else -1
     int nbx;                // activation blocks per row
     int units;              // conversion-kernel units (warp steps) per token
-    int unit_begin;         // first conversion unit of this matrix (all tokens of earlier ones)
     int warp_begin, warp_end;  // the decode warps of this matrix
     int upr;                // work units per row: 1 (whole rows), or 2 for rows of two stages
                             // runs: the two runs may go to different warps and are then added
@@ -90,7 +89,6 @@ struct GemvJob {
 struct GemvBatch {
     GemvJob job[GEMV_MAX_JOBS];
     int n_jobs;
-    int total_units;        // conversion-kernel units of all matrices and tokens
     int64_t total_bytes;
     int64_t n_tok;
     int* err;
@@ -109,13 +107,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // Sum over aligned groups of 2^lg lanes (lg <= 5).
-__device__ __forceinline__ float group_sum(float v, int lg) {
-#pragma unroll
-    for (int k = 0; k < 5; k++)
-        if (k < lg) v += __shfl_xor_sync(0xffffffffu, v, 1 << k);
-    return v;
-}
-
 // Window of packed warp steps whose row sums are reduced together: 8 / NT steps.
 template <int NT>
 struct Win {
@@ -903,14 +894,10 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
     // the conversion kernel: a programmatic dependent of the preceding work on the stream
     // (it waits for that work to finish before touching memory); a previous decode launch
     // releases it early, so its launch latency overlaps that launch's tail
-    int64_t units = 0;
     for (int j = 0; j < b.n_jobs; j++) {
         GemvJob& J = b.job[j];
         J.units = small_block(J.type) ? (J.nbx + 3) / 4 : J.nbx;
-        J.unit_begin = (int)units;
-        units += b.n_tok * J.units;
     }
-    b.total_units = (int)units;
     // Each CTA converts the activations of its own matrices (staged in shared memory) when
     // that is at most one conversion unit per warp and the rows fit next to the rings: no
     // conversion launch and no workspace round trip.  More units per CTA cost more than the
