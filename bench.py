@@ -138,6 +138,17 @@ def recorded_traffic(summary: str, source: str):
     return int(m.group(1))
 
 
+def max_over_ranks(t: float, dist, device: str = "cuda") -> float:
+    """The largest of the ranks' elapsed times (every rank gets it): a whole-job figure is the
+    work of all ranks over the time of the slowest one."""
+    if dist is None:
+        return t
+    import torch
+    tt = torch.tensor([t], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
 def time_graphs(torch, graphs, steps, stream, tail=None):
     """Seconds for `steps` replays (cycling over graphs), plus one replay of `tail`."""
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -239,10 +250,7 @@ def gpu_arm(args, rank, world, dist):
         while len(clk.lines) < 5 and extra < 40:
             timed_steps()
             extra += 1
-    if dist:
-        tt = torch.tensor([t], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
+    t = max_over_ranks(t, dist)
     value = alg_bytes * args.steps * world / t / 1e9
     ms_per_step = t / args.steps * 1e3
     n_ps = max(100, args.steps // 4)
@@ -315,7 +323,7 @@ def gpu_arm(args, rank, world, dist):
     s0 = time.perf_counter()
     for k in range(e2e_steps):
         e2e_step(k % n_copies)
-    e2e_t = time.perf_counter() - s0
+    e2e_t = max_over_ranks(time.perf_counter() - s0, dist)
     e2e_value = alg_bytes * e2e_steps * world / e2e_t / 1e9
     # the same step captured in a CUDA graph (copies and launches), one replay + a synchronize
     # per step, as a decode loop would run it
@@ -335,7 +343,7 @@ def gpu_arm(args, rank, world, dist):
     for k in range(e2e_steps):
         e2e_graphs[k % n_copies].replay()
         stream.synchronize()
-    e2e_graph_value = alg_bytes * e2e_steps * world / (time.perf_counter() - s0) / 1e9
+    e2e_graph_value = alg_bytes * e2e_steps * world / max_over_ranks(time.perf_counter() - s0, dist) / 1e9
 
     # ---------------- prefill: Llama-8B FFN up/down, Q4_K, 512 tokens ----------------
     pre = workloads.LLAMA8B_FFN
