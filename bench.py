@@ -637,6 +637,80 @@ def oracle_arm(budget_s: float, max_steps: int | None = None):
                       f"row-split over {cores} threads"}, done, el
 
 
+def oracle_configs(budget_s: float = 4.0):
+    """The oracle (CPU, this machine's cores) on every benchmark configuration: single thread
+    on the decode configurations, row-split over all cores on the 512-token prefill, and on a
+    sampled subset of the Llama-8B sweep (64 rows x 16 tokens of each distinct matrix shape,
+    extrapolated to the whole sweep by the number of multiply-adds).  Each measurement runs
+    for about budget_s seconds.  Weights are blocks of the real formats; their values do not
+    change the oracle's speed, so a matrix is one quantized 128-row slice repeated."""
+    import numpy as np
+
+    import oracle
+    from gguf_block_quantized_gb300 import synth, workloads
+
+    cores = os.cpu_count() or 1
+
+    def weights(m, seed):
+        rows = min(128, m.n_out)
+        q = oracle.quantize(m.wtype, synth.normal(seed, (rows, m.n_in), 0.02))
+        return np.ascontiguousarray(np.tile(q, (-(-m.n_out // rows), 1))[:m.n_out])
+
+    def timed(fn):
+        n, t0 = 0, time.perf_counter()
+        while True:
+            fn()
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                return el / n
+
+    out = {"cores": cores}
+    for name, mats, n_tok, threads in (("q8_0_2048x2048_decode", workloads.Q8_0_SQUARE, 1, 1),
+                                       ("llama1b_layer_decode", workloads.LLAMA1B_LAYER, 1, 1),
+                                       ("q6_k_lm_head_decode_1tok", workloads.LM_HEAD_1B, 1, 1),
+                                       ("q6_k_lm_head_decode_4tok", workloads.LM_HEAD_1B, 4, 1)):
+        Ws = [weights(m, 900 + i) for i, m in enumerate(mats)]
+        Xs = [synth.normal(950 + i, (n_tok, m.n_in)) for i, m in enumerate(mats)]
+        t = timed(lambda: [oracle.mul_mat(m.wtype, Ws[i], m.n_out, m.n_in, Xs[i], n_threads=threads)
+                           for i, m in enumerate(mats)])
+        alg = sum(workloads.gemv_bytes(m, n_tok) for m in mats)
+        out[name] = {"value": round(alg / t / 1e9, 4), "unit": "GB/s", "threads": threads, "s_per_pass": round(t, 4)}
+    # 512-token prefill of the FFN up matrix, rows split over all cores
+    m = workloads.LLAMA8B_FFN[0]
+    W = weights(m, 960)
+    X = synth.normal(961, (512, m.n_in))
+    t = timed(lambda: oracle.mul_mat(m.wtype, W, m.n_out, m.n_in, X, n_threads=cores))
+    out["q4_k_14336x4096_prefill_512tok"] = {"value": round(workloads.gemm_flops(m, 512) / t / 1e12, 5),
+                                             "unit": "TFLOP/s", "threads": cores, "s_per_pass": round(t, 3)}
+    # the Llama-8B sweep: sampled entries of each distinct shape, extrapolated
+    mats = workloads.llama8b_q4_k_m()
+    shapes = {}
+    for mm in mats:
+        shapes[(mm.wtype, mm.n_out, mm.n_in)] = shapes.get((mm.wtype, mm.n_out, mm.n_in), 0) + 1
+    rng = np.random.default_rng(962)
+    for n_tok, key in ((1, "llama8b_q4_k_m_decode_1tok"), (2048, "llama8b_q4_k_m_prefill_2048tok")):
+        t_all, macs_all = 0.0, 0
+        for (wt, n_out, n_in), count in shapes.items():
+            mm = workloads.Matrix("s", wt, n_out, n_in)
+            W = weights(mm, 963)
+            X = synth.normal(964, (n_tok, n_in))
+            rows = np.sort(rng.choice(n_out, 64, replace=False))
+            toks = np.sort(rng.choice(n_tok, min(16, n_tok), replace=False))
+            t = timed(lambda: oracle.mul_mat_sampled(wt, W, n_out, n_in, X, rows, toks)) if budget_s > 0 else 0.0
+            frac = (rows.size * toks.size) / (n_out * n_tok)  # sampled share of the outputs
+            t_all += count * t / frac
+            macs_all += count * n_out * n_in * n_tok
+        if n_tok == 1:
+            alg = sum(workloads.gemv_bytes(mm, 1) for mm in mats)
+            out[key] = {"value": round(alg / t_all / 1e9, 4), "unit": "GB/s", "threads": 1,
+                        "note": "extrapolated from 64 sampled rows of each distinct shape"}
+        else:
+            out[key] = {"value": round(2 * macs_all / t_all / 1e12, 6), "unit": "TFLOP/s", "threads": 1,
+                        "note": "extrapolated from 64 rows x 16 tokens of each distinct shape"}
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -645,12 +719,19 @@ def main():
     ap.add_argument("--impl", default="syn", choices=["syn", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--quick", action="store_true", help="skip the Llama-8B weight sweep")
+    ap.add_argument("--oracle-configs", action="store_true",
+                    help="time the CPU oracle on every configuration (no GPU work) and print one JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+
+    if args.oracle_configs:
+        if rank == 0:
+            print(json.dumps({"oracle_configs": oracle_configs(budget_s=args.cpu_budget / 2)}), flush=True)
+        return
 
     if args.impl == "reference":
         if rank != 0:
