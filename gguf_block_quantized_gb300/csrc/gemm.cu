@@ -20,9 +20,12 @@
 //               tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16) from one thread;
 //   warp 2      activation producer: 2-D TMA loads of x~ tiles (BN x 64, 128-byte swizzle)
 //               into a 3-deep operand ring (it alone waits for the conversion kernel);
-//   warps 3-10  dequantize: raw blocks -> fp16 A tile (128 x 64) in the canonical K-major
-//               128-byte-swizzled layout the MMA descriptor reads, in half2 arithmetic;
-//   warps 11-14 epilogue: tcgen05.ld 32x32b from TMEM, store (or add, when split) to Y.
+//   warps 3-18  dequantize, two teams of 8 taking alternate 64-k steps: raw blocks -> fp16
+//               A tile (128 x 64) in the canonical K-major 128-byte-swizzled layout the MMA
+//               descriptor reads, in half2 arithmetic (F16 weights: no dequantization, warp 0
+//               loads the fp16 tile by TMA straight into that layout);
+//   warps 19-22 epilogue: tcgen05.ld 32x32b from TMEM, then per warp a 32 x 16 staging box
+//               and one 2-D TMA store (or reduce-add, when split along K) to Y.
 // All hand-offs are mbarriers; every wait is bounded (clock64) and gives up with a
 // recorded error instead of hanging.  Index arithmetic is 32-bit: 64-bit division runs on
 // the fp64 pipe.

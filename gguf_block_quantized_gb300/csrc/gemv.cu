@@ -21,12 +21,15 @@
 //      It does so before waiting for the conversion launch, then releases the next launch
 //      on the stream (whose own weight copies then overlap this launch's tail).
 //   2. One thread bulk-copies the converted activations of the CTA's matrices into shared
-//      memory.
-//   3. Each lane decodes whole blocks (one per warp step): unpacks 4/6/8-bit codes in
-//      registers, forms the integer sub-block dots with dp4a, applies the integer sub-block
-//      scales and then the fp32 block scales.  Rows of at most 32 blocks are spread over
-//      groups of lanes (several rows per step, reduced within the group); wider rows take
-//      several steps and a whole-warp reduction.
+//      memory.  When every CTA needs at most one conversion unit per warp (narrow inputs,
+//      few tokens), there is no conversion launch: the CTA bulk-copies its fp32 activation
+//      rows into shared memory and its warps run the encoder there (k_gemv<NT, true>).
+//   3. Each lane decodes half a K-quant block or two 32-weight blocks per warp step: unpacks
+//      4/5/6/8-bit codes in registers, forms the integer sub-block dots with dp4a, applies
+//      the integer sub-block scales and then the fp32 block scales.  Rows of at most 32
+//      blocks are spread over aligned groups of lanes, several rows per step; the partial
+//      sums of a window of steps are reduced together (a transposed butterfly) and stored by
+//      one coalesced store.  Wider rows take several steps and a whole-warp reduction.
 #include <algorithm>
 #include <mutex>
 
