@@ -22,6 +22,8 @@ namespace {
 using syn::launch_act_half;
 
 std::atomic<long long> g_launches{0};
+// Decode/prefill threshold: -1 = per format (decode_max_tok), else the same n for every
+// format (syn_set_gemv_max_tok, or SYN_GEMV_MAX_TOK in the environment at load time)
 std::atomic<int> g_gemv_max_tok{[] {
     const char* e = std::getenv("SYN_GEMV_MAX_TOK");
     if (e && *e) {
@@ -29,8 +31,20 @@ std::atomic<int> g_gemv_max_tok{[] {
         long v = std::strtol(e, &end, 10);
         if (end && *end == 0 && v >= 0 && v < (1 << 30)) return (int)v;
     }
-    return 8;
+    return -1;
 }()};
+
+// Largest n_tok that runs on the decode kernels.  Per format, the measured crossover with
+// the tensor-core prefill on GB300 (decode re-reads the weights per group of 8 tokens and
+// its per-token work is larger for the 32-weight formats and F16): K-quants 8, Q8_0 / Q4_0
+// / Q5_0 4, F16 2.
+int decode_max_tok(int type) {
+    const int v = g_gemv_max_tok.load();
+    if (v >= 0) return v;
+    if (type == SYN_TYPE_Q4_K || type == SYN_TYPE_Q6_K) return 8;
+    if (type == SYN_TYPE_F16) return 2;
+    return 4;
+}
 
 std::atomic<int> g_det{0};       // deterministic mode (syn_set_deterministic)
 std::atomic<int> g_sm_limit{0};  // 0: every SM
@@ -180,10 +194,7 @@ const char* syn_strerror(int status) {
 
 int64_t syn_launch_count(void) { return g_launches.load(); }
 
-int syn_set_gemv_max_tok(int n) {
-    if (n < 0) return -1;
-    return g_gemv_max_tok.exchange(n);
-}
+int syn_set_gemv_max_tok(int n) { return g_gemv_max_tok.exchange(n < 0 ? -1 : n); }
 
 int syn_set_deterministic(int on) { return g_det.exchange(on ? 1 : 0); }
 
@@ -290,7 +301,7 @@ int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in, const floa
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool det = g_det.load() != 0;
-    if (type == SYN_TYPE_F16 && (det || n_tok <= g_gemv_max_tok.load())) {
+    if (type == SYN_TYPE_F16 && (det || n_tok <= decode_max_tok(type))) {
         void* ws;
         rc = workspace_for(s, (size_t)(n_tok * n_in * 2 + 256), &ws);
         if (rc) return rc;
@@ -300,7 +311,7 @@ int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in, const floa
     }
     const bool fits = syn::gemv_act_bytes(type, n_in) <= syn::gemv_act_limit();
     if (det && !fits) return SYN_ERR_SHAPE;
-    if (det || (n_tok <= g_gemv_max_tok.load() && fits)) {
+    if (det || (n_tok <= decode_max_tok(type) && fits)) {
         const syn::GemvDesc d{type, W, n_out, n_in, X, Y};
         void* ws;
         rc = workspace_for(s, (size_t)syn::gemv_workspace_bytes(1, &d, n_tok), &ws);
@@ -342,14 +353,6 @@ int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_strea
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool det = g_det.load() != 0;
-    if (n_tok > g_gemv_max_tok.load()) {
-        for (int i = 0; i < n; i++) {
-            rc = syn_mul_mat(descs[i].type, descs[i].W, descs[i].n_out, descs[i].n_in, descs[i].X, n_tok, descs[i].Y,
-                             stream);
-            if (rc) return rc;
-        }
-        return SYN_OK;
-    }
     // pack the products into launches within the decode kernel's activation and job limits
     syn::GemvDesc group[syn::GEMV_MAX_JOBS];
     int ng = 0;
@@ -368,7 +371,9 @@ int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_strea
     for (int i = 0; i < n; i++) {
         const syn_mat_desc& d = descs[i];
         const int64_t a = d.type == SYN_TYPE_F16 ? 0 : syn::gemv_act_bytes(d.type, d.n_in);
-        if (d.type == SYN_TYPE_F16 || a > syn::gemv_act_limit()) {  // own launch (F16 decode, or too wide)
+        // its own call: F16, rows too wide for the decode kernel, or (outside the deterministic
+        // mode) more tokens than its format decodes
+        if (d.type == SYN_TYPE_F16 || a > syn::gemv_act_limit() || (!det && n_tok > decode_max_tok(d.type))) {
             rc = syn_mul_mat(d.type, d.W, d.n_out, d.n_in, d.X, n_tok, d.Y, stream);
             if (rc) return rc;
             continue;

@@ -141,9 +141,10 @@ SYN_API int syn_quantize_activations(int wtype, const float* X, int64_t n_tok, i
 
 /* Y = ggml_mul_mat(W, X) as described at the top of this file.
  * type: Q8_0, Q4_K, Q6_K, Q4_0, Q5_0 or F16 (Q8_K is activation-only: SYN_ERR_TYPE).
- * n_tok <= the decode threshold (default 8, see syn_set_gemv_max_tok) runs the decode
- * kernel: one launch that quantizes X in shared memory and streams W once per group of
- * up to 8 tokens.  Larger n_tok runs the prefill path: one kernel quantizes X and writes
+ * n_tok <= the decode threshold (per format by default: 8 for Q4_K and Q6_K, 4 for Q8_0,
+ * Q4_0 and Q5_0, 2 for F16; see syn_set_gemv_max_tok) runs the decode kernel: one
+ * launch that quantizes X in shared memory and streams W once per group of up to 8
+ * tokens.  Larger n_tok runs the prefill path: one kernel quantizes X and writes
  * the dequantized fp16 activations into the library workspace, a second runs the
  * tensor-core GEMM on W tiles dequantized to fp16 in shared memory (fp32 accumulation).
  * Accuracy: |y - y_ref| <= 1e-4 * ||dequant(w_row)||_2 * ||x||_2 per element, where
@@ -157,7 +158,7 @@ SYN_API int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in,
 
 /* One product of a group (see syn_mul_mat_batch). */
 typedef struct {
-    int type;          /* a weight format: Q8_0, Q4_K, Q6_K, Q4_0 or Q5_0 */
+    int type;          /* a weight format: Q8_0, Q4_K, Q6_K, Q4_0, Q5_0 or F16 */
     const void* W;     /* n_out x n_in weights, 16-byte aligned */
     int64_t n_out;
     int64_t n_in;
@@ -166,12 +167,13 @@ typedef struct {
 } syn_mat_desc;
 
 /* n independent products Y_i = ggml_mul_mat(W_i, X_i), all with n_tok tokens: the same
- * result as n calls of syn_mul_mat.  In decode (n_tok <= the decode threshold) the group
- * runs in as few launches as the decode kernel's limits allow (at most 16 matrices and
- * 56 KiB of converted activations per launch), so the products of a layer (q, k, v, o,
- * gate, up, down) share one launch and all SMs stream their weights together.  Larger
- * n_tok runs each product on the prefill path.  Arguments are checked as for syn_mul_mat
- * before anything is enqueued.  Asynchronous. */
+ * result as n calls of syn_mul_mat.  The quantized products with n_tok <= their format's
+ * decode threshold (see syn_mul_mat) run in as few launches as the decode kernel's limits
+ * allow (at most 16 matrices and 56 KiB of converted activations per launch), so the
+ * products of a layer (q, k, v, o, gate, up, down) share one launch and all SMs stream
+ * their weights together.  The others (F16, rows too wide for the decode kernel, or more
+ * tokens than the format decodes) run one by one as in syn_mul_mat.  Arguments are checked
+ * as for syn_mul_mat before anything is enqueued.  Asynchronous. */
 SYN_API int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_stream_t stream);
 
 /* Pre-size the prefill workspace of (current device, stream) for products with up to
@@ -191,10 +193,12 @@ SYN_API int syn_release(void);
 SYN_API int syn_block_sums(int type, const void* W, int64_t n_out, int64_t n_in,
                    const void* Xq, int64_t n_tok, int32_t* S, syn_stream_t stream);
 
-/* Decode/prefill threshold: products with n_tok <= n use the decode kernel.  n >= 0;
- * 0 forces the prefill path for every n_tok >= 1.  Returns the previous value.
- * Process-wide; the default is 8, or the value of the environment variable
- * SYN_GEMV_MAX_TOK when the library is loaded. */
+/* Decode/prefill threshold.  By default (n < 0) it depends on the format: products with
+ * n_tok <= 8 (Q4_K, Q6_K), <= 4 (Q8_0, Q4_0, Q5_0) or <= 2 (F16) use the decode kernels,
+ * larger ones the tensor-core prefill (the measured crossovers on GB300).  n >= 0 sets the
+ * same threshold for every format (0 forces the prefill path for every n_tok >= 1).
+ * Returns the previous value (-1: per format).  Process-wide; the environment variable
+ * SYN_GEMV_MAX_TOK, when set at load time, gives the initial value. */
 SYN_API int syn_set_gemv_max_tok(int n);
 
 /* Deterministic mode (on != 0; process-wide, default off; returns the previous setting).

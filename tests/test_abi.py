@@ -49,8 +49,10 @@ def test_host_functions(lib):
     assert lib.syn_row_bytes(3, 100) == -1 and lib.syn_row_bytes(1, 0) == -1
     assert lib.syn_strerror(lib.ERR_ALIGN).decode().startswith("pointer")
     old = lib.syn_set_gemv_max_tok(5)
+    if not os.environ.get("SYN_GEMV_MAX_TOK"):
+        assert old == -1  # per-format thresholds by default
     assert lib.syn_set_gemv_max_tok(old) == 5
-    assert lib.syn_set_gemv_max_tok(-1) == -1
+    assert lib.syn_set_gemv_max_tok(-7) == old and lib.syn_set_gemv_max_tok(old) == -1
     assert lib.syn_set_deterministic(7) == 0 and lib.syn_set_deterministic(0) == 1
     assert lib.syn_set_sm_limit(-1) == -1
     assert lib.syn_set_sm_limit(5) == 0 and lib.syn_set_sm_limit(0) == 5

@@ -469,6 +469,31 @@ def test_sm_limit_parity(syn, lim):
     assert syn.device_status() == syn.OK
 
 
+@pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q6_K, oracle.Q8_0, oracle.Q4_0, oracle.Q5_0, oracle.F16])
+def test_default_per_format_threshold(syn, wt):
+    """The default (per-format) decode/prefill choice: token counts on both sides of each
+    format's crossover, single and grouped, against the oracle."""
+    n_out, n_in = 136, 768
+    Wq = oracle.quantize(wt, synth.normal(40 + wt, (n_out, n_in), 0.02))
+    old = syn.set_gemv_max_tok(-1)
+    try:
+        for n_tok in (1, 2, 3, 4, 5, 8, 9):
+            X = synth.normal(50 + n_tok, (n_tok, n_in))
+            ref = oracle.mul_mat(wt, Wq, n_out, n_in, X)
+            bound = tolerance(wt, Wq, n_in, X)
+            assert_close(host(syn.mul_mat(wt, dev(Wq), n_out, n_in, dev(X))), ref, bound, f"type {wt} n_tok {n_tok}")
+            Wd, Xd = dev(Wq), dev(X)
+            Y1, Y2 = (torch.full((n_tok, n_out), np.nan, device="cuda") for _ in range(2))
+            syn.mul_mat_batch([(wt, Wd, n_out, n_in, Xd, Y1), (oracle.Q4_K, Wd if wt == oracle.Q4_K else
+                               dev(oracle.quantize(oracle.Q4_K, synth.normal(60, (n_out, n_in), 0.02))),
+                               n_out, n_in, Xd, Y2)], n_tok)
+            assert_close(host(Y1), ref, bound, f"batch type {wt} n_tok {n_tok}")
+            assert np.isfinite(host(Y2)).all()
+    finally:
+        assert syn.set_gemv_max_tok(old) == -1
+    assert syn.device_status() == syn.OK
+
+
 def test_mul_mat_zero_and_degenerate(syn):
     wt, n_out, n_in = oracle.Q4_K, 40, 512
     Wq = oracle.quantize(wt, inputs_mixed(n_out, n_in, 3))
@@ -507,7 +532,7 @@ def sampled_check(syn, m, n_tok, workload, index, n_rows=48, n_toks=4, path=None
     W32 = synth.weight(workload, index, m.n_out, m.n_in)
     X = synth.activations(workload, index, n_tok, m.n_in)
     Wq = oracle.quantize(m.wtype, W32)
-    old = syn.set_gemv_max_tok(8) if path is None else syn.set_gemv_max_tok(1 << 20 if path == "gemv" else 0)
+    old = syn.set_gemv_max_tok(-1 if path is None else (1 << 20 if path == "gemv" else 0))
     try:
         Y = host(syn.mul_mat(m.wtype, dev(Wq), m.n_out, m.n_in, dev(X)))
     finally:
