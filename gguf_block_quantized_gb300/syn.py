@@ -185,12 +185,38 @@ def mul_mat(t: int, W, n_out: int, n_in: int, X, Y=None, stream=None):
     return Y
 
 
-def mul_mat_batch(items, n_tok: int, stream=None):
-    """items: list of (type, W, n_out, n_in, X, Y) with torch CUDA tensors; one grouped call."""
+def _descs(items):
     arr = (MatDesc * len(items))()
     for k, (t, W, n_out, n_in, X, Y) in enumerate(items):
         arr[k] = MatDesc(t, _ptr(W), n_out, n_in, _ptr(X), _ptr(Y))
-    check(syn_mul_mat_batch(len(items), arr, n_tok, _stream(stream)), "syn_mul_mat_batch")
+    return arr
+
+
+def mul_mat_batch(items, n_tok: int, stream=None):
+    """items: list of (type, W, n_out, n_in, X, Y) with torch CUDA tensors; one grouped call."""
+    check(syn_mul_mat_batch(len(items), _descs(items), n_tok, _stream(stream)), "syn_mul_mat_batch")
+
+
+class PreparedBatch:
+    """A grouped call whose arguments stay the same from call to call (a decode loop over fixed
+    buffers): the descriptor array and the stream handle are marshalled once, and each call is
+    the one syn_mul_mat_batch call.  Holds references to the tensors it points at."""
+
+    def __init__(self, items, n_tok: int, stream=None):
+        self._items = list(items)
+        self._arr = _descs(self._items)
+        self._n = len(self._items)
+        self._n_tok = n_tok
+        self._stream = _stream(stream)
+
+    def __call__(self):
+        rc = syn_mul_mat_batch(self._n, self._arr, self._n_tok, self._stream)
+        if rc:
+            check(rc, "syn_mul_mat_batch")
+
+
+def prepare_batch(items, n_tok: int, stream=None) -> PreparedBatch:
+    return PreparedBatch(items, n_tok, stream)
 
 
 def block_sums(t: int, W, n_out: int, n_in: int, Xq, n_tok: int, stream=None):

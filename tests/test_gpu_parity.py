@@ -267,6 +267,29 @@ def test_mul_mat_batch_mixed_group(syn, n_tok):
     assert syn.device_status() == syn.OK
 
 
+def test_prepared_batch_matches_grouped_call(syn):
+    """The prepared grouped call (descriptors marshalled once) runs the same launches as
+    mul_mat_batch: bit-identical outputs, and repeated calls see updated inputs."""
+    shapes = [(oracle.Q4_K, 512, 2048), (oracle.Q6_K, 256, 2048), (oracle.Q8_0, 300, 1024)]
+    Ws = [dev(oracle.quantize(wt, synth.normal(70 + k, (n_out, n_in), 0.02))) for k, (wt, n_out, n_in) in enumerate(shapes)]
+    for n_tok in (1, 3):
+        Xs = [dev(synth.normal(80 + k, (n_tok, n_in))) for k, (_, _, n_in) in enumerate(shapes)]
+        Ya = [torch.full((n_tok, n_out), np.nan, device="cuda") for _, n_out, _ in shapes]
+        Yb = [torch.full((n_tok, n_out), np.nan, device="cuda") for _, n_out, _ in shapes]
+        syn.mul_mat_batch([(wt, W, n_out, n_in, X, Y) for (wt, n_out, n_in), W, X, Y in zip(shapes, Ws, Xs, Ya)], n_tok)
+        pb = syn.prepare_batch([(wt, W, n_out, n_in, X, Y) for (wt, n_out, n_in), W, X, Y in zip(shapes, Ws, Xs, Yb)],
+                               n_tok, stream=torch.cuda.current_stream())
+        pb()
+        for a, b in zip(Ya, Yb):
+            assert torch.equal(a, b)
+        for X in Xs:
+            X.mul_(-1.0)  # the next call reads the new contents of the same buffers
+        pb()
+        for a, b in zip(Ya, Yb):
+            assert torch.equal(-a, b)
+    assert syn.device_status() == syn.OK
+
+
 def test_mul_mat_orientation_example_exact(syn):
     """ggml_mul_mat(A, B^T) = C^T with the examples/simple integers, exact on both paths."""
     A = np.array([[2, 8], [5, 1], [4, 2], [8, 6]], np.float32)
