@@ -31,6 +31,7 @@
 //      sums of a window of steps are reduced together (a transposed butterfly) and stored by
 //      one coalesced store.  Wider rows take several steps and a whole-warp reduction.
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "kernels.h"
@@ -791,36 +792,10 @@ static int64_t act_bytes_per_token(int type, int64_t n_in) {
     return n_in + ds * 4 + sum_bytes(type, n_in);
 }
 
-template <int NT>
-static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
-    sms = std::min(sms, GV_MAX_SMS);  // one CTA per SM, up to the size of the warp table
-    int64_t off = 0;
-    for (int j = 0; j < b.n_jobs; j++) {
-        GemvJob& J = b.job[j];
-        J.act_q = (int)off;
-        off = up16(off + (int64_t)NT * J.n_in);
-        J.act_d = (int)off;
-        off = up16(off + (int64_t)NT * J.ds * 4);
-        J.act_s = (int)off;
-        off = up16(off + (int64_t)NT * sum_bytes(J.type, J.n_in));
-    }
-    off = (off + 127) & ~int64_t(127);
-    b.off_stage = (int)off;
-    off += (int64_t)GV_WARPS * GV_NS * GV_SLOT;
-    b.off_bar = (int)off;
-    off += GV_WARPS * GV_NS * 8;
-    b.off_flag = (int)off;
-    off += 16;  // abort flag, activation barrier
-    if (off > 227 * 1024) return cudaErrorInvalidConfiguration;
-    b.off_x = (int)up16(off);
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(k_gemv<NT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(k_gemv<NT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+// Work partition of a launch: warps per matrix (and whether long rows are split into two
+// runs), the warp -> matrix table, and whether the CTAs convert their own activations.
+// x_need: the shared memory the fused conversion stages per CTA.
+static cudaError_t plan_partition(GemvBatch& b, int sms, int NT, int64_t& x_need) {
     // Warps per matrix: the smallest per-warp byte bound T for which ceil(units / units per
     // warp) warps of every matrix fit in the grid (units per warp = floor(T / unit bytes)),
     // found by bisection; the warps left over go to the matrices in proportion to bytes.
@@ -906,7 +881,8 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
     // conversion launch and no workspace round trip.  More units per CTA cost more than the
     // launch they save (every CTA would repeat the divisions of the encoder).
     const int64_t nt = std::min<int64_t>(NT, b.n_tok);
-    int64_t x_need = 0, u_need = 0;
+    int64_t u_need = 0;
+    x_need = 0;
     for (int c = 0; c < sms; c++) {
         int64_t xb = 0, ub = 0;
         for (int j = b.warp_job[c * GV_WARPS]; j <= b.warp_job[c * GV_WARPS + GV_WARPS - 1]; j++) {
@@ -917,6 +893,109 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
         u_need = std::max(u_need, ub);
     }
     b.fused = u_need <= GV_WARPS && b.off_x + x_need <= 227 * 1024 ? 1 : 0;
+    return cudaSuccess;
+}
+
+// The partition is a pure function of the shapes, and a decode loop repeats the same shapes
+// every step; the bisection costs about as much host time as a launch, so the last few
+// partitions are kept per host thread.
+struct GemvPlanKey {
+    int sms, n_jobs, nt_max, pad;
+    int64_t n_tok;
+    int type[GEMV_MAX_JOBS], upr[GEMV_MAX_JOBS];
+    int64_t n_out[GEMV_MAX_JOBS], n_in[GEMV_MAX_JOBS];
+};
+struct GemvPlan {
+    GemvPlanKey key;
+    bool valid;
+    int fused;
+    int64_t x_need;
+    int upr[GEMV_MAX_JOBS], n_units[GEMV_MAX_JOBS], warp_begin[GEMV_MAX_JOBS], warp_end[GEMV_MAX_JOBS];
+    uint8_t warp_job[GV_MAX_SMS * GV_WARPS];
+};
+
+static cudaError_t plan_cached(GemvBatch& b, int sms, int NT, int64_t& x_need) {
+    static thread_local GemvPlan plans[4];
+    static thread_local int next = 0;
+    GemvPlanKey k;
+    memset(&k, 0, sizeof(k));
+    k.sms = sms;
+    k.n_jobs = b.n_jobs;
+    k.nt_max = NT;
+    k.n_tok = b.n_tok;
+    for (int j = 0; j < b.n_jobs; j++) {
+        k.type[j] = b.job[j].type;
+        k.upr[j] = b.job[j].upr;
+        k.n_out[j] = b.job[j].n_out;
+        k.n_in[j] = b.job[j].n_in;
+    }
+    const int GW = sms * GV_WARPS;
+    for (GemvPlan& P : plans) {
+        if (!P.valid || memcmp(&P.key, &k, sizeof(k)) != 0) continue;
+        for (int j = 0; j < b.n_jobs; j++) {
+            GemvJob& J = b.job[j];
+            J.upr = P.upr[j];
+            J.n_units = P.n_units[j];
+            J.warp_begin = P.warp_begin[j];
+            J.warp_end = P.warp_end[j];
+            J.units = small_block(J.type) ? (J.nbx + 3) / 4 : J.nbx;
+        }
+        memcpy(b.warp_job, P.warp_job, (size_t)GW);
+        b.fused = P.fused;
+        x_need = P.x_need;
+        return cudaSuccess;
+    }
+    const cudaError_t e = plan_partition(b, sms, NT, x_need);
+    if (e != cudaSuccess) return e;
+    GemvPlan& P = plans[next];
+    next = (next + 1) % 4;
+    P.key = k;
+    for (int j = 0; j < b.n_jobs; j++) {
+        P.upr[j] = b.job[j].upr;
+        P.n_units[j] = b.job[j].n_units;
+        P.warp_begin[j] = b.job[j].warp_begin;
+        P.warp_end[j] = b.job[j].warp_end;
+    }
+    memcpy(P.warp_job, b.warp_job, (size_t)GW);
+    P.fused = b.fused;
+    P.x_need = x_need;
+    P.valid = true;
+    return cudaSuccess;
+}
+
+template <int NT>
+static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
+    sms = std::min(sms, GV_MAX_SMS);  // one CTA per SM, up to the size of the warp table
+    int64_t off = 0;
+    for (int j = 0; j < b.n_jobs; j++) {
+        GemvJob& J = b.job[j];
+        J.act_q = (int)off;
+        off = up16(off + (int64_t)NT * J.n_in);
+        J.act_d = (int)off;
+        off = up16(off + (int64_t)NT * J.ds * 4);
+        J.act_s = (int)off;
+        off = up16(off + (int64_t)NT * sum_bytes(J.type, J.n_in));
+    }
+    off = (off + 127) & ~int64_t(127);
+    b.off_stage = (int)off;
+    off += (int64_t)GV_WARPS * GV_NS * GV_SLOT;
+    b.off_bar = (int)off;
+    off += GV_WARPS * GV_NS * 8;
+    b.off_flag = (int)off;
+    off += 16;  // abort flag, activation barrier
+    if (off > 227 * 1024) return cudaErrorInvalidConfiguration;
+    b.off_x = (int)up16(off);
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(k_gemv<NT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(k_gemv<NT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    int64_t x_need = 0;
+    const cudaError_t pe = plan_cached(b, sms, NT, x_need);
+    if (pe != cudaSuccess) return pe;
     const size_t smem = b.fused ? (size_t)(b.off_x + x_need) : (size_t)b.off_x;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

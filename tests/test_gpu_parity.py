@@ -290,6 +290,41 @@ def test_prepared_batch_matches_grouped_call(syn):
     assert syn.device_status() == syn.OK
 
 
+def test_decode_plans_interleaved(syn):
+    """Grouped decode calls of different shapes interleaved (the host keeps the last few work
+    partitions by shape): every call matches the oracle, and repeats are bit-identical."""
+    cfgs = [([(oracle.Q4_K, 2048, 2048), (oracle.Q6_K, 512, 2048)], 1),
+            ([(oracle.Q8_0, 4096, 1024), (oracle.Q4_0, 300, 512), (oracle.Q5_0, 777, 1024)], 2),
+            ([(oracle.Q4_K, 8192, 2048)], 1),
+            ([(oracle.Q6_K, 2048, 8192), (oracle.Q4_K, 512, 2048)], 3),
+            ([(oracle.Q4_K, 8192, 2048)], 5),
+            ([(oracle.Q8_0, 64, 256)], 1)]
+    data = []
+    for c, (shapes, n_tok) in enumerate(cfgs):
+        Wq = [oracle.quantize(wt, synth.normal(90 + 7 * c + k, (n_out, n_in), 0.02)) for k, (wt, n_out, n_in) in enumerate(shapes)]
+        Xs = [synth.normal(95 + 7 * c + k, (n_tok, n_in)) for k, (_, _, n_in) in enumerate(shapes)]
+        data.append((shapes, n_tok, [dev(w) for w in Wq], [dev(x) for x in Xs], Wq, Xs))
+    old = syn.set_gemv_max_tok(8)
+    try:
+        first = {}
+        for rnd in range(3):
+            for c, (shapes, n_tok, Wd, Xd, Wq, Xs) in enumerate(data):
+                Ys = [torch.full((n_tok, n_out), np.nan, device="cuda") for _, n_out, _ in shapes]
+                syn.mul_mat_batch([(wt, W, n_out, n_in, X, Y) for (wt, n_out, n_in), W, X, Y in zip(shapes, Wd, Xd, Ys)], n_tok)
+                got = [host(Y) for Y in Ys]
+                if rnd == 0:
+                    for (wt, n_out, n_in), w, x, y in zip(shapes, Wq, Xs, got):
+                        ref = oracle.mul_mat(wt, w, n_out, n_in, x)
+                        assert_close(y, ref, tolerance(wt, w, n_in, x), f"cfg {c} type {wt} {n_out}x{n_in}")
+                    first[c] = got
+                else:
+                    for a, b in zip(first[c], got):
+                        assert np.array_equal(a, b), f"cfg {c} round {rnd}"
+    finally:
+        syn.set_gemv_max_tok(old)
+    assert syn.device_status() == syn.OK
+
+
 def test_mul_mat_orientation_example_exact(syn):
     """ggml_mul_mat(A, B^T) = C^T with the examples/simple integers, exact on both paths."""
     A = np.array([[2, 8], [5, 1], [4, 2], [8, 6]], np.float32)
