@@ -169,9 +169,9 @@ typedef struct {
 /* n independent products Y_i = ggml_mul_mat(W_i, X_i), all with n_tok tokens: the same
  * result as n calls of syn_mul_mat.  The quantized products with n_tok <= their format's
  * decode threshold (see syn_mul_mat) run in as few launches as the decode kernel's limits
- * allow (at most 16 matrices and 56 KiB of converted activations per launch), so the
- * products of a layer (q, k, v, o, gate, up, down) share one launch and all SMs stream
- * their weights together.  The others (F16, rows too wide for the decode kernel, or more
+ * allow (at most 16 matrices and 83,456 bytes of converted activations per token group and
+ * launch), so the products of a layer (q, k, v, o, gate, up, down) share one launch and all
+ * SMs stream their weights together.  The others (F16, rows too wide for the decode kernel, or more
  * tokens than the format decodes) run one by one as in syn_mul_mat.  Arguments are checked
  * as for syn_mul_mat before anything is enqueued.  Asynchronous. */
 SYN_API int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_stream_t stream);
@@ -215,8 +215,8 @@ SYN_API int syn_set_gemv_max_tok(int n);
  *     syn_mul_mat_batch calls, or split of the tokens into calls (the counterpart of D1).
  * Accuracy is that of the decode path (the tolerance of syn_mul_mat).  Prefill is far
  * slower in this mode (no tensor cores).  Products whose converted activation row does not
- * fit the decode kernel's shared memory (n_in above about 60,000 for the 8-bit activation
- * formats) return SYN_ERR_SHAPE in this mode.  syn_mul_mat_prefill_static is not affected
+ * fit the decode kernel's shared memory (n_in above 72,960 for Q4_K / Q6_K, 74,112 for
+ * Q8_0, 70,208 for Q4_0 / Q5_0) return SYN_ERR_SHAPE in this mode.  syn_mul_mat_prefill_static is not affected
  * (it always runs the tensor-core prefill). */
 SYN_API int syn_set_deterministic(int on);
 

@@ -512,6 +512,40 @@ def test_deterministic_mode_rejects_too_wide_rows(syn):
     assert_close(Y, oracle.mul_mat(wt, Wq, n_out, n_in, X), tolerance(wt, Wq, n_in, X), "wide row, default mode")
 
 
+# the widest rows the decode kernel takes (converted activations of one token within its
+# shared-memory budget), as documented with syn_set_deterministic
+DECODE_MAX_N_IN = {oracle.Q4_K: 72960, oracle.Q6_K: 72960, oracle.Q8_0: 74112, oracle.Q4_0: 70208, oracle.Q5_0: 70208}
+
+
+@pytest.mark.parametrize("wt", sorted(DECODE_MAX_N_IN))
+def test_decode_widest_rows(syn, wt):
+    """At the documented widest row the decode kernels run it (deterministic mode accepts it)
+    and match the oracle; one block wider is rejected in that mode."""
+    n_out, n_in = 5, DECODE_MAX_N_IN[wt]
+    be = 256 if wt in (oracle.Q4_K, oracle.Q6_K) else 32
+    Wq = oracle.quantize(wt, synth.normal(820 + wt, (n_out, n_in + be), 0.02))
+    X = synth.normal(830 + wt, (2, n_in + be))
+    old = syn.set_deterministic(True)
+    try:
+        Wn = oracle.quantize(wt, synth.normal(820 + wt, (n_out, n_in), 0.02))
+        Xn = np.ascontiguousarray(X[:, :n_in])
+        Y = host(syn.mul_mat(wt, dev(Wn), n_out, n_in, dev(Xn)))
+        W2, X2 = dev(Wq), dev(X)
+        Y2 = torch.empty((2, n_out), device="cuda")
+        assert syn.syn_mul_mat(wt, syn._ptr(W2), n_out, n_in + be, syn._ptr(X2), 2, syn._ptr(Y2), None) == syn.ERR_SHAPE
+    finally:
+        syn.set_deterministic(old)
+    assert_close(Y, oracle.mul_mat(wt, Wn, n_out, n_in, Xn), tolerance(wt, Wn, n_in, Xn), f"widest row {n_in}")
+    assert syn.device_status() == syn.OK
+
+
+@pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q8_0])
+def test_mul_mat_gemm_many_token_tiles(syn, wt):
+    """Prefill over 17 token tiles of 256 with a ragged last one, and a ragged row count."""
+    Y, ref, bound = run_mul_mat(syn, wt, 130, 512, 4097, 840 + wt, "gemm")
+    assert_close(Y, ref, bound, "4097 tokens")
+
+
 @pytest.mark.parametrize("lim", [1, 7, 64])
 def test_sm_limit_parity(syn, lim):
     """Products on a limited number of SMs (decode, grouped decode and tensor-core prefill)
