@@ -11,8 +11,9 @@
  *      i.e. ggml_mul_mat(W, X) = (X W^T): each token's outputs are contiguous.
  *
  * Xq is X converted, row by row, to the weight format's vec_dot_type before the product
- * (Q8_0 for Q8_0 weights, Q8_K for Q4_K and Q6_K weights): the product is that of the
- * quantized activations, as on the pages, not the exact fp32 product.
+ * (Q8_0 for Q8_0, Q4_0 and Q5_0 weights, Q8_K for Q4_K and Q6_K weights, fp16 for F16
+ * weights): the product is that of the converted activations, as on the pages, not the
+ * exact fp32 product.
  *
  * Conventions for every entry point:
  *   - pointers are DEVICE pointers on the current CUDA device unless stated otherwise,
@@ -90,10 +91,12 @@ enum {
     SYN_ERR_NOTFOUND = -13, /* no GGUF key / tensor with that name or index              */
 };
 
-/* Elements per block: 32 (Q8_0, Q4_0, Q5_0), 256 (Q4_K, Q6_K, Q8_K) or 1 (F16); -1 for an unknown type. */
+/* Elements per block: 32 (Q8_0, Q4_0, Q5_0), 256 (Q4_K, Q6_K, Q8_K) or 1 (F16); -1 for an
+ * unknown type. */
 SYN_API int64_t syn_block_elems(int type);
 
-/* Bytes per block: 34, 144, 210, 292; -1 for an unknown type. */
+/* Bytes per block: 34 (Q8_0), 144 (Q4_K), 210 (Q6_K), 292 (Q8_K), 18 (Q4_0), 22 (Q5_0),
+ * 2 (F16); -1 for an unknown type. */
 SYN_API int64_t syn_block_bytes(int type);
 
 /* Bytes of one row of n elements: (n / elems) * bytes; -1 if the type is unknown or
@@ -123,30 +126,32 @@ SYN_API int syn_quantize(int type, const float* src, void* dst, int64_t n_rows, 
                  syn_stream_t stream);
 
 /* Expand blocks back to fp32 ("dequantize_row_*", same page, section 5): dst gets
- * n_rows * n_per_row floats.  Q8_0: d*q; Q4_K: (d*sc)*q - (dmin*mn); Q6_K:
- * (d*sc)*(q-32); Q8_K: d*q; Q4_0: d*(q-8); Q5_0: d*(q-16); F16: the value — each product and difference
- * one fp32 rounding, no FMA,
- * so the result is bit-exact with the CPU oracle.  Asynchronous.  Alignment: 16 B. */
+ * n_rows * n_per_row floats.  Q8_0: d*q; Q4_K: (d*sc)*q - (dmin*mn); Q6_K: (d*sc)*(q-32);
+ * Q8_K: d*q; Q4_0: d*(q-8); Q5_0: d*(q-16); F16: the value.  Each product and difference is
+ * one fp32 rounding (no FMA), so the result is bit-exact with the CPU oracle.
+ * Asynchronous.  Alignment: 16 B. */
 SYN_API int syn_dequantize(int type, const void* src, float* dst, int64_t n_rows, int64_t n_per_row,
                    syn_stream_t stream);
 
 /* The activation step of the product on its own (from_float to the vec_dot_type):
  * X (n_tok x n_in fp32) -> codes qs (n_tok x n_in int8), scales d (n_tok x n_in/Bx fp32,
- * Bx = 32 for Q8_0/Q4_0/Q5_0 weights, 256 for K-quant weights; for Q8_0 the value of
- * the stored fp16 scale) and, for K-quant weights only, bsums (n_tok x n_in/16 int16; may
- * be NULL otherwise).  wtype is the WEIGHT format (Q8_0, Q4_K, Q6_K, Q4_0 or Q5_0).  This is the same device
- * code the product kernels run on their inputs.  Asynchronous.  Alignment: 16 B. */
+ * Bx = 32 for Q8_0/Q4_0/Q5_0 weights, 256 for K-quant weights; for the 32-blocks the value
+ * of the stored fp16 scale) and, for K-quant weights only, bsums (n_tok x n_in/16 int16; may
+ * be NULL otherwise).  wtype is the WEIGHT format (Q8_0, Q4_K, Q6_K, Q4_0 or Q5_0).  This
+ * is the same device code the product kernels run on their inputs.  Asynchronous.
+ * Alignment: 16 B. */
 SYN_API int syn_quantize_activations(int wtype, const float* X, int64_t n_tok, int64_t n_in,
                              int8_t* qs, float* d, int16_t* bsums, syn_stream_t stream);
 
 /* Y = ggml_mul_mat(W, X) as described at the top of this file.
  * type: Q8_0, Q4_K, Q6_K, Q4_0, Q5_0 or F16 (Q8_K is activation-only: SYN_ERR_TYPE).
  * n_tok <= the decode threshold (per format by default: 8 for Q4_K and Q6_K, 4 for Q8_0,
- * Q4_0 and Q5_0, 2 for F16; see syn_set_gemv_max_tok) runs the decode kernel: one
- * launch that quantizes X in shared memory and streams W once per group of up to 8
- * tokens.  Larger n_tok runs the prefill path: one kernel quantizes X and writes
- * the dequantized fp16 activations into the library workspace, a second runs the
- * tensor-core GEMM on W tiles dequantized to fp16 in shared memory (fp32 accumulation).
+ * Q4_0 and Q5_0, 2 for F16; see syn_set_gemv_max_tok) runs the decode kernels: X is
+ * converted (by a conversion launch into the library workspace, or, for narrow inputs,
+ * inside the decode CTAs) and W is streamed once per group of up to 8 tokens.  Larger
+ * n_tok runs the prefill path: one kernel converts X and writes the dequantized fp16
+ * activations into the library workspace, a second runs the tensor-core GEMM on W tiles
+ * dequantized to fp16 in shared memory (fp32 accumulation).
  * Accuracy: |y - y_ref| <= 1e-4 * ||dequant(w_row)||_2 * ||x||_2 per element, where
  * y_ref is the same product evaluated in fp64.  W, X, Y: 16-byte aligned, not aliased.
  * n_tok == 0 is a no-op.  Asynchronous.  The prefill path may grow the workspace (see
@@ -171,9 +176,9 @@ typedef struct {
  * decode threshold (see syn_mul_mat) run in as few launches as the decode kernel's limits
  * allow (at most 16 matrices and 83,456 bytes of converted activations per token group and
  * launch), so the products of a layer (q, k, v, o, gate, up, down) share one launch and all
- * SMs stream their weights together.  The others (F16, rows too wide for the decode kernel, or more
- * tokens than the format decodes) run one by one as in syn_mul_mat.  Arguments are checked
- * as for syn_mul_mat before anything is enqueued.  Asynchronous. */
+ * SMs stream their weights together.  The others (F16, rows too wide for the decode
+ * kernel, or more tokens than the format decodes) run one by one as in syn_mul_mat.
+ * Arguments are checked as for syn_mul_mat before anything is enqueued.  Asynchronous. */
 SYN_API int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_stream_t stream);
 
 /* Pre-size the prefill workspace of (current device, stream) for products with up to
@@ -216,8 +221,8 @@ SYN_API int syn_set_gemv_max_tok(int n);
  * Accuracy is that of the decode path (the tolerance of syn_mul_mat).  Prefill is far
  * slower in this mode (no tensor cores).  Products whose converted activation row does not
  * fit the decode kernel's shared memory (n_in above 72,960 for Q4_K / Q6_K, 74,112 for
- * Q8_0, 70,208 for Q4_0 / Q5_0) return SYN_ERR_SHAPE in this mode.  syn_mul_mat_prefill_static is not affected
- * (it always runs the tensor-core prefill). */
+ * Q8_0, 70,208 for Q4_0 / Q5_0) return SYN_ERR_SHAPE in this mode.
+ * syn_mul_mat_prefill_static is not affected (it always runs the tensor-core prefill). */
 SYN_API int syn_set_deterministic(int on);
 
 /* At most n SMs for the library's launches (n >= 1; 0 = all of them, the default).
