@@ -775,22 +775,35 @@ static_assert(gemm_bars_fit<SYN_Q4_K>() && gemm_bars_fit<SYN_Q6_K>() && gemm_bar
                   gemm_bars_fit<SYN_Q4_0>() && gemm_bars_fit<SYN_Q5_0>() && gemm_bars_fit<SYN_F16>(),
               "barrier area");
 
-#ifndef SYN_GEMM_SPLIT_PENALTY
-#define SYN_GEMM_SPLIT_PENALTY 0.15
+// Cost model of a K split (microseconds on GB300, fitted to measured Q4_K products): whole
+// waves of units, each 1/S of a tile's multiply-adds at about 7 TFLOP/s per SM plus a fixed
+// pipeline cost; for S > 1, zeroing Y and adding S partial tiles into it at L2.
+#ifndef SYN_GEMM_SM_TFLOPS
+#define SYN_GEMM_SM_TFLOPS 7.0
+#endif
+#ifndef SYN_GEMM_UNIT_US
+#define SYN_GEMM_UNIT_US 1.0
+#endif
+#ifndef SYN_GEMM_ZERO_US_PER_MB
+#define SYN_GEMM_ZERO_US_PER_MB 0.15
+#endif
+#ifndef SYN_GEMM_ADD_US_PER_MB
+#define SYN_GEMM_ADD_US_PER_MB 0.08
 #endif
 
-// Pick the K split so that units fill the SMs in whole waves: minimise
-// ceil(tiles * S / sms) / S, with a penalty for splitting (the partial tiles are added
-// into Y with atomics), preferring the smaller S on ties (each split keeps >= 2
-// super-steps).
-static int pick_split(int64_t tiles, int n_super, int sms) {
+// Pick the K split S (1..16, each split >= 2 super-steps) of least modelled time, the
+// smaller S on ties.
+static int pick_split(int64_t tiles, int n_super, int sms, int bn, int64_t n_out, int64_t n_tok) {
+    const double tile_us = 2.0 * GEMM_BM * bn * (double)n_super * GEMM_SUPER / (SYN_GEMM_SM_TFLOPS * 1e6);
+    const double y_mb = 4.0 * (double)n_out * (double)n_tok / 1e6;
     int best = 1;
-    double best_t = 1e30;
+    double best_t = 1e300;
     for (int S = 1; S <= 16; S++) {
         if (S > 1 && n_super / S < 2) break;
         const int64_t waves = (tiles * S + sms - 1) / sms;
-        const double t = (double)waves / S + (S > 1 ? SYN_GEMM_SPLIT_PENALTY : 0.0);
-        if (t < best_t - 1e-9) {
+        double t = (double)waves * (tile_us / S + SYN_GEMM_UNIT_US);
+        if (S > 1) t += y_mb * (SYN_GEMM_ZERO_US_PER_MB + S * SYN_GEMM_ADD_US_PER_MB);
+        if (t < best_t * (1.0 - 1e-9)) {
             best_t = t;
             best = S;
         }
@@ -828,7 +841,7 @@ static int gemm_bn(int64_t n_tok) { return (int)std::min<int64_t>(256, (n_tok + 
 bool gemm_needs_zero(int64_t n_out, int64_t n_in, int64_t n_tok, int sms) {
     const int bn = gemm_bn(n_tok);
     const int64_t tiles = ((n_out + GEMM_BM - 1) / GEMM_BM) * ((n_tok + bn - 1) / bn);
-    return pick_split(tiles, (int)((n_in + GEMM_SUPER - 1) / GEMM_SUPER), sms) > 1;
+    return pick_split(tiles, (int)((n_in + GEMM_SUPER - 1) / GEMM_SUPER), sms, bn, n_out, n_tok) > 1;
 }
 
 cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, const void* xh, int64_t n_tok,
@@ -852,7 +865,7 @@ cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, co
     const int64_t tiles = (int64_t)p.n_m * p.n_n;
     if (tiles * 16 > (int64_t(1) << 30) || (int64_t)p.n_super * 16 > (int64_t(1) << 30))
         return cudaErrorInvalidValue;  // 32-bit unit and super-step arithmetic
-    p.n_split = pick_split(tiles, p.n_super, sms);
+    p.n_split = pick_split(tiles, p.n_super, sms, p.bn, n_out, n_tok);
     p.n_units = (int)(tiles * p.n_split);
     p.accumulate = p.n_split > 1 ? 1 : 0;
     // kind::f16 instruction descriptor: D fp32, A and B fp16, both K-major, N, M = 128
