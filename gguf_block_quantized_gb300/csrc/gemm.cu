@@ -60,17 +60,17 @@ template <int T> struct GemmFmt;
 // covers the slice from the 16-byte boundary at or below it (ESIZE: the tensor map's
 // element size, 2 where the box is wider than 256 elements of one byte); RAW_ROW: bytes
 // reserved per row in a raw stage for the per-row copy windows; RAW_STAGES: ring depth.
-// A_STAGES / B_STAGES: depths of the dequantized-weight and activation rings.  The
-// activation tiles come from L2 with the longest latency, so their ring gets what the
-// shared memory allows.
+// A_STAGES / B_STAGES: depths of the dequantized-weight and activation rings, measured per
+// format: a deeper A ring (5 stages) lets the two dequantizer teams run ahead of the MMA,
+// and 2-3 activation stages cover the L2 latency of the activation tiles.
 #ifndef SYN_GEMM_Q4K_RAW
 #define SYN_GEMM_Q4K_RAW 2
 #endif
 #ifndef SYN_GEMM_Q4K_A
-#define SYN_GEMM_Q4K_A 3
+#define SYN_GEMM_Q4K_A 5
 #endif
 #ifndef SYN_GEMM_Q4K_B
-#define SYN_GEMM_Q4K_B 4
+#define SYN_GEMM_Q4K_B 3
 #endif
 template <int R, int A, int B> struct GemmDepth {
     static constexpr int RAW_STAGES = R, A_STAGES = A, B_STAGES = B;
@@ -78,21 +78,55 @@ template <int R, int A, int B> struct GemmDepth {
 template <> struct GemmFmt<SYN_Q4_K> : GemmDepth<SYN_GEMM_Q4K_RAW, SYN_GEMM_Q4K_A, SYN_GEMM_Q4K_B> {
     static constexpr int BB = 144, SB_BYTES = 144, BOX = 144, ESIZE = 1, RAW_ROW = 144;
 };
-template <> struct GemmFmt<SYN_Q6_K> : GemmDepth<2, 3, 3> {
+#ifndef SYN_GEMM_Q6K_RAW
+#define SYN_GEMM_Q6K_RAW 2
+#endif
+#ifndef SYN_GEMM_Q6K_A
+#define SYN_GEMM_Q6K_A 5
+#endif
+#ifndef SYN_GEMM_Q6K_B
+#define SYN_GEMM_Q6K_B 2
+#endif
+template <> struct GemmFmt<SYN_Q6_K> : GemmDepth<SYN_GEMM_Q6K_RAW, SYN_GEMM_Q6K_A, SYN_GEMM_Q6K_B> {
     static constexpr int BB = 210, SB_BYTES = 210, BOX = 240, ESIZE = 1, RAW_ROW = 240;
 };
-template <> struct GemmFmt<SYN_Q4_0> : GemmDepth<2, 3, 4> {
+// ring depths (raw, A, B) of the other formats
+#ifndef SYN_GEMM_Q40_A
+#define SYN_GEMM_Q40_A 5
+#endif
+#ifndef SYN_GEMM_Q40_B
+#define SYN_GEMM_Q40_B 3
+#endif
+#ifndef SYN_GEMM_Q50_A
+#define SYN_GEMM_Q50_A 3
+#endif
+#ifndef SYN_GEMM_Q50_B
+#define SYN_GEMM_Q50_B 3
+#endif
+#ifndef SYN_GEMM_F16_A
+#define SYN_GEMM_F16_A 4
+#endif
+#ifndef SYN_GEMM_F16_B
+#define SYN_GEMM_F16_B 4
+#endif
+#ifndef SYN_GEMM_Q80_A
+#define SYN_GEMM_Q80_A 3
+#endif
+#ifndef SYN_GEMM_Q80_B
+#define SYN_GEMM_Q80_B 3
+#endif
+template <> struct GemmFmt<SYN_Q4_0> : GemmDepth<2, SYN_GEMM_Q40_A, SYN_GEMM_Q40_B> {
     static constexpr int BB = 18, SB_BYTES = 144, BOX = 144, ESIZE = 1, RAW_ROW = 160;
 };
-template <> struct GemmFmt<SYN_Q5_0> : GemmDepth<2, 3, 3> {
+template <> struct GemmFmt<SYN_Q5_0> : GemmDepth<2, SYN_GEMM_Q50_A, SYN_GEMM_Q50_B> {
     static constexpr int BB = 22, SB_BYTES = 176, BOX = 176, ESIZE = 1, RAW_ROW = 192;
 };
 // F16: no raw ring; the weight tile is loaded by TMA straight into the A ring (the same
 // 128-byte-swizzled K-major layout as the activation tiles)
-template <> struct GemmFmt<SYN_F16> : GemmDepth<1, 4, 4> {  // (one raw stage of 0 bytes: unused)
+template <> struct GemmFmt<SYN_F16> : GemmDepth<1, SYN_GEMM_F16_A, SYN_GEMM_F16_B> {  // (one raw stage of 0 bytes: unused)
     static constexpr int BB = 2, SB_BYTES = 512, BOX = 128, ESIZE = 2, RAW_ROW = 0;
 };
-template <> struct GemmFmt<SYN_Q8_0> : GemmDepth<2, 3, 3> {
+template <> struct GemmFmt<SYN_Q8_0> : GemmDepth<2, SYN_GEMM_Q80_A, SYN_GEMM_Q80_B> {
     static constexpr int BB = 34, SB_BYTES = 272, BOX = 272, ESIZE = 2, RAW_ROW = 288;
 };
 
