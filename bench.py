@@ -590,24 +590,36 @@ def other_configs(torch, syn, synth, workloads, stream, l2, hbm_peak, tc_peak, q
                                          "weight_bytes": wsum, "matrices": len(mats),
                                          "api": "syn_mul_mat_batch per layer + syn_mul_mat for the lm_head"}
     del X1, Y1
-    # prefill at 2048 tokens: one syn_mul_mat per matrix
+    # prefill at 2048 tokens, called as a model calls it: per layer q/k/v in one grouped call on
+    # the attention input, o on its own input, gate/up in one grouped call on the FFN input,
+    # down on its own input; then the lm_head (a grouped call converts a shared input once)
     p_tok = 2048
-    XP = inputs(p_tok, 4998)
-    YP = {}
-    for m in mats:
-        if m.n_out not in YP:
-            YP[m.n_out] = torch.empty((p_tok, m.n_out), device="cuda")
+    gen.manual_seed(4998)
+    d_model, d_ffn = layers[0][0].n_in, layers[0][6].n_in
+    XA, XO, XF = (torch.randn((p_tok, d_model), generator=gen, device="cuda") for _ in range(3))
+    XD = torch.randn((p_tok, d_ffn), generator=gen, device="cuda")
+    YP = [torch.empty((p_tok, m.n_out), device="cuda") for m in layers[0]]
+    YH = torch.empty((p_tok, head.n_out), device="cuda")
     syn.syn_reserve(max(dims), p_tok, stream.cuda_stream)
 
     def prefill(_c):
-        for i, m in enumerate(mats):
-            syn.mul_mat(m.wtype, W[i], m.n_out, m.n_in, XP[m.n_in], Y=YP[m.n_out], stream=stream)
+        for k, lay in enumerate(layers):
+            w = W[7 * k:7 * k + 7]
+            syn.mul_mat_batch([(lay[i].wtype, w[i], lay[i].n_out, lay[i].n_in, XA, YP[i]) for i in range(3)], p_tok,
+                              stream=stream)
+            syn.mul_mat(lay[3].wtype, w[3], lay[3].n_out, lay[3].n_in, XO, Y=YP[3], stream=stream)
+            syn.mul_mat_batch([(lay[i].wtype, w[i], lay[i].n_out, lay[i].n_in, XF, YP[i]) for i in (4, 5)], p_tok,
+                              stream=stream)
+            syn.mul_mat(lay[6].wtype, w[6], lay[6].n_out, lay[6].n_in, XD, Y=YP[6], stream=stream)
+        syn.mul_mat(head.wtype, W[-1], head.n_out, head.n_in, XF, Y=YH, stream=stream)
     t = time_calls(torch, stream, prefill, 1, 1, trials=3)
     fl = sum(workloads.gemm_flops(m, p_tok) for m in mats)
     out["llama8b_q4_k_m_prefill_2048tok"] = {"value": round(fl / t / 1e12, 1), "unit": "TFLOP/s",
                                              "frac": round(fl / t / 1e12 / tc_peak, 4), "ms": round(t * 1e3, 3),
-                                             "flops": fl, "matrices": len(mats)}
-    del W, XP, YP
+                                             "flops": fl, "matrices": len(mats),
+                                             "api": "per layer syn_mul_mat_batch(q, k, v), syn_mul_mat(o), "
+                                                    "syn_mul_mat_batch(gate, up), syn_mul_mat(down); syn_mul_mat(lm_head)"}
+    del W, XA, XO, XF, XD, YP, YH
     torch.cuda.empty_cache()
     return out
 

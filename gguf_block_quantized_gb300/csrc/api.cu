@@ -10,6 +10,7 @@
 #include <atomic>
 #include <cstdlib>
 #include <map>
+#include <vector>
 #include <mutex>
 #include <utility>
 
@@ -287,6 +288,38 @@ int syn_release(void) {
     return SYN_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// The prefill path of products that share one activation input (the same X, n_in and
+// vec_dot_type: q/k/v, or gate/up, of a layer): Y of the products split along K zeroed,
+// X converted once into the workspace, then one tensor-core launch per product.
+int prefill_group(const syn_mat_desc* const* g, int m, int64_t n_tok, const DeviceState* st, cudaStream_t s) {
+    const int64_t n_in = g[0]->n_in;
+    const int xt = vec_dot(g[0]->type);
+    void* ws;
+    int rc = workspace_for(s, prefill_ws_bytes(n_in, n_tok), &ws);
+    if (rc) return rc;
+    for (int i = 0; i < m; i++)
+        if (syn::gemm_needs_zero(g[i]->n_out, n_in, n_tok, sms_of(st)) &&
+            cudaMemsetAsync(g[i]->Y, 0, (size_t)n_tok * g[i]->n_out * sizeof(float), s) != cudaSuccess)
+            return SYN_ERR_CUDA;
+    if (launch_act_half(xt, g[0]->X, n_tok * (n_in / elems(xt)), ws, sms_of(st), s) != cudaSuccess) return SYN_ERR_CUDA;
+    g_launches++;
+    for (int i = 0; i < m; i++) {
+        if (syn::launch_gemm(g[i]->type, g[i]->W, g[i]->n_out, n_in, ws, n_tok, g[i]->Y, st->words, sms_of(st), s) !=
+            cudaSuccess)
+            return SYN_ERR_CUDA;
+        g_launches++;
+    }
+    return SYN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in, const float* X, int64_t n_tok, float* Y,
                 syn_stream_t stream) {
     if (!is_weight(type)) return SYN_ERR_TYPE;
@@ -320,19 +353,9 @@ int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in, const floa
         if (rc == SYN_OK) g_launches += 2;
         return rc;
     }
-    void* ws;
-    rc = workspace_for(s, prefill_ws_bytes(n_in, n_tok), &ws);
-    if (rc) return rc;
-    const int xt = vec_dot(type);
-    if (syn::gemm_needs_zero(n_out, n_in, n_tok, sms_of(st)) &&
-        cudaMemsetAsync(Y, 0, (size_t)n_tok * n_out * sizeof(float), s) != cudaSuccess)
-        return SYN_ERR_CUDA;
-    if (launch_act_half(xt, X, n_tok * (n_in / elems(xt)), ws, sms_of(st), s) != cudaSuccess) return SYN_ERR_CUDA;
-    g_launches++;
-    if (syn::launch_gemm(type, W, n_out, n_in, ws, n_tok, Y, st->words, sms_of(st), s) != cudaSuccess)
-        return SYN_ERR_CUDA;
-    g_launches++;
-    return SYN_OK;
+    const syn_mat_desc d{type, W, n_out, n_in, X, Y};
+    const syn_mat_desc* g = &d;
+    return prefill_group(&g, 1, n_tok, st, s);
 }
 
 int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_stream_t stream) {
@@ -368,12 +391,16 @@ int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_strea
         act = 0;
         return r;
     };
+    std::vector<const syn_mat_desc*> pre;  // products on the tensor-core prefill path
     for (int i = 0; i < n; i++) {
         const syn_mat_desc& d = descs[i];
         const int64_t a = d.type == SYN_TYPE_F16 ? 0 : syn::gemv_act_bytes(d.type, d.n_in);
-        // its own call: F16, rows too wide for the decode kernel, or (outside the deterministic
-        // mode) more tokens than its format decodes
-        if (d.type == SYN_TYPE_F16 || a > syn::gemv_act_limit() || (!det && n_tok > decode_max_tok(d.type))) {
+        if (!det && (n_tok > decode_max_tok(d.type) || a > syn::gemv_act_limit())) {
+            pre.push_back(&d);
+            continue;
+        }
+        // F16 decode, or a row too wide for the decode kernel in deterministic mode: its own call
+        if (d.type == SYN_TYPE_F16 || a > syn::gemv_act_limit()) {
             rc = syn_mul_mat(d.type, d.W, d.n_out, d.n_in, d.X, n_tok, d.Y, stream);
             if (rc) return rc;
             continue;
@@ -385,7 +412,25 @@ int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_strea
         group[ng++] = syn::GemvDesc{d.type, d.W, d.n_out, d.n_in, d.X, d.Y};
         act += a;
     }
-    return flush();
+    rc = flush();
+    if (rc) return rc;
+    // prefill products grouped by activation input, each group converting its input once
+    std::vector<char> done(pre.size(), 0);
+    std::vector<const syn_mat_desc*> g;
+    for (size_t i = 0; i < pre.size(); i++) {
+        if (done[i]) continue;
+        g.clear();
+        for (size_t j = i; j < pre.size(); j++) {
+            if (done[j] || pre[j]->X != pre[i]->X || pre[j]->n_in != pre[i]->n_in ||
+                vec_dot(pre[j]->type) != vec_dot(pre[i]->type))
+                continue;
+            g.push_back(pre[j]);
+            done[j] = 1;
+        }
+        rc = prefill_group(g.data(), (int)g.size(), n_tok, st, s);
+        if (rc) return rc;
+    }
+    return SYN_OK;
 }
 
 int syn_block_sums(int type, const void* W, int64_t n_out, int64_t n_in, const void* Xq, int64_t n_tok, int32_t* S,

@@ -176,9 +176,12 @@ typedef struct {
  * decode threshold (see syn_mul_mat) run in as few launches as the decode kernel's limits
  * allow (at most 16 matrices and 83,456 bytes of converted activations per token group and
  * launch), so the products of a layer (q, k, v, o, gate, up, down) share one launch and all
- * SMs stream their weights together.  The others (F16, rows too wide for the decode
- * kernel, or more tokens than the format decodes) run one by one as in syn_mul_mat.
- * Arguments are checked as for syn_mul_mat before anything is enqueued.  Asynchronous. */
+ * SMs stream their weights together.  The products with more tokens than their format
+ * decodes (or rows too wide for the decode kernel) take the prefill path; those of them that
+ * share one activation input (the same X pointer, n_in and vec_dot_type, e.g. q/k/v or
+ * gate/up of a layer) convert it once and run one tensor-core launch each.  F16 products in
+ * decode run as in syn_mul_mat.  Arguments are checked as for syn_mul_mat before anything
+ * is enqueued.  Asynchronous. */
 SYN_API int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_stream_t stream);
 
 /* Pre-size the prefill workspace of (current device, stream) for products with up to

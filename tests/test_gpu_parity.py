@@ -267,6 +267,32 @@ def test_mul_mat_batch_mixed_group(syn, n_tok):
     assert syn.device_status() == syn.OK
 
 
+@pytest.mark.parametrize("n_tok", [6, 300])
+def test_mul_mat_batch_shared_inputs(syn, n_tok):
+    """A grouped call whose products share activation inputs (q/k/v on one input, gate/up on
+    another, formats with the same vec_dot_type or not): on the prefill path each shared input
+    is converted once; every product matches the oracle, and matches its own syn_mul_mat."""
+    n_in = 1024
+    XA, XF = synth.normal(610, (n_tok, n_in)), synth.normal(611, (n_tok, n_in))
+    specs = [(oracle.Q4_K, 384, XA), (oracle.Q4_K, 128, XA), (oracle.Q6_K, 128, XA), (oracle.Q8_0, 256, XA),
+             (oracle.F16, 64, XA), (oracle.Q4_K, 640, XF), (oracle.Q4_K, 640, XF), (oracle.Q5_0, 96, XF)]
+    XAd, XFd = dev(XA), dev(XF)
+    items, refs, singles = [], [], []
+    for i, (wt, n_out, X) in enumerate(specs):
+        Wq = oracle.quantize(wt, synth.normal(620 + i, (n_out, n_in), 0.02))
+        Wd = dev(Wq)
+        Xd = XAd if X is XA else XFd
+        items.append((wt, Wd, n_out, n_in, Xd, torch.full((n_tok, n_out), np.nan, device="cuda")))
+        refs.append((oracle.mul_mat(wt, Wq, n_out, n_in, X), tolerance(wt, Wq, n_in, X)))
+        singles.append(host(syn.mul_mat(wt, Wd, n_out, n_in, Xd)))
+    syn.mul_mat_batch(items, n_tok)
+    for (wt, _, n_out, _, _, Yd), (ref, bound), y1 in zip(items, refs, singles):
+        y = host(Yd)
+        assert_close(y, ref, bound, f"shared-input batch type {wt} {n_out}x{n_in} n_tok {n_tok}")
+        assert_close(y, y1, 2 * bound, f"batch vs single type {wt} {n_out}")
+    assert syn.device_status() == syn.OK
+
+
 def test_prepared_batch_matches_grouped_call(syn):
     """The prepared grouped call (descriptors marshalled once) runs the same launches as
     mul_mat_batch: bit-identical outputs, and repeated calls see updated inputs."""
