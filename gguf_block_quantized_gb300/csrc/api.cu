@@ -358,19 +358,34 @@ int syn_mul_mat(int type, const void* W, int64_t n_out, int64_t n_in, const floa
     return prefill_group(&g, 1, n_tok, st, s);
 }
 
-int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_stream_t stream) {
-    if (n < 0) return SYN_ERR_SHAPE;
-    if (n == 0 || n_tok == 0) return n_tok < 0 ? SYN_ERR_SHAPE : SYN_OK;
+}  // extern "C"
+
+namespace {
+
+// Argument checks of syn_mul_mat_batch (SYN_OK also for the no-op n == 0 or n_tok == 0).
+int check_batch(int n, const syn_mat_desc* descs, int64_t n_tok) {
+    if (n < 0 || n_tok < 0) return SYN_ERR_SHAPE;
+    if (n == 0 || n_tok == 0) return SYN_OK;
     if (!descs) return SYN_ERR_NULL;
     for (int i = 0; i < n; i++) {
         const syn_mat_desc& d = descs[i];
         if (!is_weight(d.type)) return SYN_ERR_TYPE;
-        if (d.n_out <= 0 || d.n_in <= 0 || n_tok < 0 || d.n_in % row_multiple(d.type) || d.n_out * d.n_in > kMaxElems ||
+        if (d.n_out <= 0 || d.n_in <= 0 || d.n_in % row_multiple(d.type) || d.n_out * d.n_in > kMaxElems ||
             n_tok * d.n_in > kMaxElems || n_tok * d.n_out > kMaxElems || d.n_out > (int64_t(1) << 31))
             return SYN_ERR_SHAPE;
         if (!d.W || !d.X || !d.Y) return SYN_ERR_NULL;
         if (!aligned16(d.W) || !aligned16(d.X) || !aligned16(d.Y)) return SYN_ERR_ALIGN;
     }
+    return SYN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_stream_t stream) {
+    const int ck = check_batch(n, descs, n_tok);
+    if (ck || n == 0 || n_tok == 0) return ck;
     DeviceState* st;
     int rc = device_state(&st);
     if (rc) return rc;
@@ -430,6 +445,21 @@ int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_strea
         rc = prefill_group(g.data(), (int)g.size(), n_tok, st, s);
         if (rc) return rc;
     }
+    return SYN_OK;
+}
+
+int syn_mul_mat_batch_staged(int n, const syn_mat_desc* descs, int64_t n_tok, const void* x_host, void* x_dev,
+                             size_t x_bytes, const void* y_dev, void* y_host, size_t y_bytes, syn_stream_t stream) {
+    const int ck = check_batch(n, descs, n_tok);
+    if (ck) return ck;
+    if ((x_bytes && (!x_host || !x_dev)) || (y_bytes && (!y_dev || !y_host))) return SYN_ERR_NULL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (x_bytes && cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return SYN_ERR_CUDA;
+    const int rc = syn_mul_mat_batch(n, descs, n_tok, stream);
+    if (rc) return rc;
+    if (y_bytes && cudaMemcpyAsync(y_host, y_dev, y_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SYN_ERR_CUDA;
     return SYN_OK;
 }
 

@@ -65,6 +65,8 @@ class MatDesc(ctypes.Structure):
 
 
 EXPORTS.append(("syn_mul_mat_batch", _i32, [_i32, ctypes.POINTER(MatDesc), _i64, _vp]))
+EXPORTS.append(("syn_mul_mat_batch_staged", _i32, [_i32, ctypes.POINTER(MatDesc), _i64, _vp, _vp, ctypes.c_size_t,
+                                                   _vp, _vp, ctypes.c_size_t, _vp]))
 
 _u32, _u64, _cp = ctypes.c_uint32, ctypes.c_uint64, ctypes.c_char_p
 _P = ctypes.POINTER
@@ -200,23 +202,37 @@ def mul_mat_batch(items, n_tok: int, stream=None):
 class PreparedBatch:
     """A grouped call whose arguments stay the same from call to call (a decode loop over fixed
     buffers): the descriptor array and the stream handle are marshalled once, and each call is
-    the one syn_mul_mat_batch call.  Holds references to the tensors it points at."""
+    the one syn_mul_mat_batch call.  With `staged=(x_host, x_dev, y_dev, y_host)` (pinned host
+    tensors and the device tensors the products read and write) each call is one
+    syn_mul_mat_batch_staged call instead: host-to-device copy, products, device-to-host copy.
+    Holds references to the tensors it points at."""
 
-    def __init__(self, items, n_tok: int, stream=None):
+    def __init__(self, items, n_tok: int, stream=None, staged=None):
         self._items = list(items)
         self._arr = _descs(self._items)
         self._n = len(self._items)
         self._n_tok = n_tok
         self._stream = _stream(stream)
+        self._staged = staged
+        if staged is not None:
+            xh, xd, yd, yh = staged
+            xb, yb = xh.numel() * xh.element_size(), yh.numel() * yh.element_size()
+            if xd.numel() * xd.element_size() < xb or yd.numel() * yd.element_size() < yb:
+                raise ValueError("staging buffers smaller than their host counterparts")
+            self._sargs = (_ptr(xh), _ptr(xd), xb, _ptr(yd), _ptr(yh), yb)
 
     def __call__(self):
-        rc = syn_mul_mat_batch(self._n, self._arr, self._n_tok, self._stream)
+        if self._staged is None:
+            rc = syn_mul_mat_batch(self._n, self._arr, self._n_tok, self._stream)
+        else:
+            xh, xd, xb, yd, yh, yb = self._sargs
+            rc = syn_mul_mat_batch_staged(self._n, self._arr, self._n_tok, xh, xd, xb, yd, yh, yb, self._stream)
         if rc:
             check(rc, "syn_mul_mat_batch")
 
 
-def prepare_batch(items, n_tok: int, stream=None) -> PreparedBatch:
-    return PreparedBatch(items, n_tok, stream)
+def prepare_batch(items, n_tok: int, stream=None, staged=None) -> PreparedBatch:
+    return PreparedBatch(items, n_tok, stream, staged)
 
 
 def block_sums(t: int, W, n_out: int, n_in: int, Xq, n_tok: int, stream=None):

@@ -184,6 +184,19 @@ typedef struct {
  * is enqueued.  Asynchronous. */
 SYN_API int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_stream_t stream);
 
+/* The grouped call with its inputs and outputs staged through host memory: copies x_bytes
+ * from x_host to x_dev, runs syn_mul_mat_batch(n, descs, n_tok, stream), then copies
+ * y_bytes from y_dev to y_host, all enqueued on `stream` in that order (one cudaMemcpyAsync
+ * each way; x_dev / y_dev are typically one buffer holding every product's X / Y).  x_host
+ * and y_host are HOST pointers (page-locked memory keeps the copies asynchronous); x_dev and
+ * y_dev device pointers.  A byte count of 0 skips that copy (its pointers may then be NULL).
+ * Returns as syn_mul_mat_batch, SYN_ERR_NULL for a missing pointer of a non-empty copy,
+ * SYN_ERR_CUDA if a copy cannot be enqueued (nothing after it is enqueued).  The result is
+ * in y_host once the stream has reached the end of the call. */
+SYN_API int syn_mul_mat_batch_staged(int n, const syn_mat_desc* descs, int64_t n_tok, const void* x_host,
+                                     void* x_dev, size_t x_bytes, const void* y_dev, void* y_host,
+                                     size_t y_bytes, syn_stream_t stream);
+
 /* Pre-size the prefill workspace of (current device, stream) for products with up to
  * max_n_in inputs and max_n_tok tokens, so that later syn_mul_mat calls allocate
  * nothing.  Synchronizes the device when it (re)allocates. */

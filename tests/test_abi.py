@@ -79,3 +79,16 @@ def test_argument_checks_need_no_gpu(lib):
     assert L.syn_quantize_activations(4, p, 1, 256, p, p, p, None) == L.ERR_TYPE
     assert L.syn_quantize_activations(2, p, 1, 256, p, p, None, None) == L.ERR_NULL
     assert L.syn_block_sums(2, p, 1, 300, p, 1, p, None) == L.ERR_SHAPE
+
+
+def test_staged_batch_checks_need_no_gpu(lib):
+    """The host-staged grouped call rejects bad arguments before enqueuing any copy."""
+    L = lib
+    p = 1 << 20
+    d = (L.MatDesc * 1)(L.MatDesc(2, p, 4, 256, p, p))
+    bad = (L.MatDesc * 1)(L.MatDesc(2, p, 4, 100, p, p))  # n_in not a multiple of 256
+    assert L.syn_mul_mat_batch_staged(1, bad, 1, p, p, 1024, p, p, 16, None) == L.ERR_SHAPE
+    assert L.syn_mul_mat_batch_staged(1, d, 1, None, p, 1024, p, p, 16, None) == L.ERR_NULL
+    assert L.syn_mul_mat_batch_staged(1, d, 1, p, p, 1024, p, None, 16, None) == L.ERR_NULL
+    assert L.syn_mul_mat_batch_staged(1, d, -1, p, p, 1024, p, p, 16, None) == L.ERR_SHAPE
+    assert L.syn_mul_mat_batch_staged(0, None, 1, None, None, 0, None, None, 0, None) == L.OK  # nothing to do

@@ -316,6 +316,39 @@ def test_prepared_batch_matches_grouped_call(syn):
     assert syn.device_status() == syn.OK
 
 
+def test_staged_batch_host_buffers(syn):
+    """The host-staged grouped call (inputs copied in from pinned host memory, outputs copied
+    out) gives the device path's outputs, bit for bit, in the host buffer."""
+    shapes = [(oracle.Q4_K, 512, 2048), (oracle.Q6_K, 256, 2048), (oracle.Q4_0, 96, 512)]
+    n_tok = 2
+    xo, yo = [0], [0]
+    for _, n_out, n_in in shapes:
+        xo.append(xo[-1] + n_tok * n_in)
+        yo.append(yo[-1] + n_tok * n_out)
+    xh = torch.from_numpy(synth.normal(700, (xo[-1],))).pin_memory()
+    yh = torch.full((yo[-1],), np.nan).pin_memory()
+    xd, yd = torch.empty(xo[-1], device="cuda"), torch.empty(yo[-1], device="cuda")
+    Ws = [dev(oracle.quantize(wt, synth.normal(710 + k, (n_out, n_in), 0.02))) for k, (wt, n_out, n_in) in enumerate(shapes)]
+    items = [(wt, Ws[k], n_out, n_in, xd[xo[k]:xo[k + 1]].view(n_tok, n_in), yd[yo[k]:yo[k + 1]].view(n_tok, n_out))
+             for k, (wt, n_out, n_in) in enumerate(shapes)]
+    stream = torch.cuda.current_stream()
+    pb = syn.prepare_batch(items, n_tok, stream=stream, staged=(xh, xd, yd, yh))
+    pb()
+    stream.synchronize()
+    got = yh.numpy().copy()
+    assert np.array_equal(xd.cpu().numpy(), xh.numpy())
+    yd.fill_(float("nan"))
+    syn.mul_mat_batch(items, n_tok, stream=stream)  # the same launches on the staged inputs
+    assert np.array_equal(got, host(yd))
+    X = xh.numpy()
+    for k, (wt, n_out, n_in) in enumerate(shapes):
+        Wq = oracle.quantize(wt, synth.normal(710 + k, (n_out, n_in), 0.02))
+        Xk = X[xo[k]:xo[k + 1]].reshape(n_tok, n_in)
+        assert_close(got[yo[k]:yo[k + 1]].reshape(n_tok, n_out), oracle.mul_mat(wt, Wq, n_out, n_in, Xk),
+                     tolerance(wt, Wq, n_in, Xk), f"staged type {wt}")
+    assert syn.device_status() == syn.OK
+
+
 def test_decode_plans_interleaved(syn):
     """Grouped decode calls of different shapes interleaved (the host keeps the last few work
     partitions by shape): every call matches the oracle, and repeats are bit-identical."""
