@@ -337,15 +337,19 @@ __global__ void __launch_bounds__(256) k_act_half(const float* __restrict__ X, i
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    // each warp loads its next blocks before it encodes the current ones, so that a load is in
+    // flight during every encode (the loop is otherwise bound by the load latency)
     if (XT == SYN_Q8_0) {
+        const int e = (lane & 7) * 4;
+        auto load = [&](int64_t b) {
+            return b < n_rows_blocks ? *reinterpret_cast<const float4*>(X + b * 32 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        };
+        float4 xn = load(warp * 4 + (lane >> 3));
         for (int64_t base = warp * 4; base < n_rows_blocks; base += n_warps * 4) {
-            int64_t b = base + (lane >> 3);
-            int e = (lane & 7) * 4;
-            float v[4] = {0.f, 0.f, 0.f, 0.f};
-            if (b < n_rows_blocks) {
-                float4 x = *reinterpret_cast<const float4*>(X + b * 32 + e);
-                v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-            }
+            const int64_t b = base + (lane >> 3);
+            const float4 x = xn;
+            xn = load(b + n_warps * 4);
+            float v[4] = {x.x, x.y, x.z, x.w};
             uint16_t db;
             bool fin;
             uint32_t q = q8_0_group(v, &db, &fin);
@@ -358,10 +362,18 @@ __global__ void __launch_bounds__(256) k_act_half(const float* __restrict__ X, i
             }
         }
     } else {
+        float4 n0 = make_float4(0.f, 0.f, 0.f, 0.f), n1 = n0;
+        if (warp < n_rows_blocks) {
+            n0 = *reinterpret_cast<const float4*>(X + warp * 256 + lane * 8);
+            n1 = *reinterpret_cast<const float4*>(X + warp * 256 + lane * 8 + 4);
+        }
         for (int64_t b = warp; b < n_rows_blocks; b += n_warps) {
-            const float* x = X + b * 256 + lane * 8;
-            float4 x0 = *reinterpret_cast<const float4*>(x);
-            float4 x1 = *reinterpret_cast<const float4*>(x + 4);
+            const float4 x0 = n0, x1 = n1;
+            const int64_t bn = b + n_warps;
+            if (bn < n_rows_blocks) {
+                n0 = *reinterpret_cast<const float4*>(X + bn * 256 + lane * 8);
+                n1 = *reinterpret_cast<const float4*>(X + bn * 256 + lane * 8 + 4);
+            }
             float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
             uint32_t w0, w1;
             float dd;
@@ -537,8 +549,21 @@ cudaError_t launch_quantize_act(int xtype, const float* X, int64_t n_blocks, int
 cudaError_t launch_act_half(int xtype, const float* X, int64_t n_blocks, void* xh, int sms,
                             cudaStream_t s) {
     if (xtype == SYN_F16) return launch_x_to_half(X, n_blocks, xh, sms, s);  // F16: rounding only
-    int64_t warps = (xtype == SYN_Q8_0) ? (n_blocks + 3) / 4 : n_blocks;
-    int g = grid_for(warps, sms);
+    const int64_t warps = (xtype == SYN_Q8_0) ? (n_blocks + 3) / 4 : n_blocks;
+    // one wave of CTAs: as many per SM as are resident at once (the grid-stride loop does the
+    // rest; a second, partial wave would leave SMs idle at its end)
+    static int per_sm[2] = {0, 0};
+    const int which = xtype == SYN_Q8_0 ? 0 : 1;
+    if (per_sm[which] == 0) {
+        int n = 0;
+        const cudaError_t e = which == 0
+            ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_act_half<SYN_Q8_0>, 256, 0)
+            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_act_half<SYN_Q8_K>, 256, 0);
+        per_sm[which] = (e == cudaSuccess && n > 0) ? n : 4;
+    }
+    int64_t ctas = (warps + 7) / 8;
+    if (ctas > (int64_t)sms * per_sm[which]) ctas = (int64_t)sms * per_sm[which];
+    const int g = ctas < 1 ? 1 : (int)ctas;
     __half* h = static_cast<__half*>(xh);
     if (xtype == SYN_Q8_0) k_act_half<SYN_Q8_0><<<g, 256, 0, s>>>(X, n_blocks, h);
     else k_act_half<SYN_Q8_K><<<g, 256, 0, s>>>(X, n_blocks, h);

@@ -9,6 +9,8 @@ Cases (synthetic weights ~N(0, 0.02), activations ~N(0, 1)):
   gemm_q4k_ffn_up    Q4_K 14336 x 4096, 512 tokens  (prefill, tensor cores)
   gemm_q4k_ffn_down  Q4_K 4096 x 14336, 512 tokens
   gemv_llama1b_layer the seven decode products of a Llama-1B-shaped layer, one grouped call
+  prefill_llama8b_layer  one Llama-8B layer at 2048 tokens as a model calls it: q/k/v grouped
+                     on one input, o, gate/up grouped on one input, down (Q4_K, Q6_K v/down)
 """
 from __future__ import annotations
 
@@ -25,7 +27,7 @@ CASES = {
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", required=True, choices=sorted(CASES) + ["gemv_llama1b_layer"])
+    ap.add_argument("--case", required=True, choices=sorted(CASES) + ["gemv_llama1b_layer", "prefill_llama8b_layer"])
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
     import torch
@@ -43,6 +45,25 @@ def main():
         torch.cuda.synchronize()
         assert syn.device_status() == syn.OK
         print(f"{args.case}: {args.reps} grouped calls done")
+        return
+    if args.case == "prefill_llama8b_layer":
+        from gguf_block_quantized_gb300 import workloads
+        lay = workloads.llama8b_q4_k_m(n_layers=1, lm_head=False)  # a Q6_K attn_v / ffn_down layer
+        n_tok = 2048
+        Ws = [syn.quantize(m.wtype, torch.from_numpy(synth.normal(20 + i, (m.n_out, m.n_in), 0.02)).cuda())
+              for i, m in enumerate(lay)]
+        XA, XO, XF = (torch.from_numpy(synth.normal(30 + i, (n_tok, lay[0].n_in))).cuda() for i in range(3))
+        XD = torch.from_numpy(synth.normal(33, (n_tok, lay[6].n_in))).cuda()
+        Ys = [torch.empty((n_tok, m.n_out), device="cuda") for m in lay]
+        syn.syn_reserve(lay[6].n_in, n_tok, torch.cuda.current_stream().cuda_stream)
+        for _ in range(args.reps):
+            syn.mul_mat_batch([(lay[i].wtype, Ws[i], lay[i].n_out, lay[i].n_in, XA, Ys[i]) for i in range(3)], n_tok)
+            syn.mul_mat(lay[3].wtype, Ws[3], lay[3].n_out, lay[3].n_in, XO, Y=Ys[3])
+            syn.mul_mat_batch([(lay[i].wtype, Ws[i], lay[i].n_out, lay[i].n_in, XF, Ys[i]) for i in (4, 5)], n_tok)
+            syn.mul_mat(lay[6].wtype, Ws[6], lay[6].n_out, lay[6].n_in, XD, Y=Ys[6])
+        torch.cuda.synchronize()
+        assert syn.device_status() == syn.OK
+        print(f"{args.case}: {args.reps} layer passes done")
         return
     wt, n_out, n_in, n_tok = CASES[args.case]
     W = syn.quantize(wt, torch.from_numpy(synth.normal(5, (n_out, n_in), 0.02)).cuda())
