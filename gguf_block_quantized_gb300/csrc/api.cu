@@ -293,7 +293,7 @@ int syn_release(void) {
 namespace {
 
 // The prefill path of products that share one activation input (the same X, n_in and
-// vec_dot_type: q/k/v, or gate/up, of a layer): Y of the products split along K zeroed,
+// vec_dot_type: q/k/v, or gate/up, of a layer): the Y columns of split tiles zeroed,
 // X converted once into the workspace, then one tensor-core launch per product.
 int prefill_group(const syn_mat_desc* const* g, int m, int64_t n_tok, const DeviceState* st, cudaStream_t s) {
     const int64_t n_in = g[0]->n_in;
@@ -302,9 +302,7 @@ int prefill_group(const syn_mat_desc* const* g, int m, int64_t n_tok, const Devi
     int rc = workspace_for(s, prefill_ws_bytes(n_in, n_tok), &ws);
     if (rc) return rc;
     for (int i = 0; i < m; i++)
-        if (syn::gemm_needs_zero(g[i]->n_out, n_in, n_tok, sms_of(st)) &&
-            cudaMemsetAsync(g[i]->Y, 0, (size_t)n_tok * g[i]->n_out * sizeof(float), s) != cudaSuccess)
-            return SYN_ERR_CUDA;
+        if (syn::gemm_zero_y(g[i]->Y, g[i]->n_out, n_in, n_tok, sms_of(st), s) != cudaSuccess) return SYN_ERR_CUDA;
     if (launch_act_half(xt, g[0]->X, n_tok * (n_in / elems(xt)), ws, sms_of(st), s) != cudaSuccess) return SYN_ERR_CUDA;
     g_launches++;
     for (int i = 0; i < m; i++) {

@@ -141,8 +141,11 @@ struct GemmParams {
     int n_super;     // 256-k super-steps per row (last one may be partial for Q8_0)
     int bn;          // tokens per tile (multiple of 16, <= 256)
     int n_m, n_n, n_split;
+    int m_full;      // m-tiles [0, m_full) run whole (one unit each, stored); the others are
+                     // split n_split ways along K (their units add into a zeroed Y)
+    int u_full;      // m_full * n_n: units of whole tiles, numbered first
     int n_units;
-    int accumulate;  // 1: add into Y (split-K), 0: store
+    int accumulate;  // 1: some units add into Y (split-K)
     int raw_tma;     // 1: weight slices by one 2-D TMA load per stage (row_bytes % 16 == 0)
     int raw_row;     // bytes per row in a raw stage: BOX (TMA) or RAW_ROW (per-row copies)
     int y_tma;       // 1: Y written by 2-D TMA stores / reduce-adds (n_out % 4 == 0)
@@ -400,13 +403,28 @@ struct GemmSmem {
 };
 
 // unit u -> tile (m, n) and k range [ss0, ss1) in 256-k super-steps (32-bit arithmetic)
-__device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& m, int& n, int& ss0, int& ss1) {
-    const int rest = u / p.n_n;
-    n = u - rest * p.n_n;
-    const int ks = rest / p.n_m;
-    m = rest - ks * p.n_m;
+__device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& m, int& n, int& ss0, int& ss1,
+                                            bool& add) {
+    if (u < p.u_full) {  // a whole tile
+        m = u / p.n_n;
+        n = u - m * p.n_n;
+        ss0 = 0;
+        ss1 = p.n_super;
+        add = false;
+        return;
+    }
+    const int v = u - p.u_full, ts = p.n_m - p.m_full;
+    const int rest = v / p.n_n;
+    n = v - rest * p.n_n;
+    const int ks = rest / ts;
+    m = p.m_full + (rest - ks * ts);
     ss0 = (ks * p.n_super) / p.n_split;
     ss1 = ((ks + 1) * p.n_super) / p.n_split;
+    add = p.n_split > 1;
+}
+__device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& m, int& n, int& ss0, int& ss1) {
+    bool add;
+    unit_coords(p, u, m, n, ss0, ss1, add);
 }
 
 template <int T>
@@ -709,7 +727,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         uint32_t ac = 0;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
             int m, n, ss0, ss1;
-            unit_coords(p, u, m, n, ss0, ss1);
+            bool add;
+            unit_coords(p, u, m, n, ss0, ss1, add);
             const int a = ac & 1;
             if (!mbar_wait(smem_u32(&acc_full[a]), (ac >> 1) & 1, p.err, abort_flag)) break;
             tc_fence_after();
@@ -739,7 +758,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            if (p.accumulate) tma_reduce_add_2d(&ymap, o0, tt, stage_s);
+                            if (add) tma_reduce_add_2d(&ymap, o0, tt, stage_s);
                             else tma_store_2d(&ymap, o0, tt, stage_s);
                             bulk_commit();
                         }
@@ -750,7 +769,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         const int64_t t = (int64_t)t0 + cb + i;
                         if (cb + i < p.bn && t < p.n_tok) {
                             float* dst = p.Y + t * p.n_out + o;
-                            if (p.accumulate) atomicAdd(dst, __uint_as_float(v[i]));
+                            if (add) atomicAdd(dst, __uint_as_float(v[i]));
                             else *dst = __uint_as_float(v[i]);
                         }
                     }
@@ -825,21 +844,39 @@ static_assert(gemm_bars_fit<SYN_Q4_K>() && gemm_bars_fit<SYN_Q6_K>() && gemm_bar
 #define SYN_GEMM_ADD_US_PER_MB 0.08
 #endif
 
-// Pick the K split S (1..16, each split >= 2 super-steps) of least modelled time, the
-// smaller S on ties.
-static int pick_split(int64_t tiles, int n_super, int sms, int bn, int64_t n_out, int64_t n_tok) {
+struct SplitPlan {
+    int S;       // K split of the split tiles (1: none)
+    int m_full;  // m-tiles run whole; the rest are split S ways
+};
+
+// Pick the schedule of least modelled time, the smaller S on ties: S = 1 (whole tiles), every
+// tile split S ways, or whole tiles for the full waves and only the m-tiles of the last,
+// partial wave split S ways (their Y columns are then the only ones zeroed and added into).
+// Each split keeps >= 2 super-steps.
+static SplitPlan pick_split(int n_m, int n_n, int n_super, int sms, int bn, int64_t n_out, int64_t n_tok) {
+    const int64_t tiles = (int64_t)n_m * n_n;
     const double tile_us = 2.0 * GEMM_BM * bn * (double)n_super * GEMM_SUPER / (SYN_GEMM_SM_TFLOPS * 1e6);
-    const double y_mb = 4.0 * (double)n_out * (double)n_tok / 1e6;
-    int best = 1;
-    double best_t = 1e300;
-    for (int S = 1; S <= 16; S++) {
-        if (S > 1 && n_super / S < 2) break;
-        const int64_t waves = (tiles * S + sms - 1) / sms;
-        double t = (double)waves * (tile_us / S + SYN_GEMM_UNIT_US);
-        if (S > 1) t += y_mb * (SYN_GEMM_ZERO_US_PER_MB + S * SYN_GEMM_ADD_US_PER_MB);
-        if (t < best_t * (1.0 - 1e-9)) {
-            best_t = t;
-            best = S;
+    auto y_mb = [&](int m_full) {
+        const int64_t cols = n_out - (int64_t)m_full * GEMM_BM;
+        return cols > 0 ? 4.0 * (double)cols * (double)n_tok / 1e6 : 0.0;
+    };
+    // m-tiles whose every token tile fits in the full waves
+    const int m_tail_from = (int)std::min<int64_t>(n_m, (tiles / sms) * sms / n_n);
+    SplitPlan best{1, n_m};
+    double best_t = (double)((tiles + sms - 1) / sms) * (tile_us + SYN_GEMM_UNIT_US);
+    for (int S = 2; S <= 16; S++) {
+        if (n_super / S < 2) break;
+        const double add = SYN_GEMM_ZERO_US_PER_MB + S * SYN_GEMM_ADD_US_PER_MB;
+        for (int m_full : {0, m_tail_from}) {
+            if (m_full >= n_m) continue;
+            const int64_t u_full = (int64_t)m_full * n_n, u_tail = (tiles - u_full) * S;
+            const double t = (double)((u_full + sms - 1) / sms) * (tile_us + SYN_GEMM_UNIT_US) +
+                             (double)((u_tail + sms - 1) / sms) * (tile_us / S + SYN_GEMM_UNIT_US) + y_mb(m_full) * add;
+            if (t < best_t * (1.0 - 1e-9)) {
+                best_t = t;
+                best = SplitPlan{S, m_full};
+            }
+            if (m_tail_from == 0) break;  // the two schedules coincide
         }
     }
     return best;
@@ -870,12 +907,21 @@ static cudaError_t run_gemm(GemmParams p, const CUtensorMap& map, const CUtensor
 
 static int gemm_bn(int64_t n_tok) { return (int)std::min<int64_t>(256, (n_tok + 15) / 16 * 16); }
 
-// Whether the product splits along K: its Y must then be zeroed before the activation
-// conversion is enqueued (the product kernel overlaps the conversion).
-bool gemm_needs_zero(int64_t n_out, int64_t n_in, int64_t n_tok, int sms) {
+static SplitPlan plan_of(int64_t n_out, int64_t n_in, int64_t n_tok, int sms) {
     const int bn = gemm_bn(n_tok);
-    const int64_t tiles = ((n_out + GEMM_BM - 1) / GEMM_BM) * ((n_tok + bn - 1) / bn);
-    return pick_split(tiles, (int)((n_in + GEMM_SUPER - 1) / GEMM_SUPER), sms, bn, n_out, n_tok) > 1;
+    return pick_split((int)((n_out + GEMM_BM - 1) / GEMM_BM), (int)((n_tok + bn - 1) / bn),
+                      (int)((n_in + GEMM_SUPER - 1) / GEMM_SUPER), sms, bn, n_out, n_tok);
+}
+
+// Zero the columns of Y that the product's split tiles add into (none when it does not
+// split): to be enqueued before the activation conversion (the product kernel overlaps it).
+cudaError_t gemm_zero_y(float* Y, int64_t n_out, int64_t n_in, int64_t n_tok, int sms, cudaStream_t s) {
+    const SplitPlan sp = plan_of(n_out, n_in, n_tok, sms);
+    if (sp.S == 1) return cudaSuccess;
+    const int64_t c0 = (int64_t)sp.m_full * GEMM_BM;
+    if (c0 == 0) return cudaMemsetAsync(Y, 0, (size_t)n_tok * n_out * sizeof(float), s);
+    return cudaMemset2DAsync(Y + c0, (size_t)n_out * sizeof(float), 0, (size_t)(n_out - c0) * sizeof(float),
+                             (size_t)n_tok, s);
 }
 
 cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, const void* xh, int64_t n_tok,
@@ -899,8 +945,11 @@ cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, co
     const int64_t tiles = (int64_t)p.n_m * p.n_n;
     if (tiles * 16 > (int64_t(1) << 30) || (int64_t)p.n_super * 16 > (int64_t(1) << 30))
         return cudaErrorInvalidValue;  // 32-bit unit and super-step arithmetic
-    p.n_split = pick_split(tiles, p.n_super, sms, p.bn, n_out, n_tok);
-    p.n_units = (int)(tiles * p.n_split);
+    const SplitPlan sp = plan_of(n_out, n_in, n_tok, sms);
+    p.n_split = sp.S;
+    p.m_full = sp.m_full;
+    p.u_full = p.m_full * p.n_n;
+    p.n_units = (int)((int64_t)p.u_full + ((int64_t)p.n_m - p.m_full) * p.n_n * p.n_split);
     p.accumulate = p.n_split > 1 ? 1 : 0;
     // kind::f16 instruction descriptor: D fp32, A and B fp16, both K-major, N, M = 128
     p.idesc = (1u << 4) | ((uint32_t)(p.bn >> 3) << 17) | ((uint32_t)(GEMM_BM >> 4) << 24);

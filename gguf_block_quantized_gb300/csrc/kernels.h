@@ -43,11 +43,11 @@ int sm_limit();
 
 // Prefill product on the tensor cores.  xh: n_tok x n_in fp16 activations, written by
 // launch_act_half immediately before on the same stream (the product kernel is its
-// programmatic dependent).  Y is overwritten, or, when gemm_needs_zero() is true, added
-// into: the caller then zeroes Y before launch_act_half.
+// programmatic dependent).  Y is overwritten, except where the product splits along K: those
+// columns are added into, so the caller enqueues gemm_zero_y() before launch_act_half.
 cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, const void* xh,
                         int64_t n_tok, float* Y, int* err, int sms, cudaStream_t s);
-bool gemm_needs_zero(int64_t n_out, int64_t n_in, int64_t n_tok, int sms);
+cudaError_t gemm_zero_y(float* Y, int64_t n_out, int64_t n_in, int64_t n_tok, int sms, cudaStream_t s);
 
 // F16 weights (n_in % 8 == 0): X -> fp16 (round to nearest even) into xh, and the decode
 // product reading W and the fp16 activations from ws (n_tok * n_in halves).

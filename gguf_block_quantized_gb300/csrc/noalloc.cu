@@ -86,9 +86,7 @@ extern "C" int syn_mul_mat_prefill_static(int type, const void* W, int64_t n_out
     void* xh = d->scratch + kHeader;
     const int xt = (type == SYN_TYPE_Q4_K || type == SYN_TYPE_Q6_K) ? SYN_TYPE_Q8_K
                  : type == SYN_TYPE_F16 ? SYN_TYPE_F16 : SYN_TYPE_Q8_0;
-    if (syn::gemm_needs_zero(n_out, n_in, n_tok, sms) &&
-        cudaMemsetAsync(Y, 0, (size_t)n_tok * n_out * sizeof(float), s) != cudaSuccess)
-        return SYN_ERR_CUDA;
+    if (syn::gemm_zero_y(Y, n_out, n_in, n_tok, sms, s) != cudaSuccess) return SYN_ERR_CUDA;
     if (syn::launch_act_half(xt, X, n_tok * (n_in / be), xh, sms, s) != cudaSuccess) return SYN_ERR_CUDA;
     syn::note_launches(1);
     if (syn::launch_gemm(type, W, n_out, n_in, xh, n_tok, Y, err, sms, s) != cudaSuccess) return SYN_ERR_CUDA;

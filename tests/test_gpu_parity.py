@@ -240,6 +240,14 @@ def test_mul_mat_gemm(syn, wt, shape):
     assert_close(Y, ref, bound, f"gemm {shape}")
 
 
+@pytest.mark.parametrize("wt", [oracle.Q4_K, oracle.Q6_K])
+def test_mul_mat_gemm_tail_split(syn, wt):
+    """160 row tiles on 152 SMs: whole tiles for the full wave, the last m-tiles split along K
+    and added into their zeroed Y columns (ragged last tile), the other columns stored."""
+    Y, ref, bound = run_mul_mat(syn, wt, 160 * 128 - 37, 1024, 16, 850 + wt, "gemm")
+    assert_close(Y, ref, bound, "tail-split prefill")
+
+
 @pytest.mark.parametrize("wt", [oracle.Q8_0, oracle.Q4_0, oracle.Q5_0])
 def test_mul_mat_row_not_multiple_of_256(syn, wt):
     # the 32-weight formats need only 32-element blocks: 800 = 25 blocks (ragged last k-step)
