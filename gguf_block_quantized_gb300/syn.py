@@ -128,6 +128,9 @@ def _torch():
 
 
 def _stream(stream=None) -> int:
+    """A torch stream (None: the current one) or a raw cudaStream_t value, as an integer."""
+    if isinstance(stream, int):
+        return stream
     torch = _torch()
     s = torch.cuda.current_stream() if stream is None else stream
     return int(s.cuda_stream)

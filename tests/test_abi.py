@@ -92,3 +92,19 @@ def test_staged_batch_checks_need_no_gpu(lib):
     assert L.syn_mul_mat_batch_staged(1, d, 1, p, p, 1024, p, None, 16, None) == L.ERR_NULL
     assert L.syn_mul_mat_batch_staged(1, d, -1, p, p, 1024, p, p, 16, None) == L.ERR_SHAPE
     assert L.syn_mul_mat_batch_staged(0, None, 1, None, None, 0, None, None, 0, None) == L.OK  # nothing to do
+
+
+def test_prepared_batch_staging_sizes_checked(lib):
+    """prepare_batch(..., staged=...) checks the staging buffers against their host
+    counterparts when it is built (marshalling only: nothing is called)."""
+    import torch
+    W = torch.zeros(16 * 144 // 4, dtype=torch.int32)  # one Q4_K row of 4096 values, as bytes
+    X, Y = torch.zeros(4096), torch.zeros(1)
+    items = [(lib.Q4_K, W, 1, 4096, X, Y)]
+    xh, yh = torch.zeros(4096), torch.zeros(1)
+    with pytest.raises(ValueError):
+        lib.PreparedBatch(items, 1, stream=0, staged=(xh, torch.zeros(100), Y, yh))
+    with pytest.raises(ValueError):
+        lib.PreparedBatch(items, 1, stream=0, staged=(xh, X, torch.zeros(0), yh))
+    pb = lib.PreparedBatch(items, 1, stream=0, staged=(xh, X, Y, yh))
+    assert pb._sargs[2] == 4096 * 4 and pb._sargs[5] == 4
