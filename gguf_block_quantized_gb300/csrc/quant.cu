@@ -4,6 +4,8 @@
 // "The GGML ecosystem, and where synapse fits", section 5: block formats (format table),
 // dequantize_row_* (embedding / norm expansion) and the activation conversion to the
 // vec_dot_type ("Products: weights against quantized activations").
+#include <atomic>
+
 #include "kernels.h"
 #include "quant_dev.cuh"
 
@@ -552,17 +554,19 @@ cudaError_t launch_act_half(int xtype, const float* X, int64_t n_blocks, void* x
     const int64_t warps = (xtype == SYN_Q8_0) ? (n_blocks + 3) / 4 : n_blocks;
     // one wave of CTAs: as many per SM as are resident at once (the grid-stride loop does the
     // rest; a second, partial wave would leave SMs idle at its end)
-    static int per_sm[2] = {0, 0};
+    static std::atomic<int> per_sm_cache[2];  // 0: not known yet
     const int which = xtype == SYN_Q8_0 ? 0 : 1;
-    if (per_sm[which] == 0) {
+    int per_sm = per_sm_cache[which].load();
+    if (per_sm == 0) {
         int n = 0;
         const cudaError_t e = which == 0
             ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_act_half<SYN_Q8_0>, 256, 0)
             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_act_half<SYN_Q8_K>, 256, 0);
-        per_sm[which] = (e == cudaSuccess && n > 0) ? n : 4;
+        per_sm = (e == cudaSuccess && n > 0) ? n : 4;
+        per_sm_cache[which].store(per_sm);
     }
     int64_t ctas = (warps + 7) / 8;
-    if (ctas > (int64_t)sms * per_sm[which]) ctas = (int64_t)sms * per_sm[which];
+    if (ctas > (int64_t)sms * per_sm) ctas = (int64_t)sms * per_sm;
     const int g = ctas < 1 ? 1 : (int)ctas;
     __half* h = static_cast<__half*>(xh);
     if (xtype == SYN_Q8_0) k_act_half<SYN_Q8_0><<<g, 256, 0, s>>>(X, n_blocks, h);
