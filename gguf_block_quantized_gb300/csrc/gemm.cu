@@ -12,7 +12,9 @@
 // GGUF", CPU and Edge Inference), so this path feeds the tensor cores.
 //
 // One persistent CTA per SM, warp-specialised, one 128 x BN output tile per work unit
-// (BN <= 256 tokens), optionally split along K:
+// (BN <= 256 tokens).  Tiles that do not fill the SMs in whole waves are split along K (all
+// of them, or only those of the last, partial wave; a cost model picks): the units of a
+// split tile add their partial sums into a Y zeroed beforehand.  Warp roles:
 //   warp 0      raw-weight producer: 128 rows x 256 k of weight blocks per raw stage, by
 //               one 2-D TMA load when the row pitch is a multiple of 16 bytes (else one
 //               1-D bulk copy per row);
