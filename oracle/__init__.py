@@ -12,8 +12,10 @@ examples/simple (ggml_mul_mat(A, B^T) = C^T).
 Parity status per function (see the tests under tests/test_oracle_*.py for the pins):
   fp16 conversion        pinned (numpy.float16 on a dense sample, boundaries exhaustive)
   quantize Q8_0/Q8_K     pinned (hand blocks, error bound, fixed point, bsum invariant)
-  quantize Q4_K/Q6_K     pinned to error bounds, fixed point and hand blocks; the encoders
-                         themselves are the plain readings of the format table
+  quantize Q4_K/Q6_K     pinned to hand-worked super-blocks (tests/golden/q4_k_worked.txt,
+                         q6_k_worked.txt: super-scales, every sub-block scale and min, every
+                         code, with rounding ties and clamps) and to the closed-form error
+                         bounds; the encoders are the plain readings of the format table
   quantize Q4_0/Q5_0     pinned to error bounds, the exact extreme, hand blocks
   F16 weights            pinned (the fp16 conversion; the product against numpy float16 casts)
   dequantize             pinned (hand-written block bytes against the format formulas)

@@ -79,6 +79,23 @@ def test_quantize_bit_exact(syn, t, shape):
     assert mism[0].size == 0, f"{mism[0].size} bytes differ, first at {mism[0][:3]}, {mism[1][:3]}"
 
 
+@pytest.mark.parametrize("t,name,n_sub", [(oracle.Q4_K, "q4_k_worked.txt", 8), (oracle.Q6_K, "q6_k_worked.txt", 16)])
+def test_quantize_worked_blocks_bit_exact(syn, t, name, n_sub):
+    """The hand-worked K-quant super-blocks (tests/golden; their scales, mins and codes are
+    pinned on the CPU) encode to the same bytes on the GPU, alone and amid other rows."""
+    import os
+    from conftest import GOLDEN, read_fixture
+    fx = read_fixture(os.path.join(GOLDEN, name))
+    xb = np.concatenate([np.array([float(v) for v in fx[f"x{j}"].split()], np.float32) for j in range(n_sub)])
+    x = inputs_mixed(9, 768, 55)
+    x[0, :256] = xb
+    x[4, 512:] = xb
+    want = oracle.quantize(t, x)
+    got = host(syn.quantize(t, dev(x)))
+    assert np.array_equal(got, want)
+    assert np.array_equal(got[0, :oracle.BLOCK_BYTES[t]], oracle.quantize(t, xb.reshape(1, 256))[0])
+
+
 @pytest.mark.parametrize("t", TYPES_ALL)
 def test_dequantize_bit_exact(syn, t):
     n_rows, n = 53, 1024

@@ -203,6 +203,52 @@ def test_q8_0_ties_away_from_zero():
     assert list(b[2:2 + tx.size].view(np.int8)) == list(tq)
 
 
+# ----------------------------------------------------------------------------------------
+# K-quant encoders: hand-worked super-blocks (format table, "The GGML ecosystem...", section 5;
+# the min-max / symmetric readings of the Q4_K and Q6_K rows).  Scales are chosen so that
+# round and floor, and round-half-away and round-half-even, give different sub-block scales,
+# and so that the super-scales are powers of two only for the divisors 63 / 127.
+# ----------------------------------------------------------------------------------------
+
+WQ4 = read_fixture(os.path.join(GOLDEN, "q4_k_worked.txt"))
+WQ6 = read_fixture(os.path.join(GOLDEN, "q6_k_worked.txt"))
+
+
+def _worked_inputs(fix, n_sub):
+    x = np.concatenate([np.array([float(v) for v in fix[f"x{j}"].split()], dtype=np.float32)
+                        for j in range(n_sub)])
+    assert x.size == 256
+    return x
+
+
+def test_q4_k_worked_block():
+    x = _worked_inputs(WQ4, 8)
+    b = oracle.quantize(Q4_K, x.reshape(1, 256))[0]
+    d, dm, sc, mn, q = oracle.unpack_q4_k(b)
+    assert d == int(WQ4["d_bits"], 16) and dm == int(WQ4["dmin_bits"], 16)
+    assert [int(v) for v in sc] == list(_ints(WQ4["sc"]))
+    assert [int(v) for v in mn] == list(_ints(WQ4["mn"]))
+    first, second, lst = _ints(WQ4["q_first"]), _ints(WQ4["q_second"]), _ints(WQ4["q_list"])
+    for j in range(8):
+        qj = [int(v) for v in q[32 * j:32 * j + 32]]
+        want = [0] * 32 if int(_ints(WQ4["sc"])[j]) == 0 else [int(first[j]), int(second[j])] + list(lst)
+        assert qj == want, j
+
+
+def test_q6_k_worked_block():
+    x = _worked_inputs(WQ6, 16)
+    b = oracle.quantize(Q6_K, x.reshape(1, 256))[0]
+    d, sc, q = oracle.unpack_q6_k(b)
+    assert d == int(WQ6["d_bits"], 16)
+    assert [int(v) for v in sc] == list(_ints(WQ6["sc"]))
+    first, lst = _ints(WQ6["q_first"]), _ints(WQ6["q_list"])
+    zero = set(int(v) for v in _ints(WQ6["zero_code_subblocks"]))
+    for j in range(16):
+        qj = [int(v) for v in q[16 * j:16 * j + 16]]
+        want = [32] * 16 if j in zero else [int(first[j])] + list(lst)
+        assert qj == want, j
+
+
 def test_zero_blocks_give_zero_scales_and_codes():
     for t in (Q8_0, Q4_K, Q6_K, Q8_K):
         n = oracle.BLOCK_ELEMS[t]
