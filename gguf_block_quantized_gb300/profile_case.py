@@ -9,6 +9,9 @@ Cases (synthetic weights ~N(0, 0.02), activations ~N(0, 1)):
   gemm_q4k_ffn_up    Q4_K 14336 x 4096, 512 tokens  (prefill, tensor cores)
   gemm_q4k_ffn_down  Q4_K 4096 x 14336, 512 tokens
   gemv_llama1b_layer the seven decode products of a Llama-1B-shaped layer, one grouped call
+  gemv_llama8b_layers  the grouped decode calls of two Llama-8B Q4_K_M layers, alternating:
+                     layer 0 (Q6_K attn_v / ffn_down) and layer 4 (all Q4_K), the weights and
+                     inputs of the benchmark's sweep
   prefill_llama8b_layer  one Llama-8B layer at 2048 tokens as a model calls it: q/k/v grouped
                      on one input, o, gate/up grouped on one input, down (Q4_K, Q6_K v/down)
 """
@@ -27,7 +30,8 @@ CASES = {
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", required=True, choices=sorted(CASES) + ["gemv_llama1b_layer", "prefill_llama8b_layer"])
+    ap.add_argument("--case", required=True, choices=sorted(CASES) + ["gemv_llama1b_layer", "gemv_llama8b_layers",
+                                                                     "prefill_llama8b_layer"])
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
     import torch
@@ -45,6 +49,26 @@ def main():
         torch.cuda.synchronize()
         assert syn.device_status() == syn.OK
         print(f"{args.case}: {args.reps} grouped calls done")
+        return
+    if args.case == "gemv_llama8b_layers":
+        from gguf_block_quantized_gb300 import workloads
+        mats = workloads.llama8b_q4_k_m()
+        d, f = mats[0].n_in, mats[6].n_in
+        xs = [torch.from_numpy(synth.activations(5, j, 1, n)).cuda() for j, n in enumerate([d, d, d, f])]
+        src = [xs[0], xs[0], xs[0], xs[1], xs[2], xs[2], xs[3]]
+        calls = []
+        for k in (0, 4):
+            lay = mats[7 * k:7 * k + 7]
+            Ws = [syn.quantize(m.wtype, torch.from_numpy(synth.weight(5, 7 * k + i, m.n_out, m.n_in)).cuda())
+                  for i, m in enumerate(lay)]
+            Ys = [torch.empty((1, m.n_out), device="cuda") for m in lay]
+            calls.append([(m.wtype, Ws[i], m.n_out, m.n_in, src[i], Ys[i]) for i, m in enumerate(lay)])
+        for _ in range(args.reps):
+            for c in calls:
+                syn.mul_mat_batch(c, 1)
+        torch.cuda.synchronize()
+        assert syn.device_status() == syn.OK
+        print(f"{args.case}: {args.reps} x 2 grouped calls done")
         return
     if args.case == "prefill_llama8b_layer":
         from gguf_block_quantized_gb300 import workloads
