@@ -374,6 +374,13 @@ int check_batch(int n, const syn_mat_desc* descs, int64_t n_tok) {
         if (!d.W || !d.X || !d.Y) return SYN_ERR_NULL;
         if (!aligned16(d.W) || !aligned16(d.X) || !aligned16(d.Y)) return SYN_ERR_ALIGN;
     }
+    // deterministic mode runs every quantized product on the decode kernel: a row too wide
+    // for its shared memory is rejected here, before any product of the call is enqueued
+    if (g_det.load())
+        for (int i = 0; i < n; i++)
+            if (descs[i].type != SYN_TYPE_F16 &&
+                syn::gemv_act_bytes(descs[i].type, descs[i].n_in) > syn::gemv_act_limit())
+                return SYN_ERR_SHAPE;
     return SYN_OK;
 }
 
@@ -451,6 +458,11 @@ int syn_mul_mat_batch_staged(int n, const syn_mat_desc* descs, int64_t n_tok, co
     const int ck = check_batch(n, descs, n_tok);
     if (ck) return ck;
     if ((x_bytes && (!x_host || !x_dev)) || (y_bytes && (!y_dev || !y_host))) return SYN_ERR_NULL;
+    if (n > 0 && n_tok > 0) {  // the device checks of syn_mul_mat_batch, before the copy
+        DeviceState* st;
+        const int rc = device_state(&st);
+        if (rc) return rc;
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (x_bytes && cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return SYN_ERR_CUDA;
@@ -480,14 +492,26 @@ int syn_block_sums(int type, const void* W, int64_t n_out, int64_t n_in, const v
 }
 
 int syn_device_status(int clear) {
-    DeviceState* st;
-    int rc = device_state(&st);
-    if (rc) return rc;
+    // Two words can hold a timeout: the per-device word of the allocating entry points and
+    // the one at the head of syn_mul_mat_prefill_static's fixed array.  Neither is created
+    // here, so a caller of the static entry point alone still allocates nothing.
+    int dev;
+    if (current_device(&dev) != SYN_OK) return SYN_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return SYN_ERR_CUDA;
-    int w = 0;
-    if (cudaMemcpy(&w, st->words, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SYN_ERR_CUDA;
-    if (clear && cudaMemset(st->words, 0, sizeof(int)) != cudaSuccess) return SYN_ERR_CUDA;
-    return w ? SYN_ERR_TIMEOUT : SYN_OK;
+    int* words = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_dev.find(dev);
+        if (it != g_dev.end() && it->second.init) words = it->second.words;
+    }
+    int w = 0, ws = 0;
+    if (words) {
+        if (cudaMemcpy(&w, words, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SYN_ERR_CUDA;
+        if (clear && cudaMemset(words, 0, sizeof(int)) != cudaSuccess) return SYN_ERR_CUDA;
+    }
+    const int rc = syn::static_status(dev, clear, &ws);
+    if (rc) return rc;
+    return (w || ws) ? SYN_ERR_TIMEOUT : SYN_OK;
 }
 
 }  // extern "C"

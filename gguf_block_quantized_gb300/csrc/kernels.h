@@ -58,4 +58,9 @@ cudaError_t launch_gemv_f16(const void* W, int64_t n_out, int64_t n_in, const fl
 // Adds n to the count syn_launch_count reports.
 void note_launches(int n);
 
+// The status word of syn_mul_mat_prefill_static's fixed array on device dev: *word gets it
+// (0 when that entry point has not run on dev); clear != 0 resets it.  Allocates nothing;
+// the caller synchronizes the device first.
+int static_status(int dev, int clear, int* word);
+
 }  // namespace syn

@@ -63,11 +63,30 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 }  // namespace
 
+namespace syn {
+
+// Read (and optionally reset) the status word at the head of the fixed array; a device
+// that has not run syn_mul_mat_prefill_static has none and reads as 0.
+int static_status(int dev, int clear, int* word) {
+    *word = 0;
+    if (dev < 0 || dev >= 64) return SYN_OK;
+    std::lock_guard<std::mutex> lk(g_mu);
+    const StaticDevice& d = g_devices[dev];
+    if (!d.ready) return SYN_OK;
+    if (cudaMemcpy(word, d.scratch, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SYN_ERR_CUDA;
+    if (clear && cudaMemset(d.scratch, 0, sizeof(int)) != cudaSuccess) return SYN_ERR_CUDA;
+    return SYN_OK;
+}
+
+}  // namespace syn
+
 extern "C" int syn_mul_mat_prefill_static(int type, const void* W, int64_t n_out, int64_t n_in, const float* X,
                                           int64_t n_tok, float* Y, syn_stream_t stream) {
     if (type < SYN_TYPE_Q8_0 || type > SYN_TYPE_F16 || type == SYN_TYPE_Q8_K) return SYN_ERR_TYPE;
     const int64_t be = syn::block_elems(type);
-    if (n_out <= 0 || n_in <= 0 || n_tok < 0 || n_in % be || n_out > (int64_t(1) << 31) ||
+    // F16 rows are read 16 bytes (8 values) at a time, as in syn_mul_mat
+    const int64_t row_multiple = type == SYN_TYPE_F16 ? 8 : be;
+    if (n_out <= 0 || n_in <= 0 || n_tok < 0 || n_in % row_multiple || n_out > (int64_t(1) << 31) ||
         n_out * n_in > (int64_t(1) << 40) || n_tok * n_out > (int64_t(1) << 40))
         return SYN_ERR_SHAPE;
     if (n_tok > (int64_t)(SYN_STATIC_SCRATCH_BYTES / 2) / n_in) return SYN_ERR_TOO_LARGE;

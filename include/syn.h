@@ -180,8 +180,8 @@ typedef struct {
  * decodes (or rows too wide for the decode kernel) take the prefill path; those of them that
  * share one activation input (the same X pointer, n_in and vec_dot_type, e.g. q/k/v or
  * gate/up of a layer) convert it once and run one tensor-core launch each.  F16 products in
- * decode run as in syn_mul_mat.  Arguments are checked as for syn_mul_mat before anything
- * is enqueued.  Asynchronous. */
+ * decode run as in syn_mul_mat.  Arguments are checked as for syn_mul_mat (including the
+ * deterministic mode's row-width limit) before anything is enqueued.  Asynchronous. */
 SYN_API int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, syn_stream_t stream);
 
 /* The grouped call with its inputs and outputs staged through host memory: copies x_bytes
@@ -191,8 +191,11 @@ SYN_API int syn_mul_mat_batch(int n, const syn_mat_desc* descs, int64_t n_tok, s
  * and y_host are HOST pointers (page-locked memory keeps the copies asynchronous); x_dev and
  * y_dev device pointers.  A byte count of 0 skips that copy (its pointers may then be NULL).
  * Returns as syn_mul_mat_batch, SYN_ERR_NULL for a missing pointer of a non-empty copy,
- * SYN_ERR_CUDA if a copy cannot be enqueued (nothing after it is enqueued).  The result is
- * in y_host once the stream has reached the end of the call. */
+ * SYN_ERR_CUDA if a copy cannot be enqueued (nothing after it is enqueued).  Argument,
+ * shape, alignment and device errors are returned before anything is enqueued; only
+ * SYN_ERR_NOMEM (workspace growth failed) or SYN_ERR_CUDA can come after the input copy,
+ * and possibly some products, were enqueued.  The result is in y_host once the stream has
+ * reached the end of the call. */
 SYN_API int syn_mul_mat_batch_staged(int n, const syn_mat_desc* descs, int64_t n_tok, const void* x_host,
                                      void* x_dev, size_t x_bytes, const void* y_dev, void* y_host,
                                      size_t y_bytes, syn_stream_t stream);
@@ -246,9 +249,10 @@ SYN_API int syn_set_deterministic(int on);
  * caller leave SMs to concurrent work; the grid of every kernel is sized to the limit. */
 SYN_API int syn_set_sm_limit(int n);
 
-/* Read (and with clear != 0, reset) the device-side error word of the current device:
- * SYN_OK, or SYN_ERR_TIMEOUT if a kernel gave up a bounded wait.  Synchronizes the
- * device. */
+/* Read (and with clear != 0, reset) the device-side error words of the current device:
+ * SYN_OK, or SYN_ERR_TIMEOUT if a kernel of any entry point (syn_mul_mat_prefill_static
+ * included) gave up a bounded wait since the last clear.  Synchronizes the device.  It
+ * allocates nothing: a device on which no product has run reads SYN_OK. */
 SYN_API int syn_device_status(int clear);
 
 /* Number of kernels this library has launched in this process (all devices). */
@@ -267,7 +271,9 @@ SYN_API int64_t syn_launch_count(void);
  * SYN_STATIC_SCRATCH_BYTES that the library holds on every device it is used on until
  * the process exits.  Products with n_tok * n_in * 2 > SYN_STATIC_SCRATCH_BYTES are
  * rejected with SYN_ERR_TOO_LARGE.  Arguments, layout, accuracy and the other error codes
- * are those of syn_mul_mat.  The first call on a device sets up that device (looks up the
+ * are those of syn_mul_mat (F16 weights need n_in % 8 == 0, as there).  A bounded-wait
+ * timeout of its kernels is reported by syn_device_status, like those of syn_mul_mat; the
+ * status word sits at the head of the fixed array.  The first call on a device sets up that device (looks up the
  * array's device address, clears its status word, synchronizes the device): make it
  * before any stream capture.  Every call on a device shares the one array and overwrites
  * it, so calls that can overlap on the GPU (different streams without ordering between

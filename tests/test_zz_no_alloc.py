@@ -3,10 +3,12 @@ memory (fixed arenas, allocators or budgets that forbid cudaMalloc, paths that m
 let a library synchronize the device through cudaMalloc/cudaFree).  Its scratch is a
 fixed device array inside the library.
 
-Checked through the C ABI against syn_mul_mat's own prefill path, within the tolerance of
-the parity tests (1e-4 * ||dequant(w_row)||_2 * ||x||_2 per element), on two calls in a
-row with different problems, so that the second call runs on scratch the first one left
-behind.  Kept in a file that pytest collects last.
+Each product is checked through the C ABI against the CPU oracle, within the tolerance of
+the parity tests (1e-4 * ||dequant(w_row)||_2 * ||x||_2 per element), on calls in a row
+with different problems, so that every call after the first runs on scratch the one
+before it left behind.  A product that fills the array exactly checks its last tokens
+(the end of the array).  After the calls, syn_device_status reports no timeout.  Kept in a
+file that pytest collects last.
 """
 import numpy as np
 import pytest
@@ -32,14 +34,6 @@ def bound(wt, Wq, n_in, X):
     return TOL * np.sqrt((X.astype(np.float64) ** 2).sum(1))[:, None] * np.sqrt((wd ** 2).sum(1))[None, :]
 
 
-def existing_prefill(syn, wt, Wd, n_out, n_in, Xd):
-    old = syn.set_gemv_max_tok(0)
-    try:
-        return syn.mul_mat(wt, Wd, n_out, n_in, Xd)
-    finally:
-        syn.set_gemv_max_tok(old)
-
-
 def static_prefill(syn, wt, Wd, n_out, n_in, Xd):
     Y = torch.full((Xd.shape[0], n_out), float("nan"), device="cuda")
     s = torch.cuda.current_stream().cuda_stream
@@ -49,24 +43,52 @@ def static_prefill(syn, wt, Wd, n_out, n_in, Xd):
     return Y
 
 
-def test_static_scratch_matches_existing_prefill_two_calls(syn):
-    cases = [(oracle.Q4_K, 1000, 2048, 300, 71), (oracle.Q6_K, 333, 1536, 40, 72)]
+def check(Y, ref, bnd, what):
+    assert np.isfinite(Y).all(), what
+    err = np.abs(Y.astype(np.float64) - ref.astype(np.float64))
+    assert (err <= bnd).all(), f"{what}: {(err > bnd).sum()} outside, max err/bound {(err / bnd).max():.3g}"
+
+
+def test_static_scratch_matches_oracle_calls_in_a_row(syn):
+    syn.device_status(True)
+    cases = [(oracle.Q4_K, 1000, 2048, 300, 71), (oracle.Q6_K, 333, 1536, 40, 72),
+             (oracle.Q8_0, 257, 1024, 130, 73), (oracle.F16, 200, 520, 77, 74),
+             (oracle.Q4_K, 128, 512, 9, 75)]
     for wt, n_out, n_in, n_tok, seed in cases:
         W = oracle.quantize(wt, synth.normal(seed, (n_out, n_in), 0.02))
         X = synth.normal(seed + 100, (n_tok, n_in))
-        Wd, Xd = torch.from_numpy(W).cuda(), torch.from_numpy(X).cuda()
-        got = static_prefill(syn, wt, Wd, n_out, n_in, Xd)
-        want = existing_prefill(syn, wt, Wd, n_out, n_in, Xd)
+        got = static_prefill(syn, wt, torch.from_numpy(W).cuda(), n_out, n_in, torch.from_numpy(X).cuda())
         torch.cuda.synchronize()
-        got, want = got.cpu().numpy(), want.cpu().numpy()
-        assert np.isfinite(got).all()
-        err = np.abs(got.astype(np.float64) - want.astype(np.float64))
-        assert (err <= bound(wt, W, n_in, X)).all(), f"case {(wt, n_out, n_in, n_tok)}: max err {err.max()}"
+        ref = oracle.mul_mat(wt, W, n_out, n_in, X)
+        check(got.cpu().numpy(), ref, bound(wt, W, n_in, X), f"{oracle.NAMES[wt]} {n_out}x{n_in} n_tok={n_tok}")
+    assert syn.device_status(True) == syn.OK
 
 
-def test_static_scratch_rejects_oversize(syn):
+def test_static_scratch_at_exact_capacity(syn):
+    """n_tok * n_in * 2 == the array's size: the last token's fp16 activations end at the
+    array's last byte.  Sampled outputs (always the last tokens) against the oracle."""
+    n_in = 4096
+    n_tok = syn.STATIC_SCRATCH_BYTES // (2 * n_in)
+    n_out = 160
+    wt = oracle.Q4_K
+    W = oracle.quantize(wt, synth.normal(81, (n_out, n_in), 0.02))
+    X = synth.normal(82, (n_tok, n_in))
+    got = static_prefill(syn, wt, torch.from_numpy(W).cuda(), n_out, n_in, torch.from_numpy(X).cuda())
+    torch.cuda.synchronize()
+    got = got.cpu().numpy()
+    rows = np.unique(np.concatenate([[0, n_out - 1], synth.integers(83, 24, 0, n_out)]))
+    toks = np.unique(np.concatenate([[0, n_tok - 2, n_tok - 1], synth.integers(84, 8, 0, n_tok)]))
+    ref = oracle.mul_mat_sampled(wt, W, n_out, n_in, X, rows, toks)
+    check(got[toks][:, rows], ref, bound(wt, W[rows], n_in, X[toks]), "exact capacity")
+    assert np.isfinite(got).all()
+    assert syn.device_status(True) == syn.OK
+
+
+def test_static_scratch_rejects_oversize_and_bad_shapes(syn):
     n_in = 4096
     n_tok = syn.STATIC_SCRATCH_BYTES // (2 * n_in) + 1
     p = 1 << 20
     assert syn.syn_mul_mat_prefill_static(oracle.Q4_K, p, 128, n_in, p, n_tok, p, None) == syn.ERR_TOO_LARGE
     assert syn.syn_strerror(syn.ERR_TOO_LARGE).decode().startswith("problem larger")
+    # F16 rows are read 8 values at a time: n_in = 12 is rejected before anything is enqueued
+    assert syn.syn_mul_mat_prefill_static(oracle.F16, p, 128, 12, p, 4, p, None) == syn.ERR_SHAPE
