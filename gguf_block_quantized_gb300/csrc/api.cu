@@ -189,6 +189,7 @@ const char* syn_strerror(int status) {
     case SYN_ERR_FORMAT: return "malformed GGUF file";
     case SYN_ERR_IO: return "file could not be opened, mapped or written";
     case SYN_ERR_NOTFOUND: return "no such GGUF key or tensor";
+    case SYN_ERR_BOUNDS: return "a kernel index check failed (SYN_DEBUG build)";
     default: return "unknown status";
     }
 }
@@ -511,7 +512,26 @@ int syn_device_status(int clear) {
     }
     const int rc = syn::static_status(dev, clear, &ws);
     if (rc) return rc;
+#ifdef SYN_DEBUG
+    // the index-check words of the kernel files (a failed check outranks a timeout it caused)
+    int wb = 0;
+    for (int v : {syn::debug_bounds_quant(clear), syn::debug_bounds_gemv(clear), syn::debug_bounds_gemv_f16(clear),
+                  syn::debug_bounds_gemm(clear)}) {
+        if (v < 0) return SYN_ERR_CUDA;
+        wb |= v;
+    }
+    if (wb) return SYN_ERR_BOUNDS;
+#endif
     return (w || ws) ? SYN_ERR_TIMEOUT : SYN_OK;
+}
+
+int syn_debug_bounds_selftest(syn_stream_t stream) {
+#ifdef SYN_DEBUG
+    return syn::launch_bounds_selftest(reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SYN_OK : SYN_ERR_CUDA;
+#else
+    (void)stream;
+    return 1;
+#endif
 }
 
 }  // extern "C"

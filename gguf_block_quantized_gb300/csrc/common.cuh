@@ -23,11 +23,19 @@
 
 // Device-side error codes written into the library's per-device error word.
 #define SYN_DEVERR_TIMEOUT 1
+#define SYN_DEVERR_BOUNDS 2
 
 // Bounded waits: a wait that has not completed after this many clock cycles (about
 // two seconds at the maximum SM clock) gives up, records SYN_DEVERR_TIMEOUT and
 // returns false so that the kernel can wind down instead of hanging.
+#ifndef SYN_WAIT_CYCLES
 #define SYN_WAIT_CYCLES (4000000000ll)
+#endif
+// Bound of a drain: the wait, after a kernel gave up, for copies or tensor-core operations
+// it had already issued (they complete on their own; the bound only keeps the wait finite).
+#ifndef SYN_DRAIN_CYCLES
+#define SYN_DRAIN_CYCLES (4000000000ll)
+#endif
 
 namespace syn {
 
@@ -89,6 +97,35 @@ __device__ __forceinline__ void lds_words_any(const uint8_t* p, uint32_t* out) {
 __device__ __forceinline__ void record_error(int* err, int code) {
     if (err) atomicCAS(err, 0, code);
 }
+
+// ---------------------------------------------------------------------------------------
+// Index checks of the SYN_DEBUG build (the stand-in for a memory checker).  SYN_IN_BOUNDS(c)
+// guards one access or copy: in the debug build it is c, and a false c records
+// SYN_DEVERR_BOUNDS in this translation unit's status word (the library is compiled
+// without relocatable device code, so each kernel file has its own word, read by its
+// SYN_BOUNDS_READER function) and the caller skips the access.  In other builds it is the
+// constant true and compiles away.
+// ---------------------------------------------------------------------------------------
+#ifdef SYN_DEBUG
+static __device__ int g_syn_bounds;
+__device__ __forceinline__ bool in_bounds(bool ok) {
+    if (!ok) atomicCAS(&g_syn_bounds, 0, SYN_DEVERR_BOUNDS);
+    return ok;
+}
+#define SYN_IN_BOUNDS(cond) (::syn::in_bounds(cond))
+// Host function `int name(int clear)`: this file's status word on the current device (and
+// reset it when clear != 0); -1 if it cannot be read.
+#define SYN_BOUNDS_READER(name)                                                               \
+    int name(int clear) {                                                                     \
+        int v = 0;                                                                            \
+        if (cudaMemcpyFromSymbol(&v, ::syn::g_syn_bounds, sizeof(int)) != cudaSuccess) return -1; \
+        const int z = 0;                                                                      \
+        if (clear && cudaMemcpyToSymbol(::syn::g_syn_bounds, &z, sizeof(int)) != cudaSuccess) return -1; \
+        return v;                                                                             \
+    }
+#else
+#define SYN_IN_BOUNDS(cond) (true)
+#endif
 
 // ---------------------------------------------------------------------------------------
 // mbarrier / bulk-copy primitives (PTX ISA: mbarrier, cp.async.bulk)
@@ -159,6 +196,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* er
             record_error(err, SYN_DEVERR_TIMEOUT);
             *abort = 1;
             return false;
+        }
+    }
+}
+
+// Wait for a phase whose copies (or tensor-core commits) were issued by this CTA, ignoring
+// the abort flag: after a kernel gave up, every asynchronous write into its shared memory
+// must have landed before the CTA leaves, or it would land in the next CTA's.  Bounded by
+// SYN_DRAIN_CYCLES (records SYN_DEVERR_TIMEOUT if it ever runs out).  Returns at once on a
+// phase that has completed, as every phase has on the normal path.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, int* err) {
+    if (mbar_try_wait(bar, parity)) return;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > SYN_DRAIN_CYCLES) {
+            record_error(err, SYN_DEVERR_TIMEOUT);
+            return;
         }
     }
 }

@@ -508,13 +508,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     if (!mbar_wait(smem_u32(&a_empty[ka]), ((kc / GEMM_A_STAGES) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
                     if (lane == 0) {
                         const uint32_t af = smem_u32(&a_full[ka]);
-                        mbar_arrive_expect_tx(af, (uint32_t)GEMM_A_BYTES);
-                        tma_load_2d(smem_u32(sA + ka * GEMM_A_BYTES), &wmap, ss * GEMM_SUPER + k4 * GEMM_BK, m * GEMM_BM, af);
+                        const int x = ss * GEMM_SUPER + k4 * GEMM_BK;
+                        // a tile of this unit, its x on a 16-byte boundary (TMA)
+                        const bool in = SYN_IN_BOUNDS(m * GEMM_BM < p.n_out && x < p.n_in && (x * 2) % 16 == 0);
+                        mbar_arrive_expect_tx(af, in ? (uint32_t)GEMM_A_BYTES : 0u);
+                        if (in) tma_load_2d(smem_u32(sA + ka * GEMM_A_BYTES), &wmap, x, m * GEMM_BM, af);
                     }
                     __syncwarp();
                 }
             }
         }
+        // the tiles still in flight (issued, not consumed: only after an abort) land first
+        for (uint32_t i = kc > (uint32_t)GEMM_A_STAGES ? kc - GEMM_A_STAGES : 0u; i < kc; i++)
+            mbar_drain(smem_u32(&a_full[i % GEMM_A_STAGES]), (i / GEMM_A_STAGES) & 1, p.err);
     } else if (warp == 0) {
         // ------------------------------ raw weight producer ------------------------------
         uint32_t rc = 0;
@@ -530,9 +536,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     // row end are filled with zeros (and counted in the transaction bytes)
                     if (lane == 0) {
                         const uint32_t rfull = smem_u32(&raw_full[rs]);
-                        mbar_arrive_expect_tx(rfull, (uint32_t)(GEMM_BM * F::BOX));
                         const int x = (int)((((int64_t)ss * F::SB_BYTES) & ~int64_t(15)) / F::ESIZE);
-                        tma_load_2d(smem_u32(sRaw + rs * RAW_STAGE), &wmap, x, m * GEMM_BM, rfull);
+                        // the slice lies in the box (from its 16-byte boundary), x is aligned,
+                        // the tile starts inside W
+                        const bool in = SYN_IN_BOUNDS(
+                            (int)(((int64_t)ss * F::SB_BYTES) & 15) + F::SB_BYTES <= p.raw_row &&
+                            (x * F::ESIZE) % 16 == 0 && (int64_t)m * GEMM_BM < p.n_out && ss < p.n_super);
+                        mbar_arrive_expect_tx(rfull, in ? (uint32_t)(GEMM_BM * F::BOX) : 0u);
+                        if (in) tma_load_2d(smem_u32(sRaw + rs * RAW_STAGE), &wmap, x, m * GEMM_BM, rfull);
                     }
                     __syncwarp();
                     rc++;
@@ -557,6 +568,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         if (hi > p.total_floor16) hi = p.total_floor16;
                         a0[i] = lo;
                         nbytes[i] = hi > lo ? (uint32_t)(hi - lo) : 0u;
+                        // the window fits the row's space in the stage and lies inside W
+                        if (!SYN_IN_BOUNDS(nbytes[i] <= (uint32_t)p.raw_row && lo >= 0 && hi <= p.total_floor16))
+                            nbytes[i] = 0;
                         my_tx += nbytes[i];
                     }
                 }
@@ -573,7 +587,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     if (end > p.total_floor16) {
                         const int64_t lo = src & ~int64_t(15);
                         for (int64_t k = (lo > p.total_floor16 ? lo : p.total_floor16); k < end; k++)
-                            rbase[r * p.raw_row + (k - lo)] = p.W[k];
+                            if (SYN_IN_BOUNDS(k - lo < p.raw_row && k < p.n_out * p.row_bytes))
+                                rbase[r * p.raw_row + (k - lo)] = p.W[k];
                     }
                 }
                 uint32_t tx = my_tx;
@@ -591,12 +606,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             if (!ok) break;
         }
+        // the slices still in flight (issued, not consumed: only after an abort) land first
+        for (uint32_t i = rc > (uint32_t)RS ? rc - RS : 0u; i < rc; i++)
+            mbar_drain(smem_u32(&raw_full[i % RS]), (i / RS) & 1, p.err);
     } else if (warp == 2) {
         // ------------------------------ activation producer ------------------------------
         // x~ is written by the conversion kernel this launch may overlap with: wait for it
         asm volatile("griddepcontrol.wait;" ::: "memory");
         uint32_t kc = 0;
-        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+#ifdef SYN_TEST_STALL
+        // timeout-test build: no activation tile is ever loaded, so the waits for one run out
+        const int u_first = n_units;
+#else
+        const int u_first = blockIdx.x;
+#endif
+        for (int u = u_first; u < n_units; u += gridDim.x) {
             int m, n, ss0, ss1;
             unit_coords(p, u, m, n, ss0, ss1);
             bool ok = true;
@@ -607,9 +631,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     if (!mbar_wait(smem_u32(&b_empty[ks]), ((kc / GEMM_B_STAGES) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
                     if (lane == 0) {
                         const uint32_t bf = smem_u32(&b_full[ks]);
-                        mbar_arrive_expect_tx(bf, (uint32_t)(p.bn * GEMM_BK * 2));
-                        tma_load_2d(smem_u32(sB + ks * GEMM_B_BYTES), &xmap, ss * GEMM_SUPER + k4 * GEMM_BK,
-                                    n * p.bn, bf);
+                        const int x = ss * GEMM_SUPER + k4 * GEMM_BK;
+                        const bool in = SYN_IN_BOUNDS((int64_t)n * p.bn < p.n_tok && x < p.n_in && (x * 2) % 16 == 0 &&
+                                                      p.bn * GEMM_BK * 2 <= GEMM_B_BYTES);
+                        mbar_arrive_expect_tx(bf, in ? (uint32_t)(p.bn * GEMM_BK * 2) : 0u);
+                        if (in) tma_load_2d(smem_u32(sB + ks * GEMM_B_BYTES), &xmap, x, n * p.bn, bf);
                     }
                     __syncwarp();
                     kc++;
@@ -617,6 +643,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             if (!ok) break;
         }
+        // the tiles still in flight (issued, not consumed: only after an abort) land first
+        for (uint32_t i = kc > (uint32_t)GEMM_B_STAGES ? kc - GEMM_B_STAGES : 0u; i < kc; i++)
+            mbar_drain(smem_u32(&b_full[i % GEMM_B_STAGES]), (i / GEMM_B_STAGES) & 1, p.err);
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         uint32_t kc = 0, ac = 0;
@@ -624,6 +653,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             int m, n, ss0, ss1;
             unit_coords(p, u, m, n, ss0, ss1);
+            // the unit is a tile of the product and a non-empty range of its K steps
+            (void)SYN_IN_BOUNDS(m >= 0 && m < p.n_m && n >= 0 && n < p.n_n && ss0 >= 0 && ss0 < ss1 &&
+                                ss1 <= p.n_super);
             const int a = ac & 1;
             if (!mbar_wait(smem_u32(&acc_empty[a]), ((ac >> 1) & 1) ^ 1, p.err, abort_flag)) break;
             tc_fence_after();
@@ -657,6 +689,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             __syncwarp();
             ac++;
         }
+        // every MMA issued has finished reading shared memory and writing TMEM before the
+        // accumulators are freed (the commit of the last A stage tracks all earlier MMAs;
+        // on the normal path the epilogue has already seen them finish)
+        if (kc > 0)
+            mbar_drain(smem_u32(&a_empty[(kc - 1) % GEMM_A_STAGES]), ((kc - 1) / GEMM_A_STAGES) & 1, p.err);
     } else if (warp < GEMM_EPI_WARP0) {
       if (T != SYN_F16) {  // F16: no dequantization, the weights arrive as fp16
         // ------------------------------ dequantize ------------------------------
@@ -677,18 +714,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const int64_t src = o * p.row_bytes + (int64_t)ss * F::SB_BYTES;
                 const uint8_t* row = sRaw + rs * RAW_STAGE + r * p.raw_row + (int)(src & 15);
                 const int nst = steps_in(ss);
+                // the slice read below lies in this row's space of the stage
+                const bool row_in = SYN_IN_BOUNDS((int)(src & 15) + F::SB_BYTES <= p.raw_row);
                 // this team's steps of the super-step: c0 and c0 + 2 (K-quants: 4 steps each)
                 const int c0 = (int)((team + GEMM_DEQ_TEAMS - kc % GEMM_DEQ_TEAMS) % GEMM_DEQ_TEAMS);
                 Q4Prep p4;
                 Q6Prep p6;
-                if (T == SYN_Q4_K && row_ok) prep_q4_k(row, c0, h, p4);
-                if (T == SYN_Q6_K && row_ok) prep_q6_k(row, c0, h, p6);
+                if (T == SYN_Q4_K && row_ok && row_in) prep_q4_k(row, c0, h, p4);
+                if (T == SYN_Q6_K && row_ok && row_in) prep_q6_k(row, c0, h, p6);
                 for (int k4 = 0; k4 < nst; k4++, kc++) {
                     if (kc % GEMM_DEQ_TEAMS != team) continue;
                     const int ks = kc % GEMM_A_STAGES;
                     uint32_t out[16];
                     const int64_t kglob = (int64_t)ss * GEMM_SUPER + k4 * GEMM_BK + h * 32;
-                    if (row_ok && kglob < p.n_in) {
+                    if (row_ok && row_in && kglob < p.n_in) {
                         if (T == SYN_Q4_K) deq32_q4_k(row, k4, h, p4, k4 >> 1, out);
                         else if (T == SYN_Q6_K) deq32_q6_k(row, k4, h, p6, k4 >> 1, out);
                         else if (T == SYN_Q8_0) deq32_q8_0(row + (2 * k4 + h) * 34, out);
@@ -760,8 +799,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            if (add) tma_reduce_add_2d(&ymap, o0, tt, stage_s);
-                            else tma_store_2d(&ymap, o0, tt, stage_s);
+                            // x of the store on a 16-byte boundary, never negative
+                            if (SYN_IN_BOUNDS(o0 >= 0 && (o0 * 4) % 16 == 0 && tt >= 0)) {
+                                if (add) tma_reduce_add_2d(&ymap, o0, tt, stage_s);
+                                else tma_store_2d(&ymap, o0, tt, stage_s);
+                            }
                             bulk_commit();
                         }
                     }
@@ -769,7 +811,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 32; i++) {
                         const int64_t t = (int64_t)t0 + cb + i;
-                        if (cb + i < p.bn && t < p.n_tok) {
+                        if (cb + i < p.bn && t < p.n_tok && SYN_IN_BOUNDS(t * p.n_out + o < p.n_tok * p.n_out)) {
                             float* dst = p.Y + t * p.n_out + o;
                             if (add) atomicAdd(dst, __uint_as_float(v[i]));
                             else *dst = __uint_as_float(v[i]);
@@ -1024,5 +1066,9 @@ cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, co
     default: return cudaErrorInvalidValue;
     }
 }
+
+#ifdef SYN_DEBUG
+SYN_BOUNDS_READER(debug_bounds_gemm)
+#endif
 
 }  // namespace syn

@@ -104,6 +104,13 @@ struct GemvBatch {
     uint8_t warp_job[GV_MAX_SMS * GV_WARPS];
 };
 
+// Bytes of dynamic shared memory this launch was given.
+__device__ __forceinline__ uint32_t dyn_smem_bytes() {
+    uint32_t v;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(v));
+    return v;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -136,7 +143,8 @@ __device__ __forceinline__ void win_flush(float (&part)[Win<NT>::N][NT], int n, 
         for (int t = 0; t < NT; t++) {
             float v = part[N - 1][t];
             for (int k = 0; k < lgl; k++) v += __shfl_xor_sync(0xffffffffu, v, 1 << (lgl - 1 - k));
-            if ((lane & ((1 << lgl) - 1)) == 0 && row < row_end && t0 + t < n_tok) Y[(t0 + t) * n_out + row] = v;
+            if ((lane & ((1 << lgl) - 1)) == 0 && row < row_end && t0 + t < n_tok && SYN_IN_BOUNDS(row < n_out))
+                Y[(t0 + t) * n_out + row] = v;
             part[N - 1][t] = 0.f;
         }
         return;
@@ -173,7 +181,7 @@ __device__ __forceinline__ void win_flush(float (&part)[Win<NT>::N][NT], int n, 
         if (i < left && writer) {
             const int step = vbase + i - (N - n);
             const int64_t row = row0 + (int64_t)step * rstep + (lane >> lgl);
-            if (step >= 0 && row < row_end) {
+            if (step >= 0 && row < row_end && SYN_IN_BOUNDS(row < n_out)) {
 #pragma unroll
                 for (int t = 0; t < NT; t++)
                     if (t0 + t < n_tok) Y[(t0 + t) * n_out + row] = part[i][t];
@@ -530,6 +538,11 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
     // the activations the CTA converts
     int jw, u0, u1;
     warp_share(b, gw, jw, u0, u1);
+    // this warp's units are units of its matrix (a failed check leaves the warp without work)
+    if (!SYN_IN_BOUNDS(jw >= 0 && jw < b.n_jobs && u0 >= 0 && u0 <= u1 && u1 <= b.job[jw].n_units)) {
+        jw = 0;
+        u1 = u0 = 0;
+    }
     const int ja = b.warp_job[blockIdx.x * GV_WARPS], jb = b.warp_job[blockIdx.x * GV_WARPS + GV_WARPS - 1];
     __syncthreads();
 
@@ -577,21 +590,37 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
         const int64_t src = (row * nb + bcol) * (int64_t)bb;
         const int64_t len = (int64_t)nblk * bb;
         const int64_t a0 = src & ~int64_t(15);
+        // the stage's blocks lie inside W, and with their 16-byte window inside the slot
+        const bool in = SYN_IN_BOUNDS(row >= 0 && nblk > 0 && src + len <= n_out * (int64_t)nb * bb &&
+                                      (int)(src & 15) + len <= GV_SLOT);
         if (lane == 0) {
             fence_proxy_async_smem();
             int64_t a1 = (src + len + 15) & ~int64_t(15);
             if (a1 > total_floor16) a1 = total_floor16;
-            const uint32_t bytes = a1 > a0 ? (uint32_t)(a1 - a0) : 0u;
+            const uint32_t bytes = in && a1 > a0 ? (uint32_t)(a1 - a0) : 0u;
             const uint32_t bar = bar0 + 8 * s;
             mbar_arrive_expect_tx(bar, bytes);
             if (bytes) bulk_g2s(ring_addr + s * GV_SLOT, W + a0, bytes, bar);
         }
-        if (src + len > total_floor16) {  // bytes past the last 16-byte boundary of W
+        if (in && src + len > total_floor16) {  // bytes past the last 16-byte boundary of W
             const int64_t from = total_floor16 > a0 ? total_floor16 : a0;
             for (int64_t k = from + lane; k < src + len; k += 32) ring[s * GV_SLOT + (k - a0)] = W[k];
             __syncwarp();
         }
     };
+
+    // After a wait gave up: the weight stages this warp issued and has not consumed, and
+    // (thread 0, which issued them) the activation copies of the current token group land
+    // before the CTA can leave, so that no bulk copy writes into the next CTA's shared memory.
+    auto drain = [&](uint32_t from, uint32_t to, bool act_pending, uint32_t act_parity) {
+        for (uint32_t k = from; k < to; k++) mbar_drain(bar0 + 8 * (k % GV_NS), (k / GV_NS) & 1, b.err);
+        if (act_pending && threadIdx.x == 0) mbar_drain(act_bar, act_parity, b.err);
+    };
+#ifdef SYN_TEST_STALL
+    constexpr bool act_issued = false;  // timeout-test build: the activation copies never come
+#else
+    constexpr bool act_issued = true;
+#endif
 
     uint32_t seq = 0;  // stage uses of this warp so far
     bool failed = false;
@@ -623,7 +652,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
             // area, then converted by the CTA's warps (units dealt round-robin over matrices
             // ja..jb) into the activation layout
             const int nt = (int)min((int64_t)NT, b.n_tok - t0);
-            if (threadIdx.x == 0) {
+            if (threadIdx.x == 0 && act_issued) {
                 uint32_t tx = 0;
                 for (int j = ja; j <= jb; j++) tx += (uint32_t)(nt * b.job[j].n_in * 4);
                 fence_proxy_async_smem();
@@ -632,11 +661,18 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
                 for (int j = ja; j <= jb; j++) {
                     const GemvJob& J = b.job[j];
                     const uint32_t by = (uint32_t)(nt * J.n_in * 4);
-                    bulk_g2s(smem_u32(smem + b.off_x + xo), J.X + t0 * J.n_in, by, act_bar);
+                    // the staging area holds the rows (a failed check leaves the phase short:
+                    // the wait for it then runs out)
+                    if (SYN_IN_BOUNDS((uint32_t)b.off_x + xo + by <= dyn_smem_bytes()))
+                        bulk_g2s(smem_u32(smem + b.off_x + xo), J.X + t0 * J.n_in, by, act_bar);
                     xo += by;
                 }
             }
-            if (!mbar_wait(act_bar, act_parity, b.err, abort_flag)) break;
+            if (!mbar_wait(act_bar, act_parity, b.err, abort_flag)) {
+                drain(seq, qi, act_issued, act_parity);
+                failed = true;
+                break;
+            }
             uint32_t xo = 0;
             int ubase = 0;
             for (int j = ja; j <= jb; j++) {
@@ -655,7 +691,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
             }
             __syncthreads();
         } else {
-        if (threadIdx.x == 0) {
+        if (threadIdx.x == 0 && act_issued) {
             const int64_t nt = min((int64_t)NT, b.n_tok - t0);
             uint32_t tx = 0;
             for (int j = ja; j <= jb; j++) {
@@ -666,6 +702,12 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
             mbar_arrive_expect_tx(act_bar, tx);
             for (int j = ja; j <= jb; j++) {
                 const GemvJob& J = b.job[j];
+                // the converted activations of NT tokens fit where the layout put them
+                // (a failed check leaves the phase short: the wait for it then runs out)
+                if (!SYN_IN_BOUNDS((uint32_t)J.act_q + (uint32_t)(NT * J.n_in) <= dyn_smem_bytes() &&
+                                   (uint32_t)J.act_d + (uint32_t)(NT * J.ds * 4) <= dyn_smem_bytes() &&
+                                   (uint32_t)J.act_s + (uint32_t)(NT * sum_bytes(J.type, J.n_in)) <= dyn_smem_bytes()))
+                    continue;
                 bulk_g2s(smem_u32(smem + J.act_q), J.actg + t0 * J.n_in, (uint32_t)(nt * J.n_in), act_bar);
                 bulk_g2s(smem_u32(smem + J.act_d), J.actg + J.g_d + t0 * J.ds * 4, (uint32_t)(nt * J.ds * 4), act_bar);
                 if (J.type != SYN_Q8_0)
@@ -673,7 +715,11 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
                              (uint32_t)(nt * sum_bytes(J.type, J.n_in)), act_bar);
             }
         }
-        if (!mbar_wait(act_bar, act_parity, b.err, abort_flag)) break;
+        if (!mbar_wait(act_bar, act_parity, b.err, abort_flag)) {
+            drain(seq, qi, act_issued, act_parity);
+            failed = true;
+            break;
+        }
         }
 
         float acc[NT];
@@ -705,14 +751,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
             }
             const uint32_t s = qc % GV_NS;
             if (!mbar_wait(bar0 + 8 * s, (qc / GV_NS) & 1, b.err, abort_flag)) {
-                // drain this warp's copies still in flight (bounded), so that no bulk copy
-                // targets the shared memory of a finished CTA
-                for (uint32_t k = qc; k < qi; k++) {
-                    const long long w0 = clock64();
-                    while (!mbar_try_wait(bar0 + 8 * (k % GV_NS), (k / GV_NS) & 1) &&
-                           clock64() - w0 < SYN_WAIT_CYCLES / 8) {
-                    }
-                }
+                drain(qc, qi, false, 0);
                 failed = true;
                 break;
             }
@@ -720,6 +759,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
             int nblk, nrows;
             extent(crow, cbcol, nblk, nrows);
             if (nblk <= 0) {  // cannot happen with a valid geometry; never spin without progress
+                drain(qc, qi, false, 0);
                 failed = true;
                 break;
             }
@@ -758,7 +798,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
 #pragma unroll
                         for (int t = 0; t < NT; t++) {
                             const float v = warp_sum(acc[t]);
-                            if (lane == 0 && t0 + t < b.n_tok) {
+                            if (lane == 0 && t0 + t < b.n_tok && SYN_IN_BOUNDS(crow + r < n_out)) {
                                 if (split) atomicAdd(Y + (t0 + t) * n_out + crow + r, v);
                                 else Y[(t0 + t) * n_out + crow + r] = v;
                             }
@@ -1119,5 +1159,9 @@ cudaError_t launch_gemv_batch(int n, const GemvDesc* d, int64_t n_tok, void* ws,
     }
 }
 
+
+#ifdef SYN_DEBUG
+SYN_BOUNDS_READER(debug_bounds_gemv)
+#endif
 
 }  // namespace syn

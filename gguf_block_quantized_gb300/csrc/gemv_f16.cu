@@ -66,7 +66,8 @@ __global__ void __launch_bounds__(F16_WARPS * 32) k_gemv_f16(const __half* __res
                 uint4 wv[F16_UNROLL];
 #pragma unroll
                 for (int u = 0; u < F16_UNROLL; u++)
-                    if (base + 256 * u < n_in) wv[u] = ldg_nc_v4(wr + base + 256 * u);
+                    if (base + 256 * u < n_in && SYN_IN_BOUNDS(base + 256 * u + 8 <= n_in))
+                        wv[u] = ldg_nc_v4(wr + base + 256 * u);
 #pragma unroll
                 for (int u = 0; u < F16_UNROLL; u++) {
                     const int k = base + 256 * u;
@@ -88,7 +89,7 @@ __global__ void __launch_bounds__(F16_WARPS * 32) k_gemv_f16(const __half* __res
                 float v = acc[t];
 #pragma unroll
                 for (int s = 16; s > 0; s >>= 1) v += __shfl_xor_sync(0xffffffffu, v, s);
-                if (lane == 0 && t0 + t < n_tok) Y[(t0 + t) * n_out + o] = v;
+                if (lane == 0 && t0 + t < n_tok && SYN_IN_BOUNDS(o < n_out)) Y[(t0 + t) * n_out + o] = v;
             }
         }
     }
@@ -117,5 +118,9 @@ cudaError_t launch_gemv_f16(const void* W, int64_t n_out, int64_t n_in, const fl
     else k_gemv_f16<8><<<(unsigned)g, F16_WARPS * 32, 0, s>>>(w, n_out, (int)n_in, x, n_tok, Y);
     return cudaGetLastError();
 }
+
+#ifdef SYN_DEBUG
+SYN_BOUNDS_READER(debug_bounds_gemv_f16)
+#endif
 
 }  // namespace syn

@@ -63,4 +63,16 @@ void note_launches(int n);
 // the caller synchronizes the device first.
 int static_status(int dev, int clear, int* word);
 
+#ifdef SYN_DEBUG
+// SYN_DEBUG build: the index-check status word of each kernel file on the current device
+// (SYN_DEVERR_BOUNDS when a check failed; -1 if unreadable), reset when clear != 0, and a
+// launch whose one check is given an out-of-range index on purpose (the access it guards,
+// into a shared array twice the checked size, is skipped).
+int debug_bounds_quant(int clear);
+int debug_bounds_gemv(int clear);
+int debug_bounds_gemv_f16(int clear);
+int debug_bounds_gemm(int clear);
+cudaError_t launch_bounds_selftest(cudaStream_t s);
+#endif
+
 }  // namespace syn

@@ -89,6 +89,7 @@ __global__ void __launch_bounds__(256) k_quantize(const float* __restrict__ src,
         }
     } else {
         for (int64_t b = warp; b < n_blocks; b += n_warps) {
+            if (!SYN_IN_BOUNDS(b >= 0 && b < n_blocks)) break;
             const float* x = src + b * 256 + lane * 8;
             float4 x0 = *reinterpret_cast<const float4*>(x);
             float4 x1 = *reinterpret_cast<const float4*>(x + 4);
@@ -230,6 +231,7 @@ __global__ void __launch_bounds__(256) k_dequantize(const uint8_t* __restrict__ 
         return;
     }
     for (int64_t b = warp; b < n_blocks; b += n_warps) {
+        if (!SYN_IN_BOUNDS(b >= 0 && b < n_blocks)) break;
         float y[8];
         if (T == SYN_Q8_K) {
             const uint8_t* p = src + b * 292;
@@ -391,7 +393,8 @@ __global__ void __launch_bounds__(256) k_act_half(const float* __restrict__ X, i
                                                __fmul_rn(dd, (float)(int8_t)(w >> (sh + 8))));
                 hv[k] = *reinterpret_cast<uint32_t*>(&h2);
             }
-            *reinterpret_cast<uint4*>(xh + b * 256 + lane * 8) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            if (SYN_IN_BOUNDS(b < n_rows_blocks))
+                *reinterpret_cast<uint4*>(xh + b * 256 + lane * 8) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
         }
     }
 }
@@ -591,5 +594,23 @@ cudaError_t launch_block_sums(int type, const void* W, int64_t n_out, int64_t nb
     }
     return cudaGetLastError();
 }
+
+#ifdef SYN_DEBUG
+SYN_BOUNDS_READER(debug_bounds_quant)
+
+// One check given an out-of-range index on purpose: idx = 4 against 4 checked elements.
+// The guarded store is skipped; were the check ever compiled wrong, it would still land in
+// the shared array (8 elements), never outside it.
+__global__ void k_bounds_selftest(int n_checked) {
+    __shared__ int slot[8];
+    const int idx = n_checked;
+    if (SYN_IN_BOUNDS(idx < n_checked)) slot[idx & 7] = 1;
+}
+
+cudaError_t launch_bounds_selftest(cudaStream_t s) {
+    k_bounds_selftest<<<1, 32, 0, s>>>(4);
+    return cudaGetLastError();
+}
+#endif
 
 }  // namespace syn

@@ -20,6 +20,7 @@ OK, ERR_TYPE, ERR_SHAPE, ERR_NULL, ERR_ALIGN, ERR_RANGE, ERR_CUDA, ERR_TIMEOUT, 
     0, -1, -2, -3, -4, -5, -6, -7, -8, -9
 ERR_TOO_LARGE = -10
 ERR_FORMAT, ERR_IO, ERR_NOTFOUND = -11, -12, -13
+ERR_BOUNDS = -14
 # GGUF metadata value types and ggml tensor element types (include/syn.h)
 GGUF_UINT8, GGUF_INT8, GGUF_UINT16, GGUF_INT16, GGUF_UINT32, GGUF_INT32, GGUF_FLOAT32, GGUF_BOOL, \
     GGUF_STRING, GGUF_ARRAY, GGUF_UINT64, GGUF_INT64, GGUF_FLOAT64 = range(13)
@@ -56,6 +57,7 @@ EXPORTS = [
     ("syn_mul_mat_prefill_static", _i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     ("syn_set_deterministic", _i32, [_i32]),
     ("syn_set_sm_limit", _i32, [_i32]),
+    ("syn_debug_bounds_selftest", _i32, [_vp]),
 ]
 
 class MatDesc(ctypes.Structure):
@@ -105,6 +107,21 @@ for _name, _res, _args in EXPORTS:
     _f.restype = _res
     _f.argtypes = _args
     globals()[_name] = _f
+
+
+def bind(path: str):
+    """The entry points of another build of the library (a checking variant made by
+    ``build.build(variant=...)``) as attributes of a namespace, with the argument types above.
+    The helpers below always call libsyn.so."""
+    import types
+    lib = ctypes.CDLL(path)
+    ns = types.SimpleNamespace(path=path)
+    for name, res, args in EXPORTS:
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+        setattr(ns, name, f)
+    return ns
 
 
 class SynError(RuntimeError):

@@ -89,6 +89,8 @@ enum {
     SYN_ERR_FORMAT = -11, /* a GGUF file is malformed or not a GGUF file               */
     SYN_ERR_IO = -12,     /* a file could not be opened, mapped or written             */
     SYN_ERR_NOTFOUND = -13, /* no GGUF key / tensor with that name or index              */
+    SYN_ERR_BOUNDS = -14, /* SYN_DEBUG build only: a kernel found an index or copy window
+                             outside its buffers and skipped that access; results invalid */
 };
 
 /* Elements per block: 32 (Q8_0, Q4_0, Q5_0), 256 (Q4_K, Q6_K, Q8_K) or 1 (F16); -1 for an
@@ -251,9 +253,26 @@ SYN_API int syn_set_sm_limit(int n);
 
 /* Read (and with clear != 0, reset) the device-side error words of the current device:
  * SYN_OK, or SYN_ERR_TIMEOUT if a kernel of any entry point (syn_mul_mat_prefill_static
- * included) gave up a bounded wait since the last clear.  Synchronizes the device.  It
- * allocates nothing: a device on which no product has run reads SYN_OK. */
+ * included) gave up a bounded wait since the last clear.  A kernel that gives up records
+ * the timeout, stops its other threads, waits for the copies and tensor-core operations it
+ * had already issued and returns: the device stays usable, the outputs of that call are
+ * invalid.  In the SYN_DEBUG build (index checks in every kernel) it returns
+ * SYN_ERR_BOUNDS if a check failed.  Synchronizes the device.  It allocates nothing: a
+ * device on which no product has run reads SYN_OK. */
 SYN_API int syn_device_status(int clear);
+
+/* Index checks (not part of the product path).  The SYN_DEBUG build of the library
+ * (`python -m gguf_block_quantized_gb300.build --variant debug`, libsyn_debug.so: same
+ * entry points) checks, before each access, the indices and copy windows its kernels
+ * derive from the launch geometry: weight-stage windows and slot sizes, TMA coordinates
+ * and their 16-byte alignment, shared-memory activation areas, unit and tile coordinates,
+ * output indices.  A failed check records the failure, skips the access, and
+ * syn_device_status returns SYN_ERR_BOUNDS.  This entry point lets a caller see that the
+ * checks are compiled in: it launches one kernel whose check is given an out-of-range
+ * index on purpose (the guarded store, into a shared array, is skipped).  Returns SYN_OK
+ * once launched in the SYN_DEBUG build (syn_device_status then returns SYN_ERR_BOUNDS),
+ * 1 in other builds (nothing launched), SYN_ERR_CUDA if the launch failed. */
+SYN_API int syn_debug_bounds_selftest(syn_stream_t stream);
 
 /* Number of kernels this library has launched in this process (all devices). */
 SYN_API int64_t syn_launch_count(void);

@@ -41,6 +41,18 @@ def test_every_declared_symbol_is_exported(lib):
     assert {n for n, _, _ in lib.EXPORTS} == set(declared())
 
 
+@pytest.mark.parametrize("variant", ["debug", "stall"])
+def test_checking_variants_build_and_export_the_boundary(lib, variant):
+    """The index-check build and the timeout-test build compile here (cross-compiled for
+    sm_103a) and export the same entry points; the product build says it has no checks."""
+    from gguf_block_quantized_gb300 import build
+    path = build.build(variant=variant)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (syn_\w+)", out))
+    assert set(declared()) <= exported
+    assert lib.syn_debug_bounds_selftest(None) == 1
+
+
 def test_host_functions(lib):
     assert [lib.syn_block_elems(t) for t in (1, 2, 3, 4)] == [32, 256, 256, 256]
     assert [lib.syn_block_bytes(t) for t in (1, 2, 3, 4)] == [34, 144, 210, 292]
