@@ -49,6 +49,9 @@ namespace syn {
 #ifndef SYN_GV_STAGE
 #define SYN_GV_STAGE 4608
 #endif
+#ifndef SYN_GV_LATE_UNITS
+#define SYN_GV_LATE_UNITS 80
+#endif
 #ifndef SYN_GV_COST_Q6_K
 #define SYN_GV_COST_Q6_K 130
 #endif
@@ -57,6 +60,9 @@ namespace syn {
 #endif
 constexpr int GV_WARPS = SYN_GV_WARPS;
 constexpr int GV_NS = SYN_GV_NS;            // stages per warp ring
+// Launches whose conversion has at least this many units let the next launch on the stream
+// start only when they end (see late_trigger).
+constexpr int GV_LATE_UNITS = SYN_GV_LATE_UNITS;
 constexpr int GV_STAGE = SYN_GV_STAGE;      // bytes of whole blocks per stage (at most)
 constexpr int GV_SLOT = GV_STAGE + 32;      // stage slot: data plus the alignment window
 constexpr int GV_MAX_SMS = 160;             // grid bound of the per-warp matrix table
@@ -78,6 +84,9 @@ struct GemvJob {
     int lg_nb;              // log2(nb) when rows are packed several per warp step, else -1
     int nbx;                // activation blocks per row
     int units;              // conversion-kernel units (warp steps) per token
+    int act_src;            // the job whose converted activations this one reads: itself, or
+                            // the first job of the launch with the same input (X, n_in and
+                            // activation layout), which converts it once for both
     int warp_begin, warp_end;  // the decode warps of this matrix
     int upr;                // work units per row: 1 (whole rows), or 2 for rows of two stages
                             // runs: the two runs may go to different warps and are then added
@@ -99,9 +108,18 @@ struct GemvBatch {
     int fused;              // 1: each CTA converts its own activations (no conversion launch)
     int off_x;              // fused: shared-memory staging of the CTA's fp32 activation rows
     int off_stage, off_bar, off_flag;
+    int late_trigger;       // 1: the next launch starts only when this one has ended.  A large
+                            // conversion of the next step (a layer like this one) would
+                            // otherwise crowd its CTAs onto the first SMs this launch frees
+                            // and run there compute-bound; started after the end, they spread
+    int n_conv;             // conversion launch: one row of CTAs per listed job (the jobs that
+    uint8_t conv_job[GEMV_MAX_JOBS];  // convert their input, or whose Y must be zeroed)
     // matrix of each decode warp of the grid: one parameter-space load instead of a
     // dependent walk over the job table
     uint8_t warp_job[GV_MAX_SMS * GV_WARPS];
+    // per CTA, bit j: the CTA copies (or converts) job j's activations, i.e. j is the first
+    // of the CTA's jobs to read them
+    uint16_t act_mask[GV_MAX_SMS];
 };
 
 // Bytes of dynamic shared memory this launch was given.
@@ -115,6 +133,14 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// Whether job j is the first of jobs ja..j to read its converted activations (the one that
+// copies or converts them for the CTA); host side, for the per-CTA masks.
+static bool first_reader(const GemvBatch& b, int ja, int j) {
+    for (int i = ja; i < j; i++)
+        if (b.job[i].act_src == b.job[j].act_src) return false;
+    return true;
 }
 
 // Sum over aligned groups of 2^lg lanes (lg <= 5).
@@ -282,12 +308,13 @@ __global__ void __launch_bounds__(128) k_act_decode(const __grid_constant__ Gemv
     const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int GW = (int)((gridDim.x * blockDim.x) >> 5);
     // 32-bit index arithmetic only (64-bit division runs on the slow fp64 pipe)
-    const int j = blockIdx.y;
+    const int j = b.conv_job[blockIdx.y];
     const GemvJob& J = b.job[j];
     if (J.upr > 1) {  // runs of this matrix's rows are added into Y by different warps
         const int ny = (int)b.n_tok * (int)J.n_out;
         for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ny; i += gridDim.x * blockDim.x) J.Y[i] = 0.f;
     }
+    if (J.act_src != j) return;  // its input is converted by the job it shares it with
     const int n_units = (int)b.n_tok * J.units;
     for (int r = gw; r < n_units; r += GW)
     {
@@ -544,6 +571,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
         u1 = u0 = 0;
     }
     const int ja = b.warp_job[blockIdx.x * GV_WARPS], jb = b.warp_job[blockIdx.x * GV_WARPS + GV_WARPS - 1];
+    const uint32_t act_mask = b.act_mask[blockIdx.x];
     __syncthreads();
 
     // the matrix, in registers for the whole launch
@@ -640,8 +668,9 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
         }
         // the next launch on the stream may start now (a following conversion kernel waits
         // for this launch to finish before it touches memory; its own decode launch then
-        // streams weights while this one drains)
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        // streams weights while this one drains), unless this launch's conversion is large
+        // (late_trigger: the next one then starts when this launch ends)
+        if (!b.late_trigger) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         // the converted activations of tokens t0.. of the CTA's matrices: written by the
         // conversion kernel this launch depends on, so wait for it first
         asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -654,11 +683,13 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
             const int nt = (int)min((int64_t)NT, b.n_tok - t0);
             if (threadIdx.x == 0 && act_issued) {
                 uint32_t tx = 0;
-                for (int j = ja; j <= jb; j++) tx += (uint32_t)(nt * b.job[j].n_in * 4);
+                for (int j = ja; j <= jb; j++)
+                    if ((act_mask >> j) & 1) tx += (uint32_t)(nt * b.job[j].n_in * 4);
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(act_bar, tx);
                 uint32_t xo = 0;
                 for (int j = ja; j <= jb; j++) {
+                    if (!((act_mask >> j) & 1)) continue;
                     const GemvJob& J = b.job[j];
                     const uint32_t by = (uint32_t)(nt * J.n_in * 4);
                     // the staging area holds the rows (a failed check leaves the phase short:
@@ -676,6 +707,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
             uint32_t xo = 0;
             int ubase = 0;
             for (int j = ja; j <= jb; j++) {
+                if (!((act_mask >> j) & 1)) continue;
                 const GemvJob& J = b.job[j];
                 const float* xs = reinterpret_cast<const float*>(smem + b.off_x + xo);
                 const int n_u = nt * J.units;
@@ -695,12 +727,14 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
             const int64_t nt = min((int64_t)NT, b.n_tok - t0);
             uint32_t tx = 0;
             for (int j = ja; j <= jb; j++) {
+                if (!((act_mask >> j) & 1)) continue;
                 const GemvJob& J = b.job[j];
                 tx += (uint32_t)(nt * J.n_in + nt * J.ds * 4 + nt * sum_bytes(J.type, J.n_in));
             }
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(act_bar, tx);
             for (int j = ja; j <= jb; j++) {
+                if (!((act_mask >> j) & 1)) continue;
                 const GemvJob& J = b.job[j];
                 // the converted activations of NT tokens fit where the layout put them
                 // (a failed check leaves the phase short: the wait for it then runs out)
@@ -925,7 +959,11 @@ static cudaError_t plan_partition(GemvBatch& b, int sms, int NT, int64_t& x_need
     x_need = 0;
     for (int c = 0; c < sms; c++) {
         int64_t xb = 0, ub = 0;
-        for (int j = b.warp_job[c * GV_WARPS]; j <= b.warp_job[c * GV_WARPS + GV_WARPS - 1]; j++) {
+        const int ja = b.warp_job[c * GV_WARPS];
+        b.act_mask[c] = 0;
+        for (int j = ja; j <= b.warp_job[c * GV_WARPS + GV_WARPS - 1]; j++) {
+            if (!first_reader(b, ja, j)) continue;
+            b.act_mask[c] |= (uint16_t)(1u << j);
             xb += nt * b.job[j].n_in * 4;
             ub += nt * b.job[j].units;
         }
@@ -942,7 +980,7 @@ static cudaError_t plan_partition(GemvBatch& b, int sms, int NT, int64_t& x_need
 struct GemvPlanKey {
     int sms, n_jobs, nt_max, pad;
     int64_t n_tok;
-    int type[GEMV_MAX_JOBS], upr[GEMV_MAX_JOBS];
+    int type[GEMV_MAX_JOBS], upr[GEMV_MAX_JOBS], act_src[GEMV_MAX_JOBS];
     int64_t n_out[GEMV_MAX_JOBS], n_in[GEMV_MAX_JOBS];
 };
 struct GemvPlan {
@@ -952,6 +990,7 @@ struct GemvPlan {
     int64_t x_need;
     int upr[GEMV_MAX_JOBS], n_units[GEMV_MAX_JOBS], warp_begin[GEMV_MAX_JOBS], warp_end[GEMV_MAX_JOBS];
     uint8_t warp_job[GV_MAX_SMS * GV_WARPS];
+    uint16_t act_mask[GV_MAX_SMS];
 };
 
 static cudaError_t plan_cached(GemvBatch& b, int sms, int NT, int64_t& x_need) {
@@ -966,6 +1005,7 @@ static cudaError_t plan_cached(GemvBatch& b, int sms, int NT, int64_t& x_need) {
     for (int j = 0; j < b.n_jobs; j++) {
         k.type[j] = b.job[j].type;
         k.upr[j] = b.job[j].upr;
+        k.act_src[j] = b.job[j].act_src;
         k.n_out[j] = b.job[j].n_out;
         k.n_in[j] = b.job[j].n_in;
     }
@@ -981,6 +1021,7 @@ static cudaError_t plan_cached(GemvBatch& b, int sms, int NT, int64_t& x_need) {
             J.units = small_block(J.type) ? (J.nbx + 3) / 4 : J.nbx;
         }
         memcpy(b.warp_job, P.warp_job, (size_t)GW);
+        memcpy(b.act_mask, P.act_mask, sizeof(P.act_mask));
         b.fused = P.fused;
         x_need = P.x_need;
         return cudaSuccess;
@@ -997,6 +1038,7 @@ static cudaError_t plan_cached(GemvBatch& b, int sms, int NT, int64_t& x_need) {
         P.warp_end[j] = b.job[j].warp_end;
     }
     memcpy(P.warp_job, b.warp_job, (size_t)GW);
+    memcpy(P.act_mask, b.act_mask, sizeof(P.act_mask));
     P.fused = b.fused;
     P.x_need = x_need;
     P.valid = true;
@@ -1009,6 +1051,12 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
     int64_t off = 0;
     for (int j = 0; j < b.n_jobs; j++) {
         GemvJob& J = b.job[j];
+        if (J.act_src != j) {  // the shared input's area
+            J.act_q = b.job[J.act_src].act_q;
+            J.act_d = b.job[J.act_src].act_d;
+            J.act_s = b.job[J.act_src].act_s;
+            continue;
+        }
         J.act_q = (int)off;
         off = up16(off + (int64_t)NT * J.n_in);
         J.act_d = (int)off;
@@ -1050,12 +1098,22 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
             }
         }
     } else {
-    // one row of 4-warp CTAs per matrix, a warp per unit (up to four SMs' worth of CTAs)
-    int64_t max_units = 1;
-    for (int j = 0; j < b.n_jobs; j++) max_units = std::max<int64_t>(max_units, b.n_tok * b.job[j].units);
-    const int64_t act_x = std::min<int64_t>((max_units + 3) / 4, std::max<int64_t>(1, (int64_t)sms * 4 / b.n_jobs));
+    // one row of 4-warp CTAs per matrix that converts its input or needs its Y zeroed, a warp
+    // per unit (up to four SMs' worth of CTAs)
+    int64_t max_units = 1, all_units = 0;
+    b.n_conv = 0;
+    for (int j = 0; j < b.n_jobs; j++) {
+        const GemvJob& J = b.job[j];
+        if (J.act_src == j) {
+            max_units = std::max<int64_t>(max_units, b.n_tok * J.units);
+            all_units += b.n_tok * J.units;
+        }
+        if (J.act_src == j || J.upr > 1) b.conv_job[b.n_conv++] = (uint8_t)j;
+    }
+    b.late_trigger = all_units >= GV_LATE_UNITS ? 1 : 0;
+    const int64_t act_x = std::min<int64_t>((max_units + 3) / 4, std::max<int64_t>(1, (int64_t)sms * 4 / b.n_conv));
     cudaLaunchConfig_t acfg = {};
-    acfg.gridDim = dim3((unsigned)act_x, (unsigned)b.n_jobs);
+    acfg.gridDim = dim3((unsigned)act_x, (unsigned)b.n_conv);
     acfg.blockDim = dim3(128);
     acfg.stream = s;
     acfg.attrs = attr;
@@ -1112,6 +1170,11 @@ static void make_job(GemvJob& J, const GemvDesc& d, int64_t byte_begin) {
 
 int64_t gemv_act_bytes(int type, int64_t n_in) { return act_bytes_per_token(type, n_in) + 64; }
 
+// Activation layouts: Q8_0 codes and scales; the same with block code sums (Q4_0, Q5_0);
+// Q8_K codes, scales and 16-sums (the K-quants).  Products share a converted input only
+// within one layout.
+static int act_kind(int type) { return type == SYN_Q8_0 ? 0 : small_block(type) ? 1 : 2; }
+
 // Global workspace of one matrix's converted activations (all tokens).
 static int64_t act_global_bytes(int type, int64_t n_in, int64_t n_tok) {
     const int64_t nbx = n_in / block_elems(type), ds = (nbx + 3) & ~int64_t(3);
@@ -1140,11 +1203,24 @@ cudaError_t launch_gemv_batch(int n, const GemvDesc* d, int64_t n_tok, void* ws,
             J.upr = 1;
             J.n_units = (int)J.n_out;
         }
+        bytes += d[j].n_out * b.job[j].row_bytes;
+        // products that read the same input in the same activation layout share its conversion
+        J.act_src = j;
+        for (int i = 0; i < j; i++)
+            if (d[i].X == d[j].X && d[i].n_in == d[j].n_in && act_kind(d[i].type) == act_kind(d[j].type)) {
+                J.act_src = i;
+                break;
+            }
+        if (J.act_src != j) {
+            J.actg = b.job[J.act_src].actg;
+            J.g_d = b.job[J.act_src].g_d;
+            J.g_s = b.job[J.act_src].g_s;
+            continue;
+        }
         J.actg = g;
         J.g_d = up16(n_tok * J.n_in);
         J.g_s = J.g_d + up16(n_tok * J.ds * 4);
         g += (act_global_bytes(d[j].type, d[j].n_in, n_tok) + 255) & ~int64_t(255);
-        bytes += d[j].n_out * b.job[j].row_bytes;
         act += gemv_act_bytes(d[j].type, d[j].n_in);
     }
     b.total_bytes = bytes;

@@ -292,15 +292,18 @@ def test_mul_mat_batch_mixed_group(syn, n_tok):
     assert syn.device_status() == syn.OK
 
 
-@pytest.mark.parametrize("n_tok", [6, 300])
+@pytest.mark.parametrize("n_tok", [1, 3, 6, 300])
 def test_mul_mat_batch_shared_inputs(syn, n_tok):
     """A grouped call whose products share activation inputs (q/k/v on one input, gate/up on
-    another, formats with the same vec_dot_type or not): on the prefill path each shared input
-    is converted once; every product matches the oracle, and matches its own syn_mul_mat."""
+    another, formats with the same activation layout or not): each shared input is converted
+    once per layout, on the decode path (one conversion unit feeds several products, and one
+    shared-memory copy serves the CTA's products) and on the prefill path; every product
+    matches the oracle, and matches its own syn_mul_mat."""
     n_in = 1024
     XA, XF = synth.normal(610, (n_tok, n_in)), synth.normal(611, (n_tok, n_in))
     specs = [(oracle.Q4_K, 384, XA), (oracle.Q4_K, 128, XA), (oracle.Q6_K, 128, XA), (oracle.Q8_0, 256, XA),
-             (oracle.F16, 64, XA), (oracle.Q4_K, 640, XF), (oracle.Q4_K, 640, XF), (oracle.Q5_0, 96, XF)]
+             (oracle.F16, 64, XA), (oracle.Q4_K, 640, XF), (oracle.Q4_K, 640, XF), (oracle.Q5_0, 96, XF),
+             (oracle.Q4_0, 64, XF), (oracle.Q8_0, 32, XA)]
     XAd, XFd = dev(XA), dev(XF)
     items, refs, singles = [], [], []
     for i, (wt, n_out, X) in enumerate(specs):
@@ -567,10 +570,12 @@ def test_deterministic_mode_invariants(syn, wt, shape):
             Wo = dev(oracle.quantize(oracle.Q6_K, synth.normal(802, (129, 8192), 0.02)))
             Xo = dev(synth.normal(803, (n_tok, 8192)))
             Yb = torch.full((n_tok, n_out), float("nan"), device="cuda")
+            Yb2 = torch.full((n_tok, n_out), float("nan"), device="cuda")
             Yo = [torch.empty((n_tok, 129), device="cuda") for _ in range(2)]
             syn.mul_mat_batch([(oracle.Q6_K, Wo, 129, 8192, Xo, Yo[0]), (wt, W, n_out, n_in, Xd, Yb),
-                               (oracle.Q6_K, Wo, 129, 8192, Xo, Yo[1])], n_tok)
+                               (oracle.Q6_K, Wo, 129, 8192, Xo, Yo[1]), (wt, W, n_out, n_in, Xd, Yb2)], n_tok)
             outs["batched"] = host(Yb)
+            outs["batched, input shared with another product"] = host(Yb2)
         for what, Y in outs.items():
             assert np.array_equal(Y.view(np.uint32), ref.view(np.uint32)), what
     finally:
