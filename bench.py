@@ -115,10 +115,11 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def recorded_traffic(key: str):
-    """DRAM bytes per launch of a kernel from profiles/traffic.json (one ncu capture), or None
-    when any source the kernel is built from has changed since the counters were taken (the
-    record holds the sha256 of those sources, concatenated in the listed order)."""
+def recorded_traffic(key: str, field: str = "bytes_per_launch"):
+    """DRAM bytes of a kernel from profiles/traffic.json (one ncu capture): per launch, or for
+    the prefill the sum over one layer's launches (field), or None when any source the kernel
+    is built from has changed since the counters were taken (the record holds the sha256 of
+    those sources, concatenated in the listed order)."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
             rec = json.load(fh)[key]
@@ -128,7 +129,7 @@ def recorded_traffic(key: str):
                 h.update(fh.read())
     except (OSError, KeyError, ValueError):
         return None
-    return int(rec["bytes_per_launch"]) if h.hexdigest() == rec["sha256"] else None
+    return int(rec[field]) if h.hexdigest() == rec["sha256"] else None
 
 
 def max_over_ranks(t: float, dist, device: str = "cuda") -> float:
@@ -404,7 +405,12 @@ def gpu_arm(args, rank, world, dist):
                                                               "one layer, mean over the 32 layers",
                                  "achieved": round(p_layer, 1), "peak": tc_peak, "unit": "TFLOP/s",
                                  "frac": round(p_layer / tc_peak, 4), "peak_source": peak_src,
-                                 "traffic": None, "launch_us": round(t_pl / len(layers) * 1e6, 2),
+                                 "traffic": recorded_traffic("k_gemm/llama8b_prefill_layer", "bytes_per_layer"),
+                                 "traffic_note": "dram__bytes_read+write of one layer's seven k_gemm launches (a "
+                                                 "Q6_K-v/down layer at 2048 tokens), from one ncu capture "
+                                                 "(profiles/traffic.json); null when the kernel's sources changed "
+                                                 "since",
+                                 "launch_us": round(t_pl / len(layers) * 1e6, 2),
                                  "lm_head_us": round(t_ph * 1e6, 1),
                                  "note": "fp16 operands; the bf16 measured peak is the denominator (same nominal rate)"}},
         "configs": configs,
