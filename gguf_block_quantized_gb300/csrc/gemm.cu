@@ -34,6 +34,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cmath>
 
 #include "kernels.h"
 #include "quant_dev.cuh"
@@ -151,6 +152,10 @@ struct GemmParams {
     int raw_tma;     // 1: weight slices by one 2-D TMA load per stage (row_bytes % 16 == 0)
     int raw_row;     // bytes per row in a raw stage: BOX (TMA) or RAW_ROW (per-row copies)
     int y_tma;       // 1: Y written by 2-D TMA stores / reduce-adds (n_out % 4 == 0)
+    int streamk_work;  // > 0: stream-K schedule: the tiles x super-steps of the product (this
+                       // many, < 2^31) dealt to the CTAs in equal contiguous ranges, each
+                       // range cut at tile boundaries into units; a unit that is not a whole
+                       // tile adds into Y (zeroed first).  0: the units below, round robin
     uint32_t idesc;
 };
 
@@ -429,6 +434,40 @@ __device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& m, 
     unit_coords(p, u, m, n, ss0, ss1, add);
 }
 
+// The units of this CTA, in order (every role of the CTA walks the same sequence): round
+// robin over the unit list, or the CTA's range of the stream-K work.
+struct UnitIter {
+    int u;      // round robin: the next unit
+    int g, g1;  // stream-K: the next and the end of this CTA's tile x super-step range
+    __device__ explicit UnitIter(const GemmParams& p) {
+        u = blockIdx.x;
+        g = (int)(((int64_t)p.streamk_work * blockIdx.x) / gridDim.x);
+        g1 = (int)(((int64_t)p.streamk_work * (blockIdx.x + 1)) / gridDim.x);
+    }
+    __device__ void stop(const GemmParams& p) {
+        u = p.n_units;
+        g = g1;
+    }
+    __device__ bool next(const GemmParams& p, int& m, int& n, int& ss0, int& ss1, bool& add) {
+        if (p.streamk_work > 0) {
+            if (g >= g1) return false;
+            const int t = g / p.n_super;  // tile: m-major, its token tiles next to each other
+            ss0 = g - t * p.n_super;
+            const int end = min(g1, (t + 1) * p.n_super);
+            ss1 = end - t * p.n_super;
+            m = t / p.n_n;
+            n = t - m * p.n_n;
+            add = !(ss0 == 0 && ss1 == p.n_super);
+            g = end;
+            return true;
+        }
+        if (u >= p.n_units) return false;
+        unit_coords(p, u, m, n, ss0, ss1, add);
+        u += (int)gridDim.x;
+        return true;
+    }
+};
+
 template <int T>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
@@ -484,7 +523,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int n_units = p.n_units;
     // number of 64-k steps in super-step ss
     auto steps_in = [&](int ss) {
         const int64_t rem = p.n_in - (int64_t)ss * GEMM_SUPER;
@@ -498,9 +536,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // n_out / n_in)
         uint32_t kc = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            int m, n, ss0, ss1;
-            unit_coords(p, u, m, n, ss0, ss1);
+        UnitIter it(p);
+        int m, n, ss0, ss1;
+        bool add;
+        while (ok && it.next(p, m, n, ss0, ss1, add)) {
             for (int ss = ss0; ss < ss1 && ok; ss++) {
                 const int nst = steps_in(ss);
                 for (int k4 = 0; k4 < nst; k4++, kc++) {
@@ -524,9 +563,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     } else if (warp == 0) {
         // ------------------------------ raw weight producer ------------------------------
         uint32_t rc = 0;
-        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-            int m, n, ss0, ss1;
-            unit_coords(p, u, m, n, ss0, ss1);
+        UnitIter it(p);
+        int m, n, ss0, ss1;
+        bool add;
+        while (it.next(p, m, n, ss0, ss1, add)) {
             bool ok = true;
             for (int ss = ss0; ss < ss1; ss++) {
                 const int rs = rc % RS;
@@ -614,15 +654,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // x~ is written by the conversion kernel this launch may overlap with: wait for it
         asm volatile("griddepcontrol.wait;" ::: "memory");
         uint32_t kc = 0;
+        UnitIter it(p);
 #ifdef SYN_TEST_STALL
-        // timeout-test build: no activation tile is ever loaded, so the waits for one run out
-        const int u_first = n_units;
-#else
-        const int u_first = blockIdx.x;
+        it.stop(p);  // timeout-test build: no activation tile is ever loaded, so the waits for one run out
 #endif
-        for (int u = u_first; u < n_units; u += gridDim.x) {
-            int m, n, ss0, ss1;
-            unit_coords(p, u, m, n, ss0, ss1);
+        int m, n, ss0, ss1;
+        bool add;
+        while (it.next(p, m, n, ss0, ss1, add)) {
             bool ok = true;
             for (int ss = ss0; ss < ss1 && ok; ss++) {
                 const int nst = steps_in(ss);
@@ -650,9 +688,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // ------------------------------ MMA issuer ------------------------------
         uint32_t kc = 0, ac = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            int m, n, ss0, ss1;
-            unit_coords(p, u, m, n, ss0, ss1);
+        UnitIter it(p);
+        int m, n, ss0, ss1;
+        bool add;
+        while (ok && it.next(p, m, n, ss0, ss1, add)) {
             // the unit is a tile of the product and a non-empty range of its K steps
             (void)SYN_IN_BOUNDS(m >= 0 && m < p.n_m && n >= 0 && n < p.n_n && ss0 >= 0 && ss0 < ss1 &&
                                 ss1 <= p.n_super);
@@ -703,9 +742,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t team = (uint32_t)(dw >> 3);
         uint32_t rc = 0, kc = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            int m, n, ss0, ss1;
-            unit_coords(p, u, m, n, ss0, ss1);
+        UnitIter it(p);
+        int m, n, ss0, ss1;
+        bool add;
+        while (ok && it.next(p, m, n, ss0, ss1, add)) {
             const int64_t o = (int64_t)m * GEMM_BM + r;
             const bool row_ok = o < p.n_out;
             for (int ss = ss0; ss < ss1 && ok; ss++) {
@@ -766,10 +806,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         float* stage = reinterpret_cast<float*>(smem + L::OUT + quarter * (GEMM_OUT_BYTES / 4));
         const uint32_t stage_s = smem_u32(stage);
         uint32_t ac = 0;
-        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-            int m, n, ss0, ss1;
-            bool add;
-            unit_coords(p, u, m, n, ss0, ss1, add);
+        UnitIter it(p);
+        int m, n, ss0, ss1;
+        bool add;
+        while (it.next(p, m, n, ss0, ss1, add)) {
             const int a = ac & 1;
             if (!mbar_wait(smem_u32(&acc_full[a]), (ac >> 1) & 1, p.err, abort_flag)) break;
             tc_fence_after();
@@ -890,7 +930,13 @@ static_assert(gemm_bars_fit<SYN_Q4_K>() && gemm_bars_fit<SYN_Q6_K>() && gemm_bar
 struct SplitPlan {
     int S;       // K split of the split tiles (1: none)
     int m_full;  // m-tiles run whole; the rest are split S ways
+    bool streamk = false;  // instead: the stream-K schedule (every CTA the same number of
+                           // super-steps), where the cost model prefers it
 };
+
+#ifndef SYN_GEMM_STREAMK
+#define SYN_GEMM_STREAMK 1
+#endif
 
 // Pick the schedule of least modelled time, the smaller S on ties: S = 1 (whole tiles), every
 // tile split S ways, or whole tiles for the full waves and only the m-tiles of the last,
@@ -920,6 +966,24 @@ static SplitPlan pick_split(int n_m, int n_n, int n_super, int sms, int bn, int6
                 best = SplitPlan{S, m_full};
             }
             if (m_tail_from == 0) break;  // the two schedules coincide
+        }
+    }
+    // stream-K: every CTA the same number of super-steps (cut into units at tile boundaries),
+    // the whole Y zeroed, and about two partial tiles per CTA added into it.  Measured faster
+    // only where the tiles do not fill one wave and K is long (Q4_K FFN down at 512 tokens:
+    // 74.6 -> 72.5 us); slower for products of short K or several waves (q/k/o at 512 and 2048
+    // tokens +1.7 to +2.5 us, Q6_K FFN down at 2048 tokens +4.4 us).
+    if (SYN_GEMM_STREAMK && tiles < sms && n_super >= 32 && tiles * n_super < (int64_t(1) << 30)) {
+        const double W = (double)tiles * n_super;
+        const double t_ss = tile_us / n_super;
+        const double partial = std::min((double)tiles + sms, 2.0 * sms);
+        const double tile_mb = 4.0 * GEMM_BM * bn / 1e6;
+        const double t = std::ceil(W / sms) * t_ss + ((double)tiles / sms + 1.0) * SYN_GEMM_UNIT_US +
+                         4.0 * (double)n_out * (double)n_tok / 1e6 * SYN_GEMM_ZERO_US_PER_MB +
+                         partial * tile_mb * SYN_GEMM_ADD_US_PER_MB;
+        if (t < best_t * (1.0 - 1e-9)) {
+            best = SplitPlan{1, n_m};
+            best.streamk = true;
         }
     }
     return best;
@@ -952,14 +1016,16 @@ static int gemm_bn(int64_t n_tok) { return (int)std::min<int64_t>(256, (n_tok + 
 
 static SplitPlan plan_of(int64_t n_out, int64_t n_in, int64_t n_tok, int sms) {
     const int bn = gemm_bn(n_tok);
-    return pick_split((int)((n_out + GEMM_BM - 1) / GEMM_BM), (int)((n_tok + bn - 1) / bn),
-                      (int)((n_in + GEMM_SUPER - 1) / GEMM_SUPER), sms, bn, n_out, n_tok);
+    const int n_m = (int)((n_out + GEMM_BM - 1) / GEMM_BM), n_n = (int)((n_tok + bn - 1) / bn);
+    const int n_super = (int)((n_in + GEMM_SUPER - 1) / GEMM_SUPER);
+    return pick_split(n_m, n_n, n_super, sms, bn, n_out, n_tok);
 }
 
 // Zero the columns of Y that the product's split tiles add into (none when it does not
 // split): to be enqueued before the activation conversion (the product kernel overlaps it).
 cudaError_t gemm_zero_y(float* Y, int64_t n_out, int64_t n_in, int64_t n_tok, int sms, cudaStream_t s) {
     const SplitPlan sp = plan_of(n_out, n_in, n_tok, sms);
+    if (sp.streamk) return cudaMemsetAsync(Y, 0, (size_t)n_tok * n_out * sizeof(float), s);
     if (sp.S == 1) return cudaSuccess;
     const int64_t c0 = (int64_t)sp.m_full * GEMM_BM;
     if (c0 == 0) return cudaMemsetAsync(Y, 0, (size_t)n_tok * n_out * sizeof(float), s);
@@ -994,6 +1060,11 @@ cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, co
     p.u_full = p.m_full * p.n_n;
     p.n_units = (int)((int64_t)p.u_full + ((int64_t)p.n_m - p.m_full) * p.n_n * p.n_split);
     p.accumulate = p.n_split > 1 ? 1 : 0;
+    if (sp.streamk) {
+        p.streamk_work = (int)(tiles * p.n_super);
+        p.n_units = p.streamk_work;  // the grid is at most this many CTAs
+        p.accumulate = 1;
+    }
     // kind::f16 instruction descriptor: D fp32, A and B fp16, both K-major, N, M = 128
     p.idesc = (1u << 4) | ((uint32_t)(p.bn >> 3) << 17) | ((uint32_t)(GEMM_BM >> 4) << 24);
 

@@ -321,6 +321,20 @@ def test_mul_mat_batch_shared_inputs(syn, n_tok):
     assert syn.device_status() == syn.OK
 
 
+@pytest.mark.parametrize("wt,n_out,n_in,n_tok", [
+    (oracle.Q4_K, 333, 8192, 70), (oracle.Q6_K, 130, 14336, 33), (oracle.Q8_0, 258, 8192, 20),
+    (oracle.Q4_0, 256, 8192, 48), (oracle.Q5_0, 129, 8192, 17), (oracle.F16, 96, 8192, 50),
+    (oracle.Q4_K, 640, 14336, 300)])
+def test_streamk_prefill(syn, wt, n_out, n_in, n_tok):
+    """Products whose tiles do not fill one wave and whose K is long (>= 32 super-steps) run
+    on the stream-K schedule: every CTA an equal range of tile x K work, partial tiles added
+    into a zeroed Y (by TMA reduce-adds, or element-wise where the Y pitch is not a multiple of
+    16 bytes).  Ragged rows and tokens; every format; against the oracle."""
+    Y, ref, bound = run_mul_mat(syn, wt, n_out, n_in, n_tok, 1300 + n_out, "gemm")
+    assert_close(Y, ref, bound, f"stream-K {oracle.NAMES[wt]} {n_out}x{n_in} n_tok {n_tok}")
+    assert syn.device_status() == syn.OK
+
+
 def test_prepared_batch_matches_grouped_call(syn):
     """The prepared grouped call (descriptors marshalled once) runs the same launches as
     mul_mat_batch: bit-identical outputs, and repeated calls see updated inputs."""
