@@ -232,4 +232,13 @@ __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
     return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
 }
 
+// 4-way byte dot product of unsigned bytes a with signed bytes b: for the high nibbles of
+// packed codes masked in place (16 x code, up to 240), whose sum is then 16 x the code sum,
+// exactly (an arithmetic shift by 4 recovers it).
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 }  // namespace syn

@@ -361,13 +361,13 @@ __device__ __forceinline__ void lane_q4_k(const uint8_t* blk, int h, int B, cons
             const uint4 x3 = *reinterpret_cast<const uint4*>(xq + k_chunk(B, 4 * c + 3));
             const uint32_t xl[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
             const uint32_t xh[8] = {x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
-            int dl = 0, dh = 0;
+            int dl = 0, dh16 = 0;  // dh16: 16 x the high-nibble dot (nibbles masked in place)
 #pragma unroll
             for (int i = 0; i < 8; i++) {
                 dl = dp4a(q[i] & 0x0F0F0F0Fu, xl[i], dl);
-                dh = dp4a((q[i] >> 4) & 0x0F0F0F0Fu, xh[i], dh);
+                dh16 = dp4a_us(q[i] & 0xF0F0F0F0u, xh[i], dh16);
             }
-            At[t] += sl * dl + sh * dh;
+            At[t] += sl * dl + sh * (dh16 >> 4);
         }
     }
     // min term: sum_j m_j * (16-sum 2j + 16-sum 2j+1) of sub-blocks 4h+j, as four 16x8-bit
@@ -471,11 +471,13 @@ __device__ __forceinline__ void lane_qx_0(const uint8_t* blk, int n, int B, cons
         uint32_t w[5];
         if (OFF == 8) lds_words_any<4>(p + 2, w + 1);
         else lds_words_any<5>(p + 2, w);  // w[0] = qh: bit k = fifth bit of code k
-        uint32_t lo[4], hi[4];  // codes 4i..4i+3 and 16+4i..16+4i+3, one per byte
+        // codes 4i..4i+3 and 16+4i..16+4i+3, one per byte (Q4_0: the high nibbles masked in
+        // place, 16 x the code, their dot divided by 16 afterwards, exactly)
+        uint32_t lo[4], hi[4];
 #pragma unroll
         for (int i = 0; i < 4; i++) {
             lo[i] = w[1 + i] & 0x0F0F0F0Fu;
-            hi[i] = (w[1 + i] >> 4) & 0x0F0F0F0Fu;
+            hi[i] = OFF == 8 ? (w[1 + i] & 0xF0F0F0F0u) : ((w[1 + i] >> 4) & 0x0F0F0F0Fu);
             if (OFF == 16) {  // spread 4 bits of qh into bit 4 of 4 bytes
                 lo[i] |= ((((w[0] >> (4 * i)) & 15u) * 0x00204081u) & 0x01010101u) << 4;
                 hi[i] |= ((((w[0] >> (16 + 4 * i)) & 15u) * 0x00204081u) & 0x01010101u) << 4;
@@ -490,10 +492,18 @@ __device__ __forceinline__ void lane_qx_0(const uint8_t* blk, int n, int B, cons
             I = dp4a(lo[1], x0.y, I);
             I = dp4a(lo[2], x0.z, I);
             I = dp4a(lo[3], x0.w, I);
-            I = dp4a(hi[0], x1.x, I);
-            I = dp4a(hi[1], x1.y, I);
-            I = dp4a(hi[2], x1.z, I);
-            I = dp4a(hi[3], x1.w, I);
+            if (OFF == 8) {
+                int H = dp4a_us(hi[0], x1.x, 0);
+                H = dp4a_us(hi[1], x1.y, H);
+                H = dp4a_us(hi[2], x1.z, H);
+                H = dp4a_us(hi[3], x1.w, H);
+                I += H >> 4;
+            } else {
+                I = dp4a(hi[0], x1.x, I);
+                I = dp4a(hi[1], x1.y, I);
+                I = dp4a(hi[2], x1.z, I);
+                I = dp4a(hi[3], x1.w, I);
+            }
             I -= OFF * (int)A.s[t * A.sst + B + e];
             acc[t] = fmaf(Dw * A.d[t * A.ds + B + e], (float)I, acc[t]);
         }
