@@ -50,7 +50,7 @@ namespace syn {
 #define SYN_GV_STAGE 4608
 #endif
 #ifndef SYN_GV_LATE_UNITS
-#define SYN_GV_LATE_UNITS 80
+#define SYN_GV_LATE_UNITS 96
 #endif
 #ifndef SYN_GV_COST_Q6_K
 #define SYN_GV_COST_Q6_K 130
