@@ -23,7 +23,7 @@
 //   2. One thread bulk-copies the converted activations of the CTA's matrices into shared
 //      memory.  When every CTA needs at most one conversion unit per warp (narrow inputs,
 //      few tokens), there is no conversion launch: the CTA bulk-copies its fp32 activation
-//      rows into shared memory and its warps run the encoder there (k_gemv<NT, true>).
+//      rows into shared memory and its warps run the encoder there (k_gemv<NT, true, FAM>).
 //   3. Each lane decodes half a K-quant block or two 32-weight blocks per warp step: unpacks
 //      4/5/6/8-bit codes in registers, forms the integer sub-block dots with dp4a, applies
 //      the integer sub-block scales and then the fp32 block scales.  Rows of at most 32
@@ -48,6 +48,9 @@ namespace syn {
 #endif
 #ifndef SYN_GV_STAGE
 #define SYN_GV_STAGE 4608
+#endif
+#ifndef SYN_GV_FAMILIES
+#define SYN_GV_FAMILIES 1
 #endif
 #ifndef SYN_GV_LATE_UNITS
 #define SYN_GV_LATE_UNITS 96
@@ -514,11 +517,15 @@ __device__ __forceinline__ void lane_qx_0(const uint8_t* blk, int n, int B, cons
 // per lane (block first + lane/2, part lane%2); the 32-weight formats take two blocks per lane.
 // `avail` = blocks of the run from `first` on; the activation block of run block i is
 // (B0 + i) & bmask (bmask = nb - 1 when the run holds several whole rows).
-template <int NT>
+// FAM: the formats the kernel instantiation handles (0: all; 2: the 32-weight formats; 3: Q4_K;
+// 4: Q6_K), so that a launch of one format runs code without the others' lanes (measured:
+// Llama-8B Q4_K layer 23.6 -> 23.0 us, Q6_K lm_head 78.8 -> 77.2 us; launches mixing Q4_K and
+// Q6_K ran slower on a K-quant-only instantiation than on the general one, and keep it).
+template <int NT, int FAM>
 __device__ __forceinline__ void lane_step(int type, const uint8_t* base, int bb, int first, int avail, int B0,
                                           int bmask, const ActView& A, float acc[NT]) {
     const int lane = threadIdx.x & 31;
-    if (small_block(type)) {
+    if (FAM == 2 || (FAM == 0 && small_block(type))) {
         const int k = 2 * lane;
         if (k < avail) {
             const uint8_t* p = base + (first + k) * bb;
@@ -531,7 +538,7 @@ __device__ __forceinline__ void lane_step(int type, const uint8_t* base, int bb,
         const int k = lane >> 1;
         if (k < avail) {
             const int B = (B0 + k) & bmask;
-            if (type == SYN_Q4_K) lane_q4_k<NT>(base + (first + k) * bb, lane & 1, B, A, acc);
+            if (FAM == 3 || (FAM != 4 && type == SYN_Q4_K)) lane_q4_k<NT>(base + (first + k) * bb, lane & 1, B, A, acc);
             else lane_q6_k<NT>(base + (first + k) * bb, lane & 1, B, A, acc);
         }
     }
@@ -552,7 +559,7 @@ __device__ __forceinline__ void warp_share(const GemvBatch& b, int gw, int& j, i
 
 // FUSED: the CTA converts its activations itself (b.fused); a separate instantiation, so that
 // the other path compiles as if it did not exist.
-template <int NT, bool FUSED>
+template <int NT, bool FUSED, int FAM>
 __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant__ GemvBatch b) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -813,7 +820,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
                 // an aligned group of 2^lgl lanes.  Stages hold a multiple of rstep rows, so the
                 // warp's steps cover its rows in order, rstep at a time.
                 for (int s0 = 0; s0 < nblk; s0 += bps) {
-                    lane_step<NT>(type, sbase, bb, s0, nblk - s0, s0, nb - 1, A, acc);
+                    lane_step<NT, FAM>(type, sbase, bb, s0, nblk - s0, s0, nb - 1, A, acc);
 #pragma unroll
                     for (int i = 0; i + 1 < PW; i++)
 #pragma unroll
@@ -837,7 +844,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) k_gemv(const __grid_constant
                 for (int r = 0; r < rows; r++) {
                     const uint8_t* rowp = sbase + (int64_t)r * nb * bb;
                     for (int s0 = 0; s0 < per_row; s0 += bps)
-                        lane_step<NT>(type, rowp, bb, s0, per_row - s0, bstart + s0, -1, A, acc);
+                        lane_step<NT, FAM>(type, rowp, bb, s0, per_row - s0, bstart + s0, -1, A, acc);
                     if (nrows > 0 || split || cbcol + nblk == nb) {
 #pragma unroll
                         for (int t = 0; t < NT; t++) {
@@ -1086,9 +1093,12 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(k_gemv<NT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(k_gemv<NT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        void (*kerns[8])(GemvBatch) = {k_gemv<NT, false, 0>, k_gemv<NT, true, 0>, k_gemv<NT, false, 2>,
+                                       k_gemv<NT, true, 2>,  k_gemv<NT, false, 3>, k_gemv<NT, true, 3>,
+                                       k_gemv<NT, false, 4>, k_gemv<NT, true, 4>};
+        for (auto k : kerns)
+            if (attr_err == cudaSuccess)
+                attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
     if (attr_err != cudaSuccess) return attr_err;
     int64_t x_need = 0;
@@ -1140,7 +1150,24 @@ static cudaError_t run_gemv(GemvBatch& b, int sms, cudaStream_t s) {
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return b.fused ? cudaLaunchKernelEx(&cfg, k_gemv<NT, true>, b) : cudaLaunchKernelEx(&cfg, k_gemv<NT, false>, b);
+    // the instantiation for the launch's formats: all Q4_K, all Q6_K, all 32-weight, or mixed
+    int fam = 0;
+    if (SYN_GV_FAMILIES) {
+        bool all_q4k = true, all_q6k = true, all_small = true;
+        for (int j = 0; j < b.n_jobs; j++) {
+            all_q4k = all_q4k && b.job[j].type == SYN_Q4_K;
+            all_q6k = all_q6k && b.job[j].type == SYN_Q6_K;
+            all_small = all_small && small_block(b.job[j].type);
+        }
+        fam = all_q4k ? 3 : all_q6k ? 4 : all_small ? 2 : 0;
+    }
+    if (fam == 3)
+        return b.fused ? cudaLaunchKernelEx(&cfg, k_gemv<NT, true, 3>, b) : cudaLaunchKernelEx(&cfg, k_gemv<NT, false, 3>, b);
+    if (fam == 4)
+        return b.fused ? cudaLaunchKernelEx(&cfg, k_gemv<NT, true, 4>, b) : cudaLaunchKernelEx(&cfg, k_gemv<NT, false, 4>, b);
+    if (fam == 2)
+        return b.fused ? cudaLaunchKernelEx(&cfg, k_gemv<NT, true, 2>, b) : cudaLaunchKernelEx(&cfg, k_gemv<NT, false, 2>, b);
+    return b.fused ? cudaLaunchKernelEx(&cfg, k_gemv<NT, true, 0>, b) : cudaLaunchKernelEx(&cfg, k_gemv<NT, false, 0>, b);
 }
 
 // One matrix of a launch.  Rows of a power-of-two number of blocks up to 32 are packed
