@@ -354,13 +354,13 @@ __global__ void __launch_bounds__(256) k_act_half(const float* __restrict__ X, i
             const float4 x = xn;
             xn = load(b + n_warps * 4);
             float v[4] = {x.x, x.y, x.z, x.w};
-            uint16_t db;
-            bool fin;
-            uint32_t q = q8_0_group(v, &db, &fin);
+            float q[4];
+            const uint16_t db = q8_0_group_codes(v, q);
             if (b < n_rows_blocks) {
-                float D = h2f_bits(db);
-                __half2 a = __floats2half2_rn(__fmul_rn(D, (float)(int8_t)(q)), __fmul_rn(D, (float)(int8_t)(q >> 8)));
-                __half2 c = __floats2half2_rn(__fmul_rn(D, (float)(int8_t)(q >> 16)), __fmul_rn(D, (float)(int8_t)(q >> 24)));
+                // the codes as floats (a -0 code made +0, the value of the integer code)
+                const float D = h2f_bits(db);
+                __half2 a = __floats2half2_rn(__fmul_rn(D, __fadd_rn(q[0], 0.0f)), __fmul_rn(D, __fadd_rn(q[1], 0.0f)));
+                __half2 c = __floats2half2_rn(__fmul_rn(D, __fadd_rn(q[2], 0.0f)), __fmul_rn(D, __fadd_rn(q[3], 0.0f)));
                 uint2 out = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&c));
                 *reinterpret_cast<uint2*>(xh + b * 32 + e) = out;
             }
@@ -379,18 +379,14 @@ __global__ void __launch_bounds__(256) k_act_half(const float* __restrict__ X, i
                 n1 = *reinterpret_cast<const float4*>(X + bn * 256 + lane * 8 + 4);
             }
             float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            uint32_t w0, w1;
-            float dd;
-            int bs;
-            bool fin;
-            q8_k_warp(v, &w0, &w1, &dd, &bs, &fin);
+            float q[8];
+            const float dd = q8_k_warp_codes(v, q);
             uint32_t hv[4];
 #pragma unroll
             for (int k = 0; k < 4; k++) {
-                uint32_t w = (k < 2) ? w0 : w1;
-                int sh = (k & 1) * 16;
-                __half2 h2 = __floats2half2_rn(__fmul_rn(dd, (float)(int8_t)(w >> sh)),
-                                               __fmul_rn(dd, (float)(int8_t)(w >> (sh + 8))));
+                // the codes as floats (a -0 code made +0, the value of the integer code)
+                __half2 h2 = __floats2half2_rn(__fmul_rn(dd, __fadd_rn(q[2 * k], 0.0f)),
+                                               __fmul_rn(dd, __fadd_rn(q[2 * k + 1], 0.0f)));
                 hv[k] = *reinterpret_cast<uint32_t*>(&h2);
             }
             if (SYN_IN_BOUNDS(b < n_rows_blocks))

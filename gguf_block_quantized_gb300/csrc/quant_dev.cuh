@@ -39,24 +39,54 @@ __device__ __forceinline__ bool all_finite4(const float* v) {
     return isfinite(v[0]) && isfinite(v[1]) && isfinite(v[2]) && isfinite(v[3]);
 }
 
+// roundf(v / d) (IEEE quotient, ties away from zero) for quotients of magnitude below 2^21,
+// given inv = the rounded reciprocal of d.  The product v * inv lies within 3 * 2^-24
+// relative of v / d, so where it is farther than 2^-12 from every half-integer, both round
+// to the same integer, taken here by adding and subtracting 1.5 * 2^23 (integer spacing at
+// that magnitude); the rest (half-integer neighbourhoods, non-finite values, an infinite
+// inv) take the IEEE division.  A NaN quotient gives 0, the integer an IEEE-to-integer
+// conversion of it gives on the device.  Keeps the special-function and conversion pipes
+// free of the per-value division, rounding and conversions.
+__device__ __forceinline__ float round_quot(float v, float d, float inv) {
+    const float r = __fmul_rn(v, inv);
+    const float t = fabsf(r);
+    const float n = __fsub_rn(__fadd_rn(t, 12582912.0f), 12582912.0f);
+    if (!(fabsf(__fsub_rn(t, n)) < 0.5f - 1.0f / 4096.0f)) {
+        const float e = roundf(__fdiv_rn(v, d));
+        return e == e ? e : 0.0f;
+    }
+    return copysignf(n, r);
+}
+
+// The integer value of a float holding an integer of magnitude below 2^22, without a
+// conversion instruction (the low mantissa bits of q + 1.5 * 2^23).
+__device__ __forceinline__ int int_of(float q) {
+    return __float_as_int(__fadd_rn(q, 12582912.0f)) - 0x4B400000;
+}
+
 // ---------------------------------------------------------------------------------------
 // Q8_0: groups of 8 lanes, 4 consecutive values per lane, one 32-block per group.
 // Returns the 4 codes packed in a word and the stored scale (fp16 bits in *dbits).
 // ---------------------------------------------------------------------------------------
+// The codes as floats (exact integers; -0 where the quotient rounds to -0); returns the
+// fp16 scale bits.
+__device__ __forceinline__ uint16_t q8_0_group_codes(const float v[4], float q[4]) {
+    const float a = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    const float amax = group_max<8>(a);
+    const __half hd = __float2half_rn(__fdiv_rn(amax, 127.0f));
+    const float D = __half2float(hd);
+    const float inv = __frcp_rn(D);
+#pragma unroll
+    for (int i = 0; i < 4; i++) q[i] = (D == 0.0f) ? 0.0f : clampf(round_quot(v[i], D, inv), -127.0f, 127.0f);
+    return __half_as_ushort(hd);
+}
+
 __device__ __forceinline__ uint32_t q8_0_group(const float v[4], uint16_t* dbits,
                                                bool* finite) {
-    float a = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-    float amax = group_max<8>(a);
-    float d = __fdiv_rn(amax, 127.0f);
-    __half hd = __float2half_rn(d);
-    float D = __half2float(hd);
-    int q[4];
-#pragma unroll
-    for (int i = 0; i < 4; i++)
-        q[i] = (D == 0.0f) ? 0 : (int)clampf(roundf(__fdiv_rn(v[i], D)), -127.0f, 127.0f);
-    *dbits = __half_as_ushort(hd);
-    *finite = all_finite4(v) && !__hisinf(hd);
-    return pack4_s8(q[0], q[1], q[2], q[3]);
+    float q[4];
+    *dbits = q8_0_group_codes(v, q);
+    *finite = all_finite4(v) && !__hisinf(__ushort_as_half(*dbits));
+    return pack4_s8(int_of(q[0]), int_of(q[1]), int_of(q[2]), int_of(q[3]));
 }
 
 // ---------------------------------------------------------------------------------------
@@ -100,18 +130,28 @@ __device__ __forceinline__ uint32_t qx_0_group(const float v[4], uint16_t* dbits
 // Returns the codes as two words, the fp32 scale, and in *bsum the sum of the 16 codes
 // of sub-block L/2 (valid in every lane).
 // ---------------------------------------------------------------------------------------
-__device__ __forceinline__ void q8_k_warp(const float v[8], uint32_t* w0, uint32_t* w1,
-                                          float* dout, int* bsum, bool* finite) {
+// The codes as floats (exact integers; -0 where the quotient rounds to -0); returns d.
+__device__ __forceinline__ float q8_k_warp_codes(const float v[8], float q[8]) {
     float a = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; i++) a = fmaxf(a, fabsf(v[i]));
-    float amax = group_max<32>(a);
-    float d = __fdiv_rn(amax, 127.0f);
+    const float amax = group_max<32>(a);
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float inv = __frcp_rn(d);
+#pragma unroll
+    for (int i = 0; i < 8; i++) q[i] = (d == 0.0f) ? 0.0f : clampf(round_quot(v[i], d, inv), -127.0f, 127.0f);
+    return d;
+}
+
+__device__ __forceinline__ void q8_k_warp(const float v[8], uint32_t* w0, uint32_t* w1,
+                                          float* dout, int* bsum, bool* finite) {
+    float qf[8];
+    const float d = q8_k_warp_codes(v, qf);
     int q[8];
     int s = 0;
 #pragma unroll
     for (int i = 0; i < 8; i++) {
-        q[i] = (d == 0.0f) ? 0 : (int)clampf(roundf(__fdiv_rn(v[i], d)), -127.0f, 127.0f);
+        q[i] = int_of(qf[i]);
         s += q[i];
     }
     s += __shfl_xor_sync(0xffffffffu, s, 1);

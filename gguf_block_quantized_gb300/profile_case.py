@@ -4,6 +4,7 @@
 
 Cases (synthetic weights ~N(0, 0.02), activations ~N(0, 1)):
   gemv_q6k_lm_head   Q6_K 128256 x 2048, 1 token    (216 MB of weights: larger than L2)
+  gemv_q6k_lm_head_4tok  the same, 4 tokens
   gemv_q4k_wide      Q4_K 32768 x 8192, 1 token     (151 MB)
   gemv_q8_0_wide     Q8_0 16384 x 8192, 1 token     (143 MB)
   gemm_q4k_ffn_up    Q4_K 14336 x 4096, 512 tokens  (prefill, tensor cores)
@@ -21,6 +22,7 @@ import argparse
 
 CASES = {
     "gemv_q6k_lm_head": (3, 128256, 2048, 1),
+    "gemv_q6k_lm_head_4tok": (3, 128256, 2048, 4),
     "gemv_q4k_wide": (2, 32768, 8192, 1),
     "gemv_q8_0_wide": (1, 16384, 8192, 1),
     "gemm_q4k_ffn_up": (2, 14336, 4096, 512),
