@@ -34,6 +34,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 
 #include "kernels.h"
@@ -152,10 +153,12 @@ struct GemmParams {
     int raw_tma;     // 1: weight slices by one 2-D TMA load per stage (row_bytes % 16 == 0)
     int raw_row;     // bytes per row in a raw stage: BOX (TMA) or RAW_ROW (per-row copies)
     int y_tma;       // 1: Y written by 2-D TMA stores / reduce-adds (n_out % 4 == 0)
-    int streamk_work;  // > 0: stream-K schedule: the tiles x super-steps of the product (this
-                       // many, < 2^31) dealt to the CTAs in equal contiguous ranges, each
-                       // range cut at tile boundaries into units; a unit that is not a whole
-                       // tile adds into Y (zeroed first).  0: the units below, round robin
+    int streamk_work;  // > 0: stream-K schedule: tiles [0, sk_tile0) whole, round robin, then
+                       // the tiles x super-steps of tiles [sk_tile0, n_m * n_n) (this many,
+                       // < 2^31) dealt to the CTAs in equal contiguous ranges, each range cut
+                       // at tile boundaries into units; a unit that is not a whole tile adds
+                       // into Y (zeroed first).  0: the units below, round robin
+    int sk_tile0;      // stream-K: the first tile of the shared range (a multiple of n_n)
     uint32_t idesc;
 };
 
@@ -435,21 +438,32 @@ __device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& m, 
 }
 
 // The units of this CTA, in order (every role of the CTA walks the same sequence): round
-// robin over the unit list, or the CTA's range of the stream-K work.
+// robin over the unit list, or (stream-K) round robin over the whole tiles before sk_tile0,
+// then the CTA's range of the shared tile x super-step work.
 struct UnitIter {
-    int u;      // round robin: the next unit
+    int u;      // round robin: the next unit (stream-K: the next whole tile)
     int g, g1;  // stream-K: the next and the end of this CTA's tile x super-step range
     __device__ explicit UnitIter(const GemmParams& p) {
         u = blockIdx.x;
-        g = (int)(((int64_t)p.streamk_work * blockIdx.x) / gridDim.x);
-        g1 = (int)(((int64_t)p.streamk_work * (blockIdx.x + 1)) / gridDim.x);
+        const int g0 = p.sk_tile0 * p.n_super;
+        g = g0 + (int)(((int64_t)p.streamk_work * blockIdx.x) / gridDim.x);
+        g1 = g0 + (int)(((int64_t)p.streamk_work * (blockIdx.x + 1)) / gridDim.x);
     }
     __device__ void stop(const GemmParams& p) {
-        u = p.n_units;
+        u = INT_MAX;
         g = g1;
     }
     __device__ bool next(const GemmParams& p, int& m, int& n, int& ss0, int& ss1, bool& add) {
         if (p.streamk_work > 0) {
+            if (u < p.sk_tile0) {  // a whole tile of the leading full waves
+                m = u / p.n_n;
+                n = u - m * p.n_n;
+                ss0 = 0;
+                ss1 = p.n_super;
+                add = false;
+                u += (int)gridDim.x;
+                return true;
+            }
             if (g >= g1) return false;
             const int t = g / p.n_super;  // tile: m-major, its token tiles next to each other
             ss0 = g - t * p.n_super;
@@ -929,13 +943,17 @@ static_assert(gemm_bars_fit<SYN_Q4_K>() && gemm_bars_fit<SYN_Q6_K>() && gemm_bar
 
 struct SplitPlan {
     int S;       // K split of the split tiles (1: none)
-    int m_full;  // m-tiles run whole; the rest are split S ways
-    bool streamk = false;  // instead: the stream-K schedule (every CTA the same number of
-                           // super-steps), where the cost model prefers it
+    int m_full;  // m-tiles run whole; the rest are split S ways (stream-K: shared)
+    bool streamk = false;  // instead: the stream-K schedule (the whole tiles of m-tiles below
+                           // m_full, then every CTA the same number of super-steps of the
+                           // rest), where the cost model prefers it
 };
 
 #ifndef SYN_GEMM_STREAMK
 #define SYN_GEMM_STREAMK 1
+#endif
+#ifndef SYN_GEMM_SK_TAIL
+#define SYN_GEMM_SK_TAIL 1
 #endif
 
 // Pick the schedule of least modelled time, the smaller S on ties: S = 1 (whole tiles), every
@@ -969,20 +987,31 @@ static SplitPlan pick_split(int n_m, int n_n, int n_super, int sms, int bn, int6
         }
     }
     // stream-K: every CTA the same number of super-steps (cut into units at tile boundaries),
-    // the whole Y zeroed, and about two partial tiles per CTA added into it.  Measured faster
-    // only where the tiles do not fill one wave and K is long (Q4_K FFN down at 512 tokens:
-    // 74.6 -> 72.5 us); slower for products of short K or several waves (q/k/o at 512 and 2048
-    // tokens +1.7 to +2.5 us, Q6_K FFN down at 2048 tokens +4.4 us).
-    if (SYN_GEMM_STREAMK && tiles < sms && n_super >= 32 && tiles * n_super < (int64_t(1) << 30)) {
-        const double W = (double)tiles * n_super;
+    // the Y columns of the shared tiles zeroed, and about two partial tiles per CTA added into
+    // them.  Over all tiles it was measured faster only where the tiles do not fill one wave
+    // and K is long (Q4_K FFN down at 512 tokens: 74.6 -> 72.5 us), slower for products of
+    // short K or several waves (q/k/o at 512 and 2048 tokens +1.7 to +2.5 us, Q6_K FFN down at
+    // 2048 tokens +4.4 us).  Where the tiles fill at least one wave, only the tiles of the last,
+    // partial wave are shared (the full waves run whole tiles, as above): Q4_K FFN down at 2048
+    // tokens 244.8 -> 235.8 us, Q6_K 281.5 -> 279.0; for K of 16 super-steps (q/o at 2048
+    // tokens, the lm_head) it lost to the split tail by ~1 %, so it too needs long K.
+    auto streamk_us = [&](int m_full) {
+        const int64_t dp = (int64_t)m_full * n_n, shared = tiles - dp;
+        const double W = (double)shared * n_super;
         const double t_ss = tile_us / n_super;
-        const double partial = std::min((double)tiles + sms, 2.0 * sms);
+        const double partial = std::min((double)shared + sms, 2.0 * sms);
         const double tile_mb = 4.0 * GEMM_BM * bn / 1e6;
-        const double t = std::ceil(W / sms) * t_ss + ((double)tiles / sms + 1.0) * SYN_GEMM_UNIT_US +
-                         4.0 * (double)n_out * (double)n_tok / 1e6 * SYN_GEMM_ZERO_US_PER_MB +
-                         partial * tile_mb * SYN_GEMM_ADD_US_PER_MB;
-        if (t < best_t * (1.0 - 1e-9)) {
-            best = SplitPlan{1, n_m};
+        return (double)((dp + sms - 1) / sms) * (tile_us + SYN_GEMM_UNIT_US) + std::ceil(W / sms) * t_ss +
+               ((double)shared / sms + 1.0) * SYN_GEMM_UNIT_US + y_mb(m_full) * SYN_GEMM_ZERO_US_PER_MB +
+               partial * tile_mb * SYN_GEMM_ADD_US_PER_MB;
+    };
+    if (SYN_GEMM_STREAMK && tiles * n_super < (int64_t(1) << 30)) {
+        int m_sk = -1;
+        if (tiles < sms && n_super >= 32) m_sk = 0;
+        else if (SYN_GEMM_SK_TAIL && tiles >= sms && n_super >= 32 && m_tail_from > 0 && m_tail_from < n_m)
+            m_sk = m_tail_from;
+        if (m_sk >= 0 && streamk_us(m_sk) < best_t * (1.0 - 1e-9)) {
+            best = SplitPlan{1, m_sk};
             best.streamk = true;
         }
     }
@@ -1025,8 +1054,7 @@ static SplitPlan plan_of(int64_t n_out, int64_t n_in, int64_t n_tok, int sms) {
 // split): to be enqueued before the activation conversion (the product kernel overlaps it).
 cudaError_t gemm_zero_y(float* Y, int64_t n_out, int64_t n_in, int64_t n_tok, int sms, cudaStream_t s) {
     const SplitPlan sp = plan_of(n_out, n_in, n_tok, sms);
-    if (sp.streamk) return cudaMemsetAsync(Y, 0, (size_t)n_tok * n_out * sizeof(float), s);
-    if (sp.S == 1) return cudaSuccess;
+    if (sp.S == 1 && !sp.streamk) return cudaSuccess;
     const int64_t c0 = (int64_t)sp.m_full * GEMM_BM;
     if (c0 == 0) return cudaMemsetAsync(Y, 0, (size_t)n_tok * n_out * sizeof(float), s);
     return cudaMemset2DAsync(Y + c0, (size_t)n_out * sizeof(float), 0, (size_t)(n_out - c0) * sizeof(float),
@@ -1061,8 +1089,9 @@ cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, co
     p.n_units = (int)((int64_t)p.u_full + ((int64_t)p.n_m - p.m_full) * p.n_n * p.n_split);
     p.accumulate = p.n_split > 1 ? 1 : 0;
     if (sp.streamk) {
-        p.streamk_work = (int)(tiles * p.n_super);
-        p.n_units = p.streamk_work;  // the grid is at most this many CTAs
+        p.sk_tile0 = p.m_full * p.n_n;
+        p.streamk_work = (int)((tiles - p.sk_tile0) * p.n_super);
+        p.n_units = p.sk_tile0 + p.streamk_work;  // the grid is at most this many CTAs
         p.accumulate = 1;
     }
     // kind::f16 instruction descriptor: D fp32, A and B fp16, both K-major, N, M = 128

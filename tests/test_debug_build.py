@@ -66,6 +66,7 @@ PRODUCTS = [
     (oracle.Q6_K, 131, 768, 3),    # 630-byte rows
     (oracle.Q4_K, 257, 2048, 1),
     (oracle.Q4_K, 96, 14336, 2),   # rows of 56 blocks, several stages per row
+    (oracle.Q6_K, 203, 2048, 4),   # two rows of 8 blocks per warp step, an odd row count
     (oracle.Q4_0, 129, 544, 1),
     (oracle.Q5_0, 67, 544, 4),
     (oracle.F16, 97, 264, 2),

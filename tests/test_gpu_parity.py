@@ -292,6 +292,29 @@ def test_mul_mat_batch_mixed_group(syn, n_tok):
     assert syn.device_status() == syn.OK
 
 
+@pytest.mark.parametrize("n_tok", [2, 3, 4])
+def test_decode_rows_of_8_blocks(syn, n_tok):
+    """Rows of 8 K-quant blocks (n_in = 2048, two rows per warp step) at 2-4 tokens: single
+    products with an odd row count (a last warp step of one row), a narrow product
+    (activations converted in the decode CTAs), and a grouped call mixing them with 4096-wide
+    rows and Q8_0."""
+    cases = [[(oracle.Q4_K, 1001, 2048)], [(oracle.Q6_K, 2047, 2048)], [(oracle.Q6_K, 37, 2048)],
+             [(oracle.Q4_K, 512, 2048), (oracle.Q6_K, 301, 2048), (oracle.Q4_K, 129, 4096),
+              (oracle.Q8_0, 200, 2048), (oracle.Q6_K, 64, 2048)]]
+    for c, shapes in enumerate(cases):
+        items, refs = [], []
+        for i, (wt, n_out, n_in) in enumerate(shapes):
+            Wq = oracle.quantize(wt, synth.normal(1500 + 10 * c + i, (n_out, n_in), 0.02))
+            X = synth.normal(1600 + 10 * c + i, (n_tok, n_in))
+            Yd = torch.full((n_tok, n_out), float("nan"), device="cuda")
+            items.append((wt, dev(Wq), n_out, n_in, dev(X), Yd))
+            refs.append((oracle.mul_mat(wt, Wq, n_out, n_in, X), tolerance(wt, Wq, n_in, X)))
+        syn.mul_mat_batch(items, n_tok)
+        for (wt, _, n_out, n_in, _, Yd), (ref, bound) in zip(items, refs):
+            assert_close(host(Yd), ref, bound, f"rows of 8 blocks {oracle.NAMES[wt]} {n_out}x{n_in} n_tok {n_tok}")
+    assert syn.device_status() == syn.OK
+
+
 @pytest.mark.parametrize("n_tok", [1, 3, 6, 300])
 def test_mul_mat_batch_shared_inputs(syn, n_tok):
     """A grouped call whose products share activation inputs (q/k/v on one input, gate/up on
@@ -332,6 +355,20 @@ def test_streamk_prefill(syn, wt, n_out, n_in, n_tok):
     16 bytes).  Ragged rows and tokens; every format; against the oracle."""
     Y, ref, bound = run_mul_mat(syn, wt, n_out, n_in, n_tok, 1300 + n_out, "gemm")
     assert_close(Y, ref, bound, f"stream-K {oracle.NAMES[wt]} {n_out}x{n_in} n_tok {n_tok}")
+    assert syn.device_status() == syn.OK
+
+
+@pytest.mark.parametrize("wt,n_out,n_in,n_tok", [(oracle.Q4_K, 1400, 8192, 40), (oracle.Q6_K, 876, 8192, 300)])
+def test_streamk_tail_prefill(syn, wt, n_out, n_in, n_tok):
+    """Products with more tiles than SMs and long K (here on 8 SMs: 11 tiles of one token
+    tile, and 14 tiles of two) run whole tiles for the full waves, then share the tiles of the
+    last wave stream-K (their Y columns zeroed, partial tiles added); against the oracle."""
+    prev = syn.set_sm_limit(8)
+    try:
+        Y, ref, bound = run_mul_mat(syn, wt, n_out, n_in, n_tok, 1350 + n_out, "gemm")
+    finally:
+        syn.set_sm_limit(prev)
+    assert_close(Y, ref, bound, f"stream-K tail {oracle.NAMES[wt]} {n_out}x{n_in} n_tok {n_tok}")
     assert syn.device_status() == syn.OK
 
 
