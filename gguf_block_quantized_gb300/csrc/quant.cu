@@ -357,10 +357,9 @@ __global__ void __launch_bounds__(256) k_act_half(const float* __restrict__ X, i
             float q[4];
             const uint16_t db = q8_0_group_codes(v, q);
             if (b < n_rows_blocks) {
-                // the codes as floats (a -0 code made +0, the value of the integer code)
                 const float D = h2f_bits(db);
-                __half2 a = __floats2half2_rn(__fmul_rn(D, __fadd_rn(q[0], 0.0f)), __fmul_rn(D, __fadd_rn(q[1], 0.0f)));
-                __half2 c = __floats2half2_rn(__fmul_rn(D, __fadd_rn(q[2], 0.0f)), __fmul_rn(D, __fadd_rn(q[3], 0.0f)));
+                __half2 a = __floats2half2_rn(__fmul_rn(D, q[0]), __fmul_rn(D, q[1]));
+                __half2 c = __floats2half2_rn(__fmul_rn(D, q[2]), __fmul_rn(D, q[3]));
                 uint2 out = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&c));
                 *reinterpret_cast<uint2*>(xh + b * 32 + e) = out;
             }
@@ -384,9 +383,7 @@ __global__ void __launch_bounds__(256) k_act_half(const float* __restrict__ X, i
             uint32_t hv[4];
 #pragma unroll
             for (int k = 0; k < 4; k++) {
-                // the codes as floats (a -0 code made +0, the value of the integer code)
-                __half2 h2 = __floats2half2_rn(__fmul_rn(dd, __fadd_rn(q[2 * k], 0.0f)),
-                                               __fmul_rn(dd, __fadd_rn(q[2 * k + 1], 0.0f)));
+                __half2 h2 = __floats2half2_rn(__fmul_rn(dd, q[2 * k]), __fmul_rn(dd, q[2 * k + 1]));
                 hv[k] = *reinterpret_cast<uint32_t*>(&h2);
             }
             if (SYN_IN_BOUNDS(b < n_rows_blocks))

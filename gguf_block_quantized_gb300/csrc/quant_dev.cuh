@@ -39,23 +39,33 @@ __device__ __forceinline__ bool all_finite4(const float* v) {
     return isfinite(v[0]) && isfinite(v[1]) && isfinite(v[2]) && isfinite(v[3]);
 }
 
-// roundf(v / d) (IEEE quotient, ties away from zero) for quotients of magnitude below 2^21,
-// given inv = the rounded reciprocal of d.  The product v * inv lies within 3 * 2^-24
-// relative of v / d, so where it is farther than 2^-12 from every half-integer, both round
-// to the same integer, taken here by adding and subtracting 1.5 * 2^23 (integer spacing at
-// that magnitude); the rest (half-integer neighbourhoods, non-finite values, an infinite
-// inv) take the IEEE division.  A NaN quotient gives 0, the integer an IEEE-to-integer
-// conversion of it gives on the device.  Keeps the special-function and conversion pipes
-// free of the per-value division, rounding and conversions.
-__device__ __forceinline__ float round_quot(float v, float d, float inv) {
-    const float r = __fmul_rn(v, inv);
-    const float t = fabsf(r);
-    const float n = __fsub_rn(__fadd_rn(t, 12582912.0f), 12582912.0f);
-    if (!(fabsf(__fsub_rn(t, n)) < 0.5f - 1.0f / 4096.0f)) {
-        const float e = roundf(__fdiv_rn(v, d));
-        return e == e ? e : 0.0f;
+// Codes q[i] = clamp(roundf(v[i] / d), -127, 127) (IEEE quotient, ties away from zero; a zero
+// code as +0, a NaN quotient as 0, the integer an IEEE-to-integer conversion of it gives on the
+// device), for d > 0 with |v[i] / d| below 2^21.  The product v * (1/d), with the reciprocal
+// rounded once, lies within 3 * 2^-24 (relative) of the IEEE quotient, so where it is farther
+// than 2^-12 from every half-integer both round to the same integer, taken here by adding and
+// subtracting 1.5 * 2^23 (integer spacing at that magnitude).  A lane with any value nearer a
+// half-integer, or non-finite, takes the IEEE division for all of its values.  Keeps the
+// special-function and conversion pipes free of per-value divisions, roundings and conversions.
+// CLAMP: the quotients may exceed 127.5 (the Q8_0 scale is rounded to fp16).
+template <int N, bool CLAMP>
+__device__ __forceinline__ void round_quots(const float* v, float d, float* q) {
+    const float inv = __frcp_rn(d);
+    bool ok = true;
+#pragma unroll
+    for (int i = 0; i < N; i++) {
+        const float r = __fmul_rn(v[i], inv);
+        const float n = __fsub_rn(__fadd_rn(r, 12582912.0f), 12582912.0f);
+        ok = ok && fabsf(__fsub_rn(r, n)) < 0.5f - 1.0f / 4096.0f;
+        q[i] = CLAMP ? clampf(n, -127.0f, 127.0f) : n;
     }
-    return copysignf(n, r);
+    if (!ok) {
+#pragma unroll
+        for (int i = 0; i < N; i++) {
+            const float e = roundf(__fdiv_rn(v[i], d));
+            q[i] = e == e ? __fadd_rn(clampf(e, -127.0f, 127.0f), 0.0f) : 0.0f;
+        }
+    }
 }
 
 // The integer value of a float holding an integer of magnitude below 2^22, without a
@@ -68,16 +78,18 @@ __device__ __forceinline__ int int_of(float q) {
 // Q8_0: groups of 8 lanes, 4 consecutive values per lane, one 32-block per group.
 // Returns the 4 codes packed in a word and the stored scale (fp16 bits in *dbits).
 // ---------------------------------------------------------------------------------------
-// The codes as floats (exact integers; -0 where the quotient rounds to -0); returns the
-// fp16 scale bits.
+// The codes as floats (exact integers, zero as +0); returns the fp16 scale bits.
 __device__ __forceinline__ uint16_t q8_0_group_codes(const float v[4], float q[4]) {
     const float a = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
     const float amax = group_max<8>(a);
     const __half hd = __float2half_rn(__fdiv_rn(amax, 127.0f));
     const float D = __half2float(hd);
-    const float inv = __frcp_rn(D);
+    if (D == 0.0f) {
 #pragma unroll
-    for (int i = 0; i < 4; i++) q[i] = (D == 0.0f) ? 0.0f : clampf(round_quot(v[i], D, inv), -127.0f, 127.0f);
+        for (int i = 0; i < 4; i++) q[i] = 0.0f;
+    } else {
+        round_quots<4, true>(v, D, q);
+    }
     return __half_as_ushort(hd);
 }
 
@@ -130,16 +142,20 @@ __device__ __forceinline__ uint32_t qx_0_group(const float v[4], uint16_t* dbits
 // Returns the codes as two words, the fp32 scale, and in *bsum the sum of the 16 codes
 // of sub-block L/2 (valid in every lane).
 // ---------------------------------------------------------------------------------------
-// The codes as floats (exact integers; -0 where the quotient rounds to -0); returns d.
+// The codes as floats (exact integers, zero as +0); returns d.  |v[i] / d| <= 127 up to
+// rounding: no clamp on the fast path.
 __device__ __forceinline__ float q8_k_warp_codes(const float v[8], float q[8]) {
     float a = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; i++) a = fmaxf(a, fabsf(v[i]));
     const float amax = group_max<32>(a);
     const float d = __fdiv_rn(amax, 127.0f);
-    const float inv = __frcp_rn(d);
+    if (d == 0.0f) {
 #pragma unroll
-    for (int i = 0; i < 8; i++) q[i] = (d == 0.0f) ? 0.0f : clampf(round_quot(v[i], d, inv), -127.0f, 127.0f);
+        for (int i = 0; i < 8; i++) q[i] = 0.0f;
+    } else {
+        round_quots<8, false>(v, d, q);
+    }
     return d;
 }
 
