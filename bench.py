@@ -401,8 +401,10 @@ def gpu_arm(args, rank, world, dist):
                     "flops": p_flops,
                     "api": "per layer syn_mul_mat_batch(q, k, v), syn_mul_mat(o), syn_mul_mat_batch(gate, up), "
                            "syn_mul_mat(down); syn_mul_mat(lm_head)",
-                    "roofline": {"bound": "tensor", "kernel": "k_act_half + k_gemm (tcgen05 kind::f16): the calls of "
-                                                              "one layer, mean over the 32 layers",
+                    "roofline": {"bound": "tensor", "kernel": "k_act_half + k_deq_half (fp16 weight expansion, "
+                                                              "at 2048 tokens all products but the Q4_K FFN down) + "
+                                                              "k_gemm (tcgen05 kind::f16): the calls of one layer, "
+                                                              "mean over the 32 layers",
                                  "achieved": round(p_layer, 1), "peak": tc_peak, "unit": "TFLOP/s",
                                  "frac": round(p_layer / tc_peak, 4), "peak_source": peak_src,
                                  "traffic": recorded_traffic("k_gemm/llama8b_prefill_layer", "bytes_per_layer"),

@@ -7,6 +7,7 @@
 // (yakaai ggml documentation, examples/simple).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdlib>
 #include <map>
@@ -46,6 +47,23 @@ int decode_max_tok(int type) {
     if (type == SYN_TYPE_F16) return 2;
     return 4;
 }
+
+// Prefill calls of at least this many tokens expand Q4_K / Q6_K weights to fp16 once per
+// product (launch_deq_half) and run the fp16 tensor-core product on them: the fused product
+// expands every weight tile again for each 256-token tile, and at 2048 tokens that costs
+// more than one pass over the weights (measured on GB300: FFN up 14336x4096 219.7 us fused,
+// 170.3 us on fp16 weights + ~25 us expansion; at 1024 tokens about even, at 512 the fused
+// product wins).  syn_set_prefill_expand_tok, or SYN_PREFILL_EXPAND_TOK at load time.
+constexpr int kPrefillExpandTok = 1536;
+std::atomic<int> g_expand_tok{[] {
+    const char* e = std::getenv("SYN_PREFILL_EXPAND_TOK");
+    if (e && *e) {
+        char* end = nullptr;
+        long v = std::strtol(e, &end, 10);
+        if (end && *end == 0 && v >= 0 && v < (1 << 30)) return (int)v;
+    }
+    return kPrefillExpandTok;
+}()};
 
 std::atomic<int> g_det{0};       // deterministic mode (syn_set_deterministic)
 std::atomic<int> g_sm_limit{0};  // 0: every SM
@@ -200,6 +218,8 @@ int syn_set_gemv_max_tok(int n) { return g_gemv_max_tok.exchange(n < 0 ? -1 : n)
 
 int syn_set_deterministic(int on) { return g_det.exchange(on ? 1 : 0); }
 
+int syn_set_prefill_expand_tok(int n) { return g_expand_tok.exchange(n < 0 ? kPrefillExpandTok : n); }
+
 int syn_set_sm_limit(int n) {
     if (n < 0) return -1;
     return g_sm_limit.exchange(n);
@@ -295,20 +315,48 @@ namespace {
 
 // The prefill path of products that share one activation input (the same X, n_in and
 // vec_dot_type: q/k/v, or gate/up, of a layer): the Y columns of split tiles zeroed,
-// X converted once into the workspace, then one tensor-core launch per product.
+// X converted once into the workspace, then one tensor-core launch per product.  At
+// g_expand_tok tokens or more, each K-quant product's weights are first expanded to fp16
+// (into the workspace after x~, reused product by product) and the product runs on them.
+// Order: the first expansion, the conversion, the first product, then expansion and product
+// for each further one.  A product kernel starts its weight loads before it waits for the
+// launch it follows, so it must follow the conversion (which writes only x~) or a finished
+// expansion (launch_deq_half does not release its dependents early).
 int prefill_group(const syn_mat_desc* const* g, int m, int64_t n_tok, const DeviceState* st, cudaStream_t s) {
     const int64_t n_in = g[0]->n_in;
     const int xt = vec_dot(g[0]->type);
+    // Q4_K rows longer than 8192 are left fused: the FFN down shape (4096 x 14336) measured
+    // 232.5 us fused against 235.0 expanded at 2048 tokens (Q6_K: 281.6 -> 249.0)
+    auto expand = [&](const syn_mat_desc* d) {
+        return n_tok >= g_expand_tok.load() &&
+               (d->type == SYN_TYPE_Q6_K || (d->type == SYN_TYPE_Q4_K && n_in <= 8192));
+    };
+    const size_t x_bytes = (prefill_ws_bytes(n_in, n_tok) + 255) & ~size_t(255);
+    size_t w_bytes = 0;
+    for (int i = 0; i < m; i++)
+        if (expand(g[i])) w_bytes = std::max(w_bytes, (size_t)(g[i]->n_out * n_in) * 2);
     void* ws;
-    int rc = workspace_for(s, prefill_ws_bytes(n_in, n_tok), &ws);
+    int rc = workspace_for(s, x_bytes + w_bytes, &ws);
     if (rc) return rc;
+    void* wh = static_cast<uint8_t*>(ws) + x_bytes;
     for (int i = 0; i < m; i++)
         if (syn::gemm_zero_y(g[i]->Y, g[i]->n_out, n_in, n_tok, sms_of(st), s) != cudaSuccess) return SYN_ERR_CUDA;
-    if (launch_act_half(xt, g[0]->X, n_tok * (n_in / elems(xt)), ws, sms_of(st), s) != cudaSuccess) return SYN_ERR_CUDA;
-    g_launches++;
     for (int i = 0; i < m; i++) {
-        if (syn::launch_gemm(g[i]->type, g[i]->W, g[i]->n_out, n_in, ws, n_tok, g[i]->Y, st->words, sms_of(st), s) !=
-            cudaSuccess)
+        int type = g[i]->type;
+        const void* W = g[i]->W;
+        if (expand(g[i])) {
+            if (syn::launch_deq_half(type, W, wh, g[i]->n_out * (n_in / elems(type)), sms_of(st), s) != cudaSuccess)
+                return SYN_ERR_CUDA;
+            g_launches++;
+            type = SYN_TYPE_F16;
+            W = wh;
+        }
+        if (i == 0) {
+            if (launch_act_half(xt, g[0]->X, n_tok * (n_in / elems(xt)), ws, sms_of(st), s) != cudaSuccess)
+                return SYN_ERR_CUDA;
+            g_launches++;
+        }
+        if (syn::launch_gemm(type, W, g[i]->n_out, n_in, ws, n_tok, g[i]->Y, st->words, sms_of(st), s) != cudaSuccess)
             return SYN_ERR_CUDA;
         g_launches++;
     }

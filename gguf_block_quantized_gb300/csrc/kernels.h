@@ -13,6 +13,9 @@ cudaError_t launch_quantize_act(int xtype, const float* X, int64_t n_blocks, int
                                 int16_t* bsums, int sms, cudaStream_t s);
 cudaError_t launch_act_half(int xtype, const float* X, int64_t n_blocks, void* xh, int sms,
                             cudaStream_t s);
+// Q4_K / Q6_K weights -> fp16 values (n_blocks blocks, 256 halves each, row-major like W),
+// each the fp32 dequantization rounded once to fp16.
+cudaError_t launch_deq_half(int type, const void* src, void* dst, int64_t n_blocks, int sms, cudaStream_t s);
 cudaError_t launch_block_sums(int type, const void* W, int64_t n_out, int64_t nb, const void* Xq,
                               int64_t n_tok, int32_t* S, cudaStream_t s);
 

@@ -283,6 +283,115 @@ __global__ void __launch_bounds__(256) k_dequantize(const uint8_t* __restrict__ 
 }
 
 // ---------------------------------------------------------------------------------------
+// K-quant weights -> fp16 rows (the prefill's A operand, expanded once per call): each value
+// is the fp32 dequantization above (the same operations, so bit for bit the value
+// syn_dequantize returns) rounded once to fp16.  One warp per 256-value block, 8 values per
+// lane, one 16-byte store per lane; codes turned into floats by placing them in the low
+// mantissa bits of 2^23 and subtracting it (exact), not by conversion instructions.
+// ---------------------------------------------------------------------------------------
+
+__device__ __forceinline__ float code_f(uint32_t bytes, int i) {
+    return __fsub_rn(__int_as_float((int)__byte_perm(bytes, 0x4B000000u, 0x7540u | (uint32_t)i)), 8388608.0f);
+}
+
+// The loads of a lane's share of one block, issued for DEQ_U blocks before any is expanded
+// (the loop is bound by load latency otherwise).
+struct DeqLoad {
+    uint4 a;   // Q4_K: the 16-byte header; Q6_K: x = D bits, y = the sub-block scale byte
+    uint2 q;   // Q4_K: 8 code bytes; Q6_K: 8 low-nibble bytes
+    uint2 h;   // Q6_K: 8 high-bit bytes
+};
+
+template <int T>
+__device__ __forceinline__ DeqLoad deq_load(const uint8_t* __restrict__ src, int64_t b, int lane) {
+    DeqLoad L;
+    if (T == SYN_Q4_K) {
+        const uint8_t* p = src + b * 144;
+        const int j = lane >> 2;
+        L.a = *reinterpret_cast<const uint4*>(p);
+        L.q = *reinterpret_cast<const uint2*>(p + 16 + 32 * (j >> 1) + 8 * (lane & 3));
+        L.h = make_uint2(0, 0);
+    } else {  // Q6_K: 2-byte aligned blocks, 16-bit loads
+        const uint8_t* p = src + b * 210;
+        const int h = lane >> 4, w = (lane * 8) & 127, quarter = w >> 5, l0 = w & 31;
+        const uint8_t* ql = p + 64 * h + l0 + ((quarter & 1) ? 32 : 0);
+        const uint8_t* qh = p + 128 + 32 * h + l0;
+        L.a = make_uint4(ld_u16(p + 208), p[192 + (lane >> 1)], 0, 0);
+        L.q = make_uint2((uint32_t)ld_u16(ql) | ((uint32_t)ld_u16(ql + 2) << 16),
+                         (uint32_t)ld_u16(ql + 4) | ((uint32_t)ld_u16(ql + 6) << 16));
+        L.h = make_uint2((uint32_t)ld_u16(qh) | ((uint32_t)ld_u16(qh + 2) << 16),
+                         (uint32_t)ld_u16(qh + 4) | ((uint32_t)ld_u16(qh + 6) << 16));
+    }
+    return L;
+}
+
+template <int T>
+__device__ __forceinline__ uint4 deq_expand(const DeqLoad& L, int lane) {
+    float y[8];
+    if (T == SYN_Q4_K) {
+        // lane: values 8L .. 8L+7 of sub-block j = L/4 (code chunk j/2, nibble j%2)
+        const float D = h2f_bits(L.a.x & 0xFFFF), Dm = h2f_bits(L.a.x >> 16);
+        const int j = lane >> 2;
+        // 6-bit scale and min of sub-block j from the 12 bytes after d and dmin
+        const uint32_t sc_lo = L.a.y & 0x3F3F3F3Fu, mn_lo = L.a.z & 0x3F3F3F3Fu;
+        const uint32_t sc_hi = (L.a.w & 0x0F0F0F0Fu) | ((L.a.y >> 2) & 0x30303030u);
+        const uint32_t mn_hi = ((L.a.w >> 4) & 0x0F0F0F0Fu) | ((L.a.z >> 2) & 0x30303030u);
+        const uint32_t sel = 0x4440u | (uint32_t)(j & 3);
+        const int sc = (int)__byte_perm(j < 4 ? sc_lo : sc_hi, 0, sel);
+        const int mn = (int)__byte_perm(j < 4 ? mn_lo : mn_hi, 0, sel);
+        const float S = __fmul_rn(D, (float)sc), M = __fmul_rn(Dm, (float)mn);
+        const int sh = (j & 1) * 4;
+        const uint32_t v0 = (L.q.x >> sh) & 0x0F0F0F0Fu, v1 = (L.q.y >> sh) & 0x0F0F0F0Fu;
+        // S * q is exact (S has at most 17 significant bits, q 4): one rounding, as in
+        // the fp32 dequantization's multiply-then-subtract
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            y[i] = __fmaf_rn(S, code_f(v0, i), -M);
+            y[4 + i] = __fmaf_rn(S, code_f(v1, i), -M);
+        }
+    } else {  // Q6_K: lane values 8L .. 8L+7, sub-block L/2
+        const float S = __fmul_rn(h2f_bits((uint16_t)L.a.x), (float)(int8_t)(uint8_t)L.a.y);
+        const int quarter = ((lane * 8) & 127) >> 5;
+        const int ns = quarter >= 2 ? 4 : 0, hs = 2 * quarter;
+        // the 6-bit codes q, one per byte; the value is S * (q - 32)
+        const uint32_t c0 = ((L.q.x >> ns) & 0x0F0F0F0Fu) | (((L.h.x >> hs) & 0x03030303u) << 4);
+        const uint32_t c1 = ((L.q.y >> ns) & 0x0F0F0F0Fu) | (((L.h.y >> hs) & 0x03030303u) << 4);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            y[i] = __fmul_rn(S, __fsub_rn(code_f(c0, i), 32.0f));
+            y[4 + i] = __fmul_rn(S, __fsub_rn(code_f(c1, i), 32.0f));
+        }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        const __half2 h2 = __floats2half2_rn(y[2 * k], y[2 * k + 1]);
+        o[k] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+constexpr int DEQ_U = 4;  // blocks per warp per iteration
+
+template <int T>
+__global__ void __launch_bounds__(256) k_deq_half(const uint8_t* __restrict__ src, __half* __restrict__ dst,
+                                                  int64_t n_blocks) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t b0 = warp * DEQ_U; b0 < n_blocks; b0 += n_warps * DEQ_U) {
+        DeqLoad L[DEQ_U];
+#pragma unroll
+        for (int u = 0; u < DEQ_U; u++)
+            if (b0 + u < n_blocks) L[u] = deq_load<T>(src, b0 + u, lane);
+#pragma unroll
+        for (int u = 0; u < DEQ_U; u++)
+            if (b0 + u < n_blocks && SYN_IN_BOUNDS(b0 + u >= 0))
+                *reinterpret_cast<uint4*>(dst + (b0 + u) * 256 + lane * 8) = deq_expand<T>(L[u], lane);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
 // activations -> vec_dot_type, structure-of-arrays (codes, scales, 16-sums)
 // ---------------------------------------------------------------------------------------
 
@@ -530,6 +639,18 @@ cudaError_t launch_dequantize(int type, const void* src, float* dst, int64_t n_b
     case SYN_Q8_K: k_dequantize<SYN_Q8_K><<<g, 256, 0, s>>>(p, dst, n_blocks); break;
     case SYN_Q4_0: k_dequantize<SYN_Q4_0><<<g, 256, 0, s>>>(p, dst, n_blocks); break;
     case SYN_Q5_0: k_dequantize<SYN_Q5_0><<<g, 256, 0, s>>>(p, dst, n_blocks); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_deq_half(int type, const void* src, void* dst, int64_t n_blocks, int sms, cudaStream_t s) {
+    const int g = grid_for((n_blocks + DEQ_U - 1) / DEQ_U, sms);
+    const uint8_t* p = static_cast<const uint8_t*>(src);
+    __half* h = static_cast<__half*>(dst);
+    switch (type) {
+    case SYN_Q4_K: k_deq_half<SYN_Q4_K><<<g, 256, 0, s>>>(p, h, n_blocks); break;
+    case SYN_Q6_K: k_deq_half<SYN_Q6_K><<<g, 256, 0, s>>>(p, h, n_blocks); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

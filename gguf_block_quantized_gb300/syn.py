@@ -57,6 +57,7 @@ EXPORTS = [
     ("syn_mul_mat_prefill_static", _i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     ("syn_set_deterministic", _i32, [_i32]),
     ("syn_set_sm_limit", _i32, [_i32]),
+    ("syn_set_prefill_expand_tok", _i32, [_i32]),
     ("syn_debug_bounds_selftest", _i32, [_vp]),
 ]
 
@@ -270,6 +271,12 @@ def set_gemv_max_tok(n: int) -> int:
 def set_deterministic(on: bool) -> bool:
     """Deterministic mode on/off; returns the previous setting."""
     return bool(syn_set_deterministic(1 if on else 0))
+
+
+def set_prefill_expand_tok(n: int) -> int:
+    """Prefill calls of at least n tokens expand K-quant weights to fp16 first (n < 0: the
+    default); returns the previous value."""
+    return int(syn_set_prefill_expand_tok(n))
 
 
 def set_sm_limit(n: int) -> int:

@@ -246,6 +246,18 @@ SYN_API int syn_set_gemv_max_tok(int n);
  * syn_mul_mat_prefill_static is not affected (it always runs the tensor-core prefill). */
 SYN_API int syn_set_deterministic(int on);
 
+/* Prefill calls (the tensor-core path) of at least n tokens first expand Q6_K weights, and
+ * Q4_K weights of rows up to 8192 values, to fp16, once per product, into the library's
+ * workspace (n_out * n_in * 2 more bytes, grown on first need like the activation
+ * workspace), then run the tensor-core product on the fp16 weights; otherwise the product
+ * expands each weight tile inside the product kernel, once per tile of up to 256 tokens.  Each expanded value is the fp32 dequantization
+ * (syn_dequantize's, bit for bit) rounded once to fp16; the result stays within the
+ * tolerance of syn_mul_mat either way.  n < 0 restores the default (1536); 0 expands at
+ * every prefill call.  Process-wide; returns the previous value; the environment variable
+ * SYN_PREFILL_EXPAND_TOK, when set at load time, gives the initial value.
+ * syn_mul_mat_prefill_static never expands (it allocates nothing). */
+SYN_API int syn_set_prefill_expand_tok(int n);
+
 /* At most n SMs for the library's launches (n >= 1; 0 = all of them, the default).
  * Process-wide; returns the previous value, or -1 (and changes nothing) for n < 0.  Lets a
  * caller leave SMs to concurrent work; the grid of every kernel is sized to the limit. */

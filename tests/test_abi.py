@@ -68,6 +68,10 @@ def test_host_functions(lib):
     assert lib.syn_set_deterministic(7) == 0 and lib.syn_set_deterministic(0) == 1
     assert lib.syn_set_sm_limit(-1) == -1
     assert lib.syn_set_sm_limit(5) == 0 and lib.syn_set_sm_limit(0) == 5
+    old = lib.syn_set_prefill_expand_tok(0)
+    if not os.environ.get("SYN_PREFILL_EXPAND_TOK"):
+        assert old == 1536
+    assert lib.syn_set_prefill_expand_tok(-3) == 0 and lib.syn_set_prefill_expand_tok(old) == 1536
 
 
 def test_argument_checks_need_no_gpu(lib):

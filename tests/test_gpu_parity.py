@@ -372,6 +372,46 @@ def test_streamk_tail_prefill(syn, wt, n_out, n_in, n_tok):
     assert syn.device_status() == syn.OK
 
 
+@pytest.mark.parametrize("wt,n_out,n_in,n_tok", [(oracle.Q4_K, 300, 1024, 40), (oracle.Q6_K, 131, 768, 60),
+                                                 (oracle.Q4_K, 257, 4096, 300), (oracle.Q6_K, 129, 512, 1600)])
+def test_prefill_expanded_weights(syn, wt, n_out, n_in, n_tok):
+    """Prefill with the K-quant weights expanded to fp16 first (forced at every token count
+    here; by default from 1536 tokens), then the fp16 tensor-core product; the last case runs
+    at the default threshold.  Ragged rows and token tiles; against the oracle."""
+    prev = syn.set_prefill_expand_tok(0 if n_tok < 1536 else -1)
+    try:
+        Y, ref, bound = run_mul_mat(syn, wt, n_out, n_in, n_tok, 1400 + n_out, "gemm")
+    finally:
+        syn.set_prefill_expand_tok(prev)
+    assert_close(Y, ref, bound, f"expanded {oracle.NAMES[wt]} {n_out}x{n_in} n_tok {n_tok}")
+    assert syn.device_status() == syn.OK
+
+
+def test_prefill_expanded_weights_grouped(syn):
+    """A grouped prefill call with expanded weights: q/k/v-like products on one input (one
+    conversion, the fp16 weight buffer reused product by product), a Q8_0 product (not
+    expanded) in the same group, and a split-tail product (on 8 SMs); against the oracle."""
+    n_tok, n_in = 96, 2048
+    shapes = [(oracle.Q4_K, 512), (oracle.Q6_K, 129), (oracle.Q8_0, 200), (oracle.Q4_K, 1100)]
+    X = synth.normal(1450, (n_tok, n_in))
+    Xd = dev(X)
+    items, refs = [], []
+    for i, (wt, n_out) in enumerate(shapes):
+        Wq = oracle.quantize(wt, synth.normal(1460 + i, (n_out, n_in), 0.02))
+        Yd = torch.full((n_tok, n_out), float("nan"), device="cuda")
+        items.append((wt, dev(Wq), n_out, n_in, Xd, Yd))
+        refs.append((oracle.mul_mat(wt, Wq, n_out, n_in, X), tolerance(wt, Wq, n_in, X)))
+    prev, lim = syn.set_prefill_expand_tok(0), syn.set_sm_limit(8)
+    try:
+        syn.mul_mat_batch(items, n_tok)
+    finally:
+        syn.set_prefill_expand_tok(prev)
+        syn.set_sm_limit(lim)
+    for (wt, _, n_out, _, _, Yd), (ref, bound) in zip(items, refs):
+        assert_close(host(Yd), ref, bound, f"expanded group {oracle.NAMES[wt]} {n_out}")
+    assert syn.device_status() == syn.OK
+
+
 def test_prepared_batch_matches_grouped_call(syn):
     """The prepared grouped call (descriptors marshalled once) runs the same launches as
     mul_mat_batch: bit-identical outputs, and repeated calls see updated inputs."""
