@@ -153,7 +153,10 @@ SYN_API int syn_quantize_activations(int wtype, const float* X, int64_t n_tok, i
  * inside the decode CTAs) and W is streamed once per group of up to 8 tokens.  Larger
  * n_tok runs the prefill path: one kernel converts X and writes the dequantized fp16
  * activations into the library workspace, a second runs the tensor-core GEMM on W tiles
- * dequantized to fp16 in shared memory (fp32 accumulation).
+ * dequantized to fp16 in shared memory (fp32 accumulation); from 1536 tokens (see
+ * syn_set_prefill_expand_tok) Q6_K weights, and Q4_K weights of rows up to 8192 values,
+ * are instead expanded to fp16 into the workspace by a launch of their own and the GEMM
+ * reads them from there.
  * Accuracy: |y - y_ref| <= 1e-4 * ||dequant(w_row)||_2 * ||x||_2 per element, where
  * y_ref is the same product evaluated in fp64.  W, X, Y: 16-byte aligned, not aliased.
  * n_tok == 0 is a no-op.  Asynchronous.  The prefill path may grow the workspace (see
@@ -203,8 +206,10 @@ SYN_API int syn_mul_mat_batch_staged(int n, const syn_mat_desc* descs, int64_t n
                                      size_t y_bytes, syn_stream_t stream);
 
 /* Pre-size the prefill workspace of (current device, stream) for products with up to
- * max_n_in inputs and max_n_tok tokens, so that later syn_mul_mat calls allocate
- * nothing.  Synchronizes the device when it (re)allocates. */
+ * max_n_in inputs and max_n_tok tokens, so that later syn_mul_mat calls allocate nothing.
+ * Prefill calls that expand their weights to fp16 (syn_set_prefill_expand_tok) need
+ * n_out * n_in * 2 bytes more, which their first call allocates.  Synchronizes the device
+ * when it (re)allocates. */
 SYN_API int syn_reserve(int64_t max_n_in, int64_t max_n_tok, syn_stream_t stream);
 
 /* Free every workspace the library holds on the current device (synchronizes it). */
