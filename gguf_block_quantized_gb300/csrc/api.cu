@@ -54,7 +54,10 @@ int decode_max_tok(int type) {
 // more than one pass over the weights (measured on GB300: FFN up 14336x4096 219.7 us fused,
 // 170.3 us on fp16 weights + ~25 us expansion; at 1024 tokens about even, at 512 the fused
 // product wins).  syn_set_prefill_expand_tok, or SYN_PREFILL_EXPAND_TOK at load time.
-constexpr int kPrefillExpandTok = 1536;
+#ifndef SYN_PREFILL_EXPAND_TOK_DEFAULT
+#define SYN_PREFILL_EXPAND_TOK_DEFAULT 1536
+#endif
+constexpr int kPrefillExpandTok = SYN_PREFILL_EXPAND_TOK_DEFAULT;
 std::atomic<int> g_expand_tok{[] {
     const char* e = std::getenv("SYN_PREFILL_EXPAND_TOK");
     if (e && *e) {

@@ -14,19 +14,21 @@
 // One persistent CTA per SM, warp-specialised, one 128 x BN output tile per work unit
 // (BN <= 256 tokens).  Tiles that do not fill the SMs in whole waves are split along K (all
 // of them, or only those of the last, partial wave; a cost model picks): the units of a
-// split tile add their partial sums into a Y zeroed beforehand.  Warp roles:
-//   warp 0      raw-weight producer: 128 rows x 256 k of weight blocks per raw stage, by
+// split tile add their partial sums into a Y zeroed beforehand.  Warp roles (mapped to
+// warps by kGemmRoles in the dequantizing kernels, so as to keep the MMA issuer's
+// sub-partition clear of dequantizers):
+//   role 0      raw-weight producer: 128 rows x 256 k of weight blocks per raw stage, by
 //               one 2-D TMA load when the row pitch is a multiple of 16 bytes (else one
 //               1-D bulk copy per row);
-//   warp 1      allocates 512 TMEM columns (two fp32 accumulators of 128 x 256) and issues
+//   role 1      allocates 512 TMEM columns (two fp32 accumulators of 128 x 256) and issues
 //               tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16) from one thread;
-//   warp 2      activation producer: 2-D TMA loads of x~ tiles (BN x 64, 128-byte swizzle)
+//   role 2      activation producer: 2-D TMA loads of x~ tiles (BN x 64, 128-byte swizzle)
 //               into a 3-deep operand ring (it alone waits for the conversion kernel);
-//   warps 3-18  dequantize, two teams of 8 taking alternate 64-k steps: raw blocks -> fp16
+//   roles 3-18  dequantize, two teams of 8 taking alternate 64-k steps: raw blocks -> fp16
 //               A tile (128 x 64) in the canonical K-major 128-byte-swizzled layout the MMA
-//               descriptor reads, in half2 arithmetic (F16 weights: no dequantization, warp 0
+//               descriptor reads, in half2 arithmetic (F16 weights: no dequantization, role 0
 //               loads the fp16 tile by TMA straight into that layout);
-//   warps 19-22 epilogue: tcgen05.ld 32x32b from TMEM, then per warp a 32 x 16 staging box
+//   roles 19-22 epilogue: tcgen05.ld 32x32b from TMEM, then per warp a 32 x 16 staging box
 //               and one 2-D TMA store (or reduce-add, when split along K) to Y.
 // All hand-offs are mbarriers; every wait is bounded (clock64) and gives up with a
 // recorded error instead of hanging.  Index arithmetic is 32-bit: 64-bit division runs on
@@ -52,8 +54,24 @@ constexpr int GEMM_SUPER = 256;       // k per raw weight stage
 #endif
 constexpr int GEMM_DEQ_TEAMS = SYN_GEMM_DEQ_TEAMS;
 constexpr int GEMM_DEQ_WARP0 = 3, GEMM_DEQ_WARPS = 8 * GEMM_DEQ_TEAMS, GEMM_EPI_WARP0 = 3 + GEMM_DEQ_WARPS;
-constexpr int GEMM_WARPS = GEMM_EPI_WARP0 + 4;
-constexpr int GEMM_THREADS = GEMM_WARPS * 32;
+// Warp roles, numbered: 0 raw-weight producer, 1 MMA issuer (and TMEM owner), 2 activation
+// producer, 3 .. 3 + GEMM_DEQ_WARPS - 1 dequantizers, then the 4 epilogue warps.  A warp runs
+// on sub-partition (warp index % 4), and an epilogue warp reads only the TMEM lanes of its own
+// sub-partition, so the four epilogue warps sit on four different ones.  Dequantizing
+// kernels run 24 warps laid out by kGemmRoles so that the MMA warp's sub-partition holds one
+// dequantizer instead of four: they otherwise take most of its issue slots and the MMAs go
+// out late (measured, Q4_K: FFN up at 512 tokens 64.7 -> 58.8 us, FFN down at 2048 tokens
+// 235.6 -> 210.1 us).  The fp16-weight kernel (no dequantizers) keeps 23 warps in role order
+// (the table's layout measured 4-8 % slower for it).
+constexpr int GEMM_ROLE_IDLE = 31;
+static_assert(GEMM_DEQ_WARPS == 16, "the role table is laid out for two teams of 8 dequantizers");
+__constant__ uint8_t kGemmRoles[24] = {GEMM_EPI_WARP0, 1, GEMM_EPI_WARP0 + 1, GEMM_EPI_WARP0 + 2, 3, 0, 4, 5, 6, 2,
+                                       7, 8, 9, GEMM_EPI_WARP0 + 3, 10, 11, 12, 13, 14, 15, 16, GEMM_ROLE_IDLE, 17,
+                                       18};
+template <int T>
+constexpr int gemm_warps() {
+    return T == SYN_F16 ? GEMM_EPI_WARP0 + 4 : 24;
+}
 constexpr int GEMM_A_BYTES = GEMM_BM * GEMM_BK * 2;   // 16 KB
 constexpr int GEMM_B_BYTES = 256 * GEMM_BK * 2;       // 32 KB (BN <= 256)
 constexpr int GEMM_OUT_TOK = 16;                      // tokens per output staging chunk
@@ -483,7 +501,7 @@ struct UnitIter {
 };
 
 template <int T>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(32 * gemm_warps<T>(), 1)
     k_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
            const __grid_constant__ CUtensorMap ymap, const GemmParams p) {
     using F = GemmFmt<T>;
@@ -510,6 +528,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(acc_empty + 3);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int role = T == SYN_F16 ? warp : (int)kGemmRoles[warp];
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < RS; i++) {
@@ -544,7 +563,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         return (int)(st < 4 ? st : 4);
     };
 
-    if (warp == 0 && T == SYN_F16) {
+    if (role == 0 && T == SYN_F16) {
         // ------------------------------ F16 weight tiles ------------------------------
         // 2-D TMA of 128 rows x 64 k of fp16 straight into the A ring (zero fill past
         // n_out / n_in)
@@ -574,7 +593,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // the tiles still in flight (issued, not consumed: only after an abort) land first
         for (uint32_t i = kc > (uint32_t)GEMM_A_STAGES ? kc - GEMM_A_STAGES : 0u; i < kc; i++)
             mbar_drain(smem_u32(&a_full[i % GEMM_A_STAGES]), (i / GEMM_A_STAGES) & 1, p.err);
-    } else if (warp == 0) {
+    } else if (role == 0) {
         // ------------------------------ raw weight producer ------------------------------
         uint32_t rc = 0;
         UnitIter it(p);
@@ -663,7 +682,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // the slices still in flight (issued, not consumed: only after an abort) land first
         for (uint32_t i = rc > (uint32_t)RS ? rc - RS : 0u; i < rc; i++)
             mbar_drain(smem_u32(&raw_full[i % RS]), (i / RS) & 1, p.err);
-    } else if (warp == 2) {
+    } else if (role == 2) {
         // ------------------------------ activation producer ------------------------------
         // x~ is written by the conversion kernel this launch may overlap with: wait for it
         asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -698,7 +717,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // the tiles still in flight (issued, not consumed: only after an abort) land first
         for (uint32_t i = kc > (uint32_t)GEMM_B_STAGES ? kc - GEMM_B_STAGES : 0u; i < kc; i++)
             mbar_drain(smem_u32(&b_full[i % GEMM_B_STAGES]), (i / GEMM_B_STAGES) & 1, p.err);
-    } else if (warp == 1) {
+    } else if (role == 1) {
         // ------------------------------ MMA issuer ------------------------------
         uint32_t kc = 0, ac = 0;
         bool ok = true;
@@ -747,10 +766,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // on the normal path the epilogue has already seen them finish)
         if (kc > 0)
             mbar_drain(smem_u32(&a_empty[(kc - 1) % GEMM_A_STAGES]), ((kc - 1) / GEMM_A_STAGES) & 1, p.err);
-    } else if (warp < GEMM_EPI_WARP0) {
+    } else if (role < GEMM_EPI_WARP0) {
       if (T != SYN_F16) {  // F16: no dequantization, the weights arrive as fp16
         // ------------------------------ dequantize ------------------------------
-        const int dw = warp - GEMM_DEQ_WARP0;
+        const int dw = role - GEMM_DEQ_WARP0;
         const int r = 32 * (dw & 3) + lane;   // row of the tile
         const int h = (dw >> 2) & 1;          // k half of the 64-wide step
         const uint32_t team = (uint32_t)(dw >> 3);
@@ -809,7 +828,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
         }
       }
-    } else {
+    } else if (role != GEMM_ROLE_IDLE) {
         // ------------------------------ epilogue ------------------------------
         // TMEM -> registers (32 columns per load); then either through a per-warp staging
         // buffer of 32 outputs x 16 tokens and one 2-D TMA store (or reduce-add, for split
@@ -1030,7 +1049,7 @@ static cudaError_t run_gemm(GemmParams p, const CUtensorMap& map, const CUtensor
     // producer and the dequantizers start before the conversion has finished
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.blockDim = dim3(32 * gemm_warps<T>());
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
