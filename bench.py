@@ -402,7 +402,7 @@ def gpu_arm(args, rank, world, dist):
                     "api": "per layer syn_mul_mat_batch(q, k, v), syn_mul_mat(o), syn_mul_mat_batch(gate, up), "
                            "syn_mul_mat(down); syn_mul_mat(lm_head)",
                     "roofline": {"bound": "tensor", "kernel": "k_act_half + k_deq_half (fp16 weight expansion, "
-                                                              "at 2048 tokens all products but the Q4_K FFN down) + "
+                                                              "at 2048 tokens the Q6_K products) + "
                                                               "k_gemm (tcgen05 kind::f16): the calls of one layer, "
                                                               "mean over the 32 layers",
                                  "achieved": round(p_layer, 1), "peak": tc_peak, "unit": "TFLOP/s",

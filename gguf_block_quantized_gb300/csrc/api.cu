@@ -48,12 +48,12 @@ int decode_max_tok(int type) {
     return 4;
 }
 
-// Prefill calls of at least this many tokens expand Q4_K / Q6_K weights to fp16 once per
-// product (launch_deq_half) and run the fp16 tensor-core product on them: the fused product
-// expands every weight tile again for each 256-token tile, and at 2048 tokens that costs
-// more than one pass over the weights (measured on GB300: FFN up 14336x4096 219.7 us fused,
-// 170.3 us on fp16 weights + ~25 us expansion; at 1024 tokens about even, at 512 the fused
-// product wins).  syn_set_prefill_expand_tok, or SYN_PREFILL_EXPAND_TOK at load time.
+// Prefill calls of at least this many tokens expand Q6_K weights (Q4_K: twice as many) to
+// fp16 once per product (launch_deq_half) and run the fp16 tensor-core product on them: the
+// fused product expands every weight tile again for each 256-token tile, and from about this
+// size that costs more than one pass over the weights (measured on GB300, 2048 tokens: Q6_K
+// FFN down 4096x14336 275.0 us fused, 252.9 us expanded; at 512 tokens the fused product
+// wins).  syn_set_prefill_expand_tok, or SYN_PREFILL_EXPAND_TOK at load time.
 #ifndef SYN_PREFILL_EXPAND_TOK_DEFAULT
 #define SYN_PREFILL_EXPAND_TOK_DEFAULT 1536
 #endif
@@ -328,11 +328,15 @@ namespace {
 int prefill_group(const syn_mat_desc* const* g, int m, int64_t n_tok, const DeviceState* st, cudaStream_t s) {
     const int64_t n_in = g[0]->n_in;
     const int xt = vec_dot(g[0]->type);
-    // Q4_K rows longer than 8192 are left fused: the FFN down shape (4096 x 14336) measured
-    // 232.5 us fused against 235.0 expanded at 2048 tokens (Q6_K: 281.6 -> 249.0)
+    // Q6_K from the threshold; Q4_K, whose fused expansion is cheaper, from twice it, and rows
+    // longer than 8192 never.  Measured at 2048 tokens (µs, fused / expanded): Q6_K FFN down
+    // 275.0 / 252.9, Q6_K lm_head 2197.5 / 1814.0; Q4_K FFN up 190.2 / 192.8, q 73.6 / 77.0,
+    // FFN down 208.3 / 207.6 at 2048 but 210.7 / 235.0 in another run (the fp16-weight product
+    // of that shape is slow to fill its last wave).
     auto expand = [&](const syn_mat_desc* d) {
-        return n_tok >= g_expand_tok.load() &&
-               (d->type == SYN_TYPE_Q6_K || (d->type == SYN_TYPE_Q4_K && n_in <= 8192));
+        const int64_t t = g_expand_tok.load();
+        return (d->type == SYN_TYPE_Q6_K && n_tok >= t) ||
+               (d->type == SYN_TYPE_Q4_K && n_in <= 8192 && n_tok >= 2 * t);
     };
     const size_t x_bytes = (prefill_ws_bytes(n_in, n_tok) + 255) & ~size_t(255);
     size_t w_bytes = 0;

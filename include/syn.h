@@ -154,9 +154,9 @@ SYN_API int syn_quantize_activations(int wtype, const float* X, int64_t n_tok, i
  * n_tok runs the prefill path: one kernel converts X and writes the dequantized fp16
  * activations into the library workspace, a second runs the tensor-core GEMM on W tiles
  * dequantized to fp16 in shared memory (fp32 accumulation); from 1536 tokens (see
- * syn_set_prefill_expand_tok) Q6_K weights, and Q4_K weights of rows up to 8192 values,
- * are instead expanded to fp16 into the workspace by a launch of their own and the GEMM
- * reads them from there.
+ * syn_set_prefill_expand_tok) Q6_K weights, and from 3072 Q4_K weights of rows up to 8192
+ * values, are instead expanded to fp16 into the workspace by a launch of their own and the
+ * GEMM reads them from there.
  * Accuracy: |y - y_ref| <= 1e-4 * ||dequant(w_row)||_2 * ||x||_2 per element, where
  * y_ref is the same product evaluated in fp64.  W, X, Y: 16-byte aligned, not aliased.
  * n_tok == 0 is a no-op.  Asynchronous.  The prefill path may grow the workspace (see
@@ -251,9 +251,9 @@ SYN_API int syn_set_gemv_max_tok(int n);
  * syn_mul_mat_prefill_static is not affected (it always runs the tensor-core prefill). */
 SYN_API int syn_set_deterministic(int on);
 
-/* Prefill calls (the tensor-core path) of at least n tokens first expand Q6_K weights, and
- * Q4_K weights of rows up to 8192 values, to fp16, once per product, into the library's
- * workspace (n_out * n_in * 2 more bytes, grown on first need like the activation
+/* Prefill calls (the tensor-core path) first expand Q6_K weights from n tokens on, and Q4_K
+ * weights of rows up to 8192 values from 2n tokens on, to fp16, once per product, into the
+ * library's workspace (n_out * n_in * 2 more bytes, grown on first need like the activation
  * workspace), then run the tensor-core product on the fp16 weights; otherwise the product
  * expands each weight tile inside the product kernel, once per tile of up to 256 tokens.  Each expanded value is the fp32 dequantization
  * (syn_dequantize's, bit for bit) rounded once to fp16; the result stays within the
