@@ -268,6 +268,24 @@ int syn_dequantize(int type, const void* src, float* dst, int64_t n_rows, int64_
     return SYN_OK;
 }
 
+int syn_dequantize_f16(int type, const void* src, void* dst, int64_t n_rows, int64_t n_per_row, syn_stream_t stream) {
+    if (type != SYN_TYPE_Q4_K && type != SYN_TYPE_Q6_K) return SYN_ERR_TYPE;
+    if (n_rows < 0 || n_per_row <= 0 || n_per_row % elems(type) || n_rows * n_per_row > kMaxElems)
+        return SYN_ERR_SHAPE;
+    if (n_rows == 0) return SYN_OK;
+    if (!src || !dst) return SYN_ERR_NULL;
+    if (!aligned16(src) || !aligned16(dst)) return SYN_ERR_ALIGN;
+    DeviceState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    const int64_t nblocks = n_rows * (n_per_row / elems(type));
+    if (syn::launch_deq_half(type, src, dst, nblocks, sms_of(st), reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return SYN_ERR_CUDA;
+    g_launches++;
+    return SYN_OK;
+}
+
 int syn_quantize_activations(int wtype, const float* X, int64_t n_tok, int64_t n_in, int8_t* qs, float* d,
                              int16_t* bsums, syn_stream_t stream) {
     if (!is_weight(wtype) || wtype == SYN_TYPE_F16) return SYN_ERR_TYPE;  // F16: syn_quantize(F16, X)

@@ -45,6 +45,7 @@ EXPORTS = [
     ("syn_row_bytes", _i64, [_i32, _i64]),
     ("syn_quantize", _i32, [_i32, _vp, _vp, _i64, _i64, _vp]),
     ("syn_dequantize", _i32, [_i32, _vp, _vp, _i64, _i64, _vp]),
+    ("syn_dequantize_f16", _i32, [_i32, _vp, _vp, _i64, _i64, _vp]),
     ("syn_quantize_activations", _i32, [_i32, _vp, _i64, _i64, _vp, _vp, _vp, _vp]),
     ("syn_mul_mat", _i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     ("syn_reserve", _i32, [_i64, _i64, _vp]),
@@ -177,6 +178,15 @@ def dequantize(t: int, q, n: int, stream=None):
     n_rows = q.numel() // row_bytes(t, n)
     out = torch.empty((n_rows, n), dtype=torch.float32, device=q.device)
     check(syn_dequantize(t, _ptr(q), _ptr(out), n_rows, n, _stream(stream)), "syn_dequantize")
+    return out
+
+
+def dequantize_f16(t: int, q, n: int, stream=None):
+    """Q4_K / Q6_K blocks -> float16 tensor (n_rows, n): syn_dequantize's values rounded to fp16."""
+    torch = _torch()
+    n_rows = q.numel() // row_bytes(t, n)
+    out = torch.empty((n_rows, n), dtype=torch.float16, device=q.device)
+    check(syn_dequantize_f16(t, _ptr(q), _ptr(out), n_rows, n, _stream(stream)), "syn_dequantize_f16")
     return out
 
 

@@ -135,6 +135,13 @@ SYN_API int syn_quantize(int type, const float* src, void* dst, int64_t n_rows, 
 SYN_API int syn_dequantize(int type, const void* src, float* dst, int64_t n_rows, int64_t n_per_row,
                    syn_stream_t stream);
 
+/* The same expansion to fp16 (Q4_K and Q6_K only; SYN_ERR_TYPE for the other formats): dst
+ * gets n_rows * n_per_row IEEE halves, each the value syn_dequantize returns rounded once to
+ * fp16 (to nearest, ties to even).  This is the weight operand the prefill product uses when
+ * it expands weights first (syn_set_prefill_expand_tok).  Asynchronous.  Alignment: 16 B. */
+SYN_API int syn_dequantize_f16(int type, const void* src, void* dst, int64_t n_rows, int64_t n_per_row,
+                               syn_stream_t stream);
+
 /* The activation step of the product on its own (from_float to the vec_dot_type):
  * X (n_tok x n_in fp32) -> codes qs (n_tok x n_in int8), scales d (n_tok x n_in/Bx fp32,
  * Bx = 32 for Q8_0/Q4_0/Q5_0 weights, 256 for K-quant weights; for the 32-blocks the value

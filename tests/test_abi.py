@@ -92,6 +92,11 @@ def test_argument_checks_need_no_gpu(lib):
     assert L.syn_quantize(1, p, p, 0, 32, None) == L.OK
     assert L.syn_quantize(1, p + 8, p, 1, 32, None) == L.ERR_ALIGN
     assert L.syn_dequantize(3, None, p, 1, 256, None) == L.ERR_NULL
+    assert L.syn_dequantize_f16(1, p, p, 1, 256, None) == L.ERR_TYPE   # Q8_0: K-quants only
+    assert L.syn_dequantize_f16(2, p, p, 1, 100, None) == L.ERR_SHAPE
+    assert L.syn_dequantize_f16(3, None, p, 1, 256, None) == L.ERR_NULL
+    assert L.syn_dequantize_f16(2, p + 2, p, 1, 256, None) == L.ERR_ALIGN
+    assert L.syn_dequantize_f16(2, p, p, 0, 256, None) == L.OK
     assert L.syn_quantize_activations(4, p, 1, 256, p, p, p, None) == L.ERR_TYPE
     assert L.syn_quantize_activations(2, p, 1, 256, p, p, None, None) == L.ERR_NULL
     assert L.syn_block_sums(2, p, 1, 300, p, 1, p, None) == L.ERR_SHAPE

@@ -105,6 +105,29 @@ def test_dequantize_bit_exact(syn, t):
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
 
 
+@pytest.mark.parametrize("t", [oracle.Q4_K, oracle.Q6_K])
+def test_dequantize_f16_bit_exact(syn, t):
+    """The fp16 expansion (the prefill's expanded weight operand): every value the oracle's
+    fp32 dequantization rounded once to fp16, bit for bit, on quantized rows and on blocks of
+    arbitrary bytes (every code, scale and sign pattern; non-finite halves left out)."""
+    n_rows, n = 37, 2048
+    Wq = oracle.quantize(t, synth.normal(1700 + t, (n_rows, n), 0.02))
+    rng = np.random.default_rng(1710 + t)
+    raw = rng.integers(0, 256, Wq.shape, dtype=np.uint8)
+    bb = oracle.BLOCK_BYTES[t]
+    blocks = raw.reshape(-1, bb)
+    # keep the fp16 scales finite and small enough that no value overflows fp16
+    d_off = (0,) if t == oracle.Q4_K else (208,)
+    for o in d_off + ((2,) if t == oracle.Q4_K else ()):
+        h = (rng.standard_normal(blocks.shape[0]) * 1e-3).astype(np.float16).view(np.uint8).reshape(-1, 2)
+        blocks[:, o:o + 2] = h
+    for W in (Wq, raw):
+        ref = oracle.dequantize(t, W, n).astype(np.float32).astype(np.float16)
+        got = host(syn.dequantize_f16(t, dev(W), n))
+        assert np.array_equal(got.view(np.uint16), ref.view(np.uint16))
+    assert syn.device_status() == syn.OK
+
+
 @pytest.mark.parametrize("t", [oracle.Q4_K, oracle.Q6_K, oracle.Q8_0, oracle.Q4_0, oracle.Q5_0])
 def test_dequantize_arbitrary_codes_bit_exact(syn, t):
     """Random block bytes (finite fp16 scales), including negative Q6_K scales."""
