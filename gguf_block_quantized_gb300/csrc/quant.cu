@@ -645,7 +645,22 @@ cudaError_t launch_dequantize(int type, const void* src, float* dst, int64_t n_b
 }
 
 cudaError_t launch_deq_half(int type, const void* src, void* dst, int64_t n_blocks, int sms, cudaStream_t s) {
-    const int g = grid_for((n_blocks + DEQ_U - 1) / DEQ_U, sms);
+    // one wave of CTAs: as many per SM as are resident at once (the grid-stride loop does the
+    // rest; a second, partial wave would leave SMs idle at its end)
+    static std::atomic<int> per_sm_cache[2];  // 0: not known yet
+    const int which = type == SYN_Q4_K ? 0 : 1;
+    int per_sm = per_sm_cache[which].load();
+    if (per_sm == 0) {
+        int n = 0;
+        const cudaError_t e = which == 0
+            ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_deq_half<SYN_Q4_K>, 256, 0)
+            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_deq_half<SYN_Q6_K>, 256, 0);
+        per_sm = (e == cudaSuccess && n > 0) ? n : 4;
+        per_sm_cache[which].store(per_sm);
+    }
+    int64_t ctas = ((n_blocks + DEQ_U - 1) / DEQ_U + 7) / 8;
+    if (ctas > (int64_t)sms * per_sm) ctas = (int64_t)sms * per_sm;
+    const int g = ctas < 1 ? 1 : (int)ctas;
     const uint8_t* p = static_cast<const uint8_t*>(src);
     __half* h = static_cast<__half*>(dst);
     switch (type) {
