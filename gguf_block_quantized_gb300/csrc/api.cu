@@ -168,6 +168,7 @@ int workspace_for(cudaStream_t s, size_t need, void** out) {
             w.bytes = 0;
         }
         if (cudaMalloc(&w.ptr, need) != cudaSuccess) {
+            (void)cudaGetLastError();  // not sticky: keep it out of the next launch check
             w.ptr = nullptr;
             return SYN_ERR_NOMEM;
         }
@@ -351,10 +352,11 @@ int prefill_group(const syn_mat_desc* const* g, int m, int64_t n_tok, const Devi
     // 275.0 / 252.9, Q6_K lm_head 2197.5 / 1814.0; Q4_K FFN up 190.2 / 192.8, q 73.6 / 77.0,
     // FFN down 208.3 / 207.6 at 2048 but 210.7 / 235.0 in another run (the fp16-weight product
     // of that shape is slow to fill its last wave).
+    bool room = true;  // false: the workspace could not take the expanded weights
     auto expand = [&](const syn_mat_desc* d) {
         const int64_t t = g_expand_tok.load();
-        return (d->type == SYN_TYPE_Q6_K && n_tok >= t) ||
-               (d->type == SYN_TYPE_Q4_K && n_in <= 8192 && n_tok >= 2 * t);
+        return room && ((d->type == SYN_TYPE_Q6_K && n_tok >= t) ||
+                        (d->type == SYN_TYPE_Q4_K && n_in <= 8192 && n_tok >= 2 * t));
     };
     const size_t x_bytes = (prefill_ws_bytes(n_in, n_tok) + 255) & ~size_t(255);
     size_t w_bytes = 0;
@@ -362,6 +364,12 @@ int prefill_group(const syn_mat_desc* const* g, int m, int64_t n_tok, const Devi
         if (expand(g[i])) w_bytes = std::max(w_bytes, (size_t)(g[i]->n_out * n_in) * 2);
     void* ws;
     int rc = workspace_for(s, x_bytes + w_bytes, &ws);
+    if (rc == SYN_ERR_NOMEM && w_bytes > 0) {
+        // no room for the expanded weights: the fused product needs only x~
+        w_bytes = 0;
+        room = false;
+        rc = workspace_for(s, x_bytes, &ws);
+    }
     if (rc) return rc;
     void* wh = static_cast<uint8_t*>(ws) + x_bytes;
     for (int i = 0; i < m; i++)
