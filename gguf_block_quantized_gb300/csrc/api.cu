@@ -222,6 +222,15 @@ int syn_set_gemv_max_tok(int n) { return g_gemv_max_tok.exchange(n < 0 ? -1 : n)
 
 int syn_set_deterministic(int on) { return g_det.exchange(on ? 1 : 0); }
 
+int syn_debug_prefill_plan(int64_t n_out, int64_t n_in, int64_t n_tok, int sms, int* out) {
+    if (n_out <= 0 || n_in <= 0 || n_tok <= 0 || sms <= 0 || n_out > (int64_t(1) << 31) || n_in > kMaxElems ||
+        n_tok > kMaxElems)
+        return SYN_ERR_SHAPE;
+    if (!out) return SYN_ERR_NULL;
+    syn::gemm_plan(n_out, n_in, n_tok, sms, out);
+    return SYN_OK;
+}
+
 int syn_set_prefill_expand_tok(int n) { return g_expand_tok.exchange(n < 0 ? kPrefillExpandTok : n); }
 
 int syn_set_sm_limit(int n) {

@@ -1069,6 +1069,18 @@ static SplitPlan plan_of(int64_t n_out, int64_t n_in, int64_t n_tok, int sms) {
     return pick_split(n_m, n_n, n_super, sms, bn, n_out, n_tok);
 }
 
+// The schedule the prefill product takes (host only): out[0] = S (K split of the split
+// tiles, 1: none), out[1] = m_full (row tiles run whole), out[2] = 1 for stream-K (the tiles of
+// row tiles >= m_full shared), out[3] = the number of tiles.
+void gemm_plan(int64_t n_out, int64_t n_in, int64_t n_tok, int sms, int out[4]) {
+    const SplitPlan sp = plan_of(n_out, n_in, n_tok, sms);
+    const int bn = gemm_bn(n_tok);
+    out[0] = sp.S;
+    out[1] = sp.m_full;
+    out[2] = sp.streamk ? 1 : 0;
+    out[3] = (int)(((n_out + GEMM_BM - 1) / GEMM_BM) * ((n_tok + bn - 1) / bn));
+}
+
 // Zero the columns of Y that the product's split tiles add into (none when it does not
 // split): to be enqueued before the activation conversion (the product kernel overlaps it).
 cudaError_t gemm_zero_y(float* Y, int64_t n_out, int64_t n_in, int64_t n_tok, int sms, cudaStream_t s) {

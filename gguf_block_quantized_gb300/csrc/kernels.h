@@ -51,6 +51,8 @@ int sm_limit();
 cudaError_t launch_gemm(int type, const void* W, int64_t n_out, int64_t n_in, const void* xh,
                         int64_t n_tok, float* Y, int* err, int sms, cudaStream_t s);
 cudaError_t gemm_zero_y(float* Y, int64_t n_out, int64_t n_in, int64_t n_tok, int sms, cudaStream_t s);
+// The prefill schedule of a product (host only): {S, m_full, stream-K, tiles}.
+void gemm_plan(int64_t n_out, int64_t n_in, int64_t n_tok, int sms, int out[4]);
 
 // F16 weights (n_in % 8 == 0): X -> fp16 (round to nearest even) into xh, and the decode
 // product reading W and the fp16 activations from ws (n_tok * n_in halves).

@@ -59,6 +59,7 @@ EXPORTS = [
     ("syn_set_deterministic", _i32, [_i32]),
     ("syn_set_sm_limit", _i32, [_i32]),
     ("syn_set_prefill_expand_tok", _i32, [_i32]),
+    ("syn_debug_prefill_plan", _i32, [_i64, _i64, _i64, _i32, ctypes.POINTER(ctypes.c_int)]),
     ("syn_debug_bounds_selftest", _i32, [_vp]),
 ]
 

@@ -231,6 +231,14 @@ SYN_API int syn_release(void);
 SYN_API int syn_block_sums(int type, const void* W, int64_t n_out, int64_t n_in,
                    const void* Xq, int64_t n_tok, int32_t* S, syn_stream_t stream);
 
+/* The tile schedule the prefill product picks for a shape on sms SMs (host only, no device
+ * needed; for checks of the planner): out[0] = the K split S of split tiles (1: none),
+ * out[1] = the row tiles (of 128 outputs) that run whole tiles, out[2] = 1 when the other row
+ * tiles' tiles are shared stream-K (equal super-step ranges per CTA) instead of split S ways,
+ * out[3] = the number of 128 x BN tiles (BN = n_tok rounded up to 16, at most 256).
+ * SYN_ERR_SHAPE for non-positive sizes or sms, SYN_ERR_NULL for out. */
+SYN_API int syn_debug_prefill_plan(int64_t n_out, int64_t n_in, int64_t n_tok, int sms, int* out);
+
 /* Decode/prefill threshold.  By default (n < 0) it depends on the format: products with
  * n_tok <= 8 (Q4_K, Q6_K), <= 4 (Q8_0, Q4_0, Q5_0) or <= 2 (F16) use the decode kernels,
  * larger ones the tensor-core prefill (the measured crossovers on GB300).  n >= 0 sets the
